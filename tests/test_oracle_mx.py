@@ -1,0 +1,207 @@
+"""Pins for the oracle's MXFP8 codec and quantizer against things other than
+itself: hand-worked blocks, an exhaustive sweep against torch's float8_e4m3fn
+cast, the half-ulp error bound, bf16 rounding against torch, and the scale
+layout's definition.  CPU only."""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import mx
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "mx_blocks.txt")
+
+
+def _parse_value(s):
+    s = s.strip()
+    if s in ("nan", "inf", "-inf"):
+        return float(s)
+    if "0x" in s:
+        return float.fromhex(s)
+    return float(s)
+
+
+def _golden_cases():
+    cases = []
+    for line in open(GOLDEN):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        name, scale, vals, codes = [p.strip() for p in line.split(";")]
+        v = np.zeros(32)
+        for tok in vals.split():
+            pos, val = tok.split("=")
+            v[int(pos)] = _parse_value(val)
+        exp = np.zeros(32, dtype=np.uint8)
+        for tok in codes.split():
+            pos, c = tok.split("=")
+            if pos == "*":
+                exp[:] = int(c, 16)
+            else:
+                exp[int(pos)] = int(c, 16)
+        cases.append((name, v, int(scale, 16), exp))
+    return cases
+
+
+@pytest.mark.parametrize("name,v,scale,codes", _golden_cases(), ids=lambda c: c if isinstance(c, str) else "")
+def test_hand_worked_blocks(name, v, scale, codes):
+    # every value in the fixture is exactly representable in bf16
+    bits = torch.tensor(v, dtype=torch.float32).to(torch.bfloat16)
+    assert np.array_equal(np.nan_to_num(bits.float().numpy().astype(np.float64), nan=7.0),
+                          np.nan_to_num(v, nan=7.0)), name
+    q, s = mx.quantize_blocks(v)
+    assert int(s) == scale, (name, hex(int(s)))
+    assert np.array_equal(q, codes), (name, [hex(c) for c in q])
+
+
+def test_golden_fixture_is_nontrivial():
+    assert len(_golden_cases()) >= 12
+
+
+def test_decode_encode_roundtrip_all_codes():
+    codes = np.arange(256, dtype=np.uint8)
+    vals = mx.e4m3_decode(codes)
+    finite = ~np.isnan(vals)
+    back = mx.e4m3_encode(vals[finite])
+    assert np.array_equal(back, codes[finite])
+    # 0x7F / 0xFF are the only NaNs; max finite is 448
+    assert np.sum(~finite) == 2
+    assert np.nanmax(vals) == 448.0 and mx.e4m3_decode(np.uint8(0x01)) == 2.0 ** -9
+
+
+def test_decode_against_torch():
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    t = codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    o = mx.e4m3_decode(codes.numpy())
+    assert np.array_equal(np.isnan(t), np.isnan(o))
+    assert np.array_equal(t[~np.isnan(t)], o[~np.isnan(o)])
+
+
+def test_e8m0_decode():
+    b = np.arange(255, dtype=np.uint8)
+    assert np.array_equal(mx.e8m0_decode(b), np.ldexp(1.0, b.astype(np.int64) - 127))
+    assert np.isnan(mx.e8m0_decode(np.uint8(255)))
+    ref = torch.arange(255, dtype=torch.int32).to(torch.uint8).view(torch.float8_e8m0fnu).to(torch.float64).numpy()
+    assert np.array_equal(ref, mx.e8m0_decode(b))
+
+
+def _all_finite_bf16():
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    v = mx.bf16_to_f64(bits)
+    return v[np.isfinite(v)]
+
+
+def test_exhaustive_cast_vs_torch():
+    """Every finite bf16 value v, scaled by every exponent at which v can sit in
+    a block (from being its amax down to below the E4M3 subnormals), cast by
+    the oracle and by torch's float8_e4m3fn conversion (an RNE cast that does
+    not saturate, hence the clamp to +-448 on torch's side)."""
+    v = _all_finite_bf16()
+    v = v[v != 0]
+    fl = mx.floor_log2(np.abs(v))
+    for d in range(-8, 12):
+        e = fl + d
+        r = np.ldexp(v, -e)
+        ours = mx.e4m3_encode(r)
+        ref = torch.from_numpy(np.clip(r, -448.0, 448.0).astype(np.float32)) \
+            .to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+        assert np.array_equal(ours, ref), d
+
+
+def test_half_ulp_bound_and_saturation():
+    g = np.random.default_rng(7)
+    v = g.standard_normal((4096, 32)) * np.where(g.random((4096, 32)) < 0.05, 100.0, 1.0)
+    v *= np.ldexp(1.0, g.integers(-40, 40, size=(4096, 1)))
+    v = mx.bf16_to_f64(mx.f64_to_bf16_bits(v))
+    q, s = mx.quantize_blocks(v)
+    e = s.astype(np.int64) - 127
+    scale = np.ldexp(1.0, e)[:, None]
+    vhat = mx.e4m3_decode(q) * scale
+    r = v / scale
+    sat = np.abs(r) > 448
+    # grid step at |r| (its binade), in scaled units
+    _, ex = np.frexp(np.abs(r))
+    step = np.ldexp(1.0, np.maximum(ex - 1, -6) - 3)
+    err = np.abs(v - vhat)
+    assert np.all(err[~sat] <= 0.5 * (step * scale)[~sat])
+    assert np.all(err[sat] < 64 * np.broadcast_to(scale, v.shape)[sat])
+    # the block amax never lands below 256 * 2^e: it encodes in the top binade
+    amax_code = np.max(q & 0x7F, axis=1)
+    assert np.all(amax_code >= 0x78)
+
+
+def test_quantize_rows_cols_relation():
+    g = np.random.default_rng(3)
+    x = mx.bf16_to_f64(mx.f64_to_bf16_bits(g.standard_normal((64, 96))))
+    qc, sc = mx.quantize_cols(x)
+    qr, sr = mx.quantize_rows(x.T.copy())
+    assert qc.shape == (96, 64) and sc.shape == (96, 2)
+    assert np.array_equal(qc, qr) and np.array_equal(sc, sr)
+    # a column block by hand: rows 0..31 of column 5
+    q5, s5 = mx.quantize_blocks(x[0:32, 5])
+    assert np.array_equal(qc[5, 0:32], q5) and sc[5, 0] == s5
+
+
+def test_f32_to_bf16_vs_torch():
+    g = np.random.default_rng(1)
+    x = (g.standard_normal(200000) * np.ldexp(1.0, g.integers(-130, 120, 200000))).astype(np.float32)
+    # exact ties: bf16 value + half an ulp
+    base = mx.bf16_to_f64(g.integers(0, 0x7F00, 2000).astype(np.uint16)).astype(np.float32)
+    ties = (base.view(np.uint32) | np.uint32(0x8000)).view(np.float32)
+    x = np.concatenate([x, ties, -ties, np.array([0.0, -0.0, np.inf, -np.inf], np.float32)])
+    ref = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(mx.f32_to_bf16_bits(x), ref)
+
+
+def test_f64_to_bf16_single_rounding():
+    g = np.random.default_rng(2)
+    x = g.standard_normal(100000) * np.ldexp(1.0, g.integers(-60, 60, 100000))
+    b = mx.f64_to_bf16_bits(x)
+    # values exactly representable in fp32 must agree with torch's fp32 -> bf16
+    x32 = x.astype(np.float32).astype(np.float64)
+    ref = torch.from_numpy(x32.astype(np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(mx.f64_to_bf16_bits(x32), ref)
+    # nearest: no neighbouring bf16 is closer
+    v = mx.bf16_to_f64(b)
+    up = mx.bf16_to_f64((b.astype(np.int64) + 1).astype(np.uint16))
+    dn = mx.bf16_to_f64((b.astype(np.int64) - 1).astype(np.uint16))
+    assert np.all(np.abs(x - v) <= np.abs(x - up)) and np.all(np.abs(x - v) <= np.abs(x - dn))
+    # a tie that fp32 would break the wrong way: 1 + 2^-8 + 2^-40 is above the
+    # midpoint of 1 and 1 + 2^-7, so it rounds up; through fp32 it would land
+    # on the midpoint and then round to even (down)
+    t = 1.0 + 2.0 ** -8 + 2.0 ** -40
+    assert mx.bf16_to_f64(mx.f64_to_bf16_bits(np.array([t])))[0] == 1.0 + 2.0 ** -7
+
+
+def test_swizzle_layout_definition():
+    # hand positions from the tile definition
+    assert mx.swizzled_offset(0, 0, 8) == 0
+    assert mx.swizzled_offset(1, 0, 8) == 16
+    assert mx.swizzled_offset(32, 0, 8) == 4
+    assert mx.swizzled_offset(33, 2, 8) == 16 + 4 + 2
+    assert mx.swizzled_offset(127, 3, 8) == 31 * 16 + 3 * 4 + 3
+    assert mx.swizzled_offset(0, 5, 8) == 512 + 1
+    assert mx.swizzled_offset(128, 0, 8) == 2 * 512
+    # bijection onto the padded buffer
+    rows, cols = 256, 12
+    rr, cc = np.meshgrid(np.arange(rows), np.arange(cols), indexing="ij")
+    off = mx.swizzled_offset(rr, cc, cols).ravel()
+    assert np.array_equal(np.sort(off), np.arange(rows * cols))
+    s = np.random.default_rng(0).integers(0, 255, (rows, cols)).astype(np.uint8)
+    assert np.array_equal(mx.unswizzle_scales(mx.swizzle_scales(s), rows, cols), s)
+    # ragged: padding bytes are zero
+    s2 = np.full((130, 5), 7, np.uint8)
+    flat = mx.swizzle_scales(s2)
+    assert flat.size == 256 * 8 and int(flat.sum()) == 7 * 130 * 5
+
+
+def test_margins_identify_decision_points():
+    # an element exactly on a rounding midpoint has margin 0; a power-of-two
+    # amax has block margin 0
+    v = np.zeros((1, 32))
+    v[0, 0] = 1.0
+    v[0, 1] = 17 / 256
+    el, bl = mx.quantize_margins(v)
+    assert el[0, 1] == 0.0 and bl[0, 0] == 0.0
+    assert el[0, 0] > 0
