@@ -1,0 +1,484 @@
+"""Benchmark of the MXFP8 MoE layer training step on GB300.
+
+One step = the whole hot path over one batch of the full-layer workload
+(T=16384 tokens, H=5120, E=16 experts, FFN F=8192, top-1 softmax router on
+N(0,1) logits): MXFP8 weight quantization (both layouts of W1|W3 and W2),
+router, grouping map, fused quantize+permute, GEMM1 with fused SwiGLU, GEMM2,
+combine, and the backward (gate gradient, gradient shuffle+quantize, dgrad2,
+SwiGLU backward+quantize, wgrad2, dgrad1, input column quantize, wgrad1,
+combine).  Metric: MoE layer fwd+bwd TFLOP/s (algorithmic GEMM FLOPs of the
+real routed rows) and, on its own workload, MXFP8 quantize GB/s.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Under torchrun (N > 1) every rank runs the same single-GPU step on its own
+GPU (replicas: the path has no exchange step), timed between barriers, and
+rank 0 prints one JSON line with the max time over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "MoE layer fwd+bwd TFLOP/s (MXFP8 grouped GEMM) and quantize GB/s, 1 GB300"
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+FP8_PER_BF16 = 2.0   # nominal dense fp8 / bf16 tensor rate (4.5 / 2.25 PFLOP/s)
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            d = json.load(open(p))
+            return d, "measured"
+        except Exception:
+            pass
+    return FALLBACK, "fallback"
+
+
+def _peak_val(d, *keys):
+    for k in keys:
+        if k in d and isinstance(d[k], (int, float)):
+            return float(d[k])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------
+# the step, launch by launch (the same C-ABI calls moe_layer_fwd/bwd make), on
+# preallocated buffers, with CUDA events between launches
+# ----------------------------------------------------------------------------
+class LayerStep:
+    def __init__(self, d, inp, dev):
+        import mxfp8_mixture_experts_gb300 as m
+        self.m = m
+        self.L = m.lib()
+        self.d = d
+        self.dev = dev
+        T, H, F, E, k = d.T, d.H, d.F, d.E, d.k
+        R = m.moe_rows_cap(T, k, E)
+        self.R = R
+        sb = lambda r, c: m.mx_scale_bytes(r, c, 1)
+        u8 = lambda n: torch.empty(int(n), dtype=torch.uint8, device=dev)
+        self.inp = inp
+        self.W13 = torch.cat([inp["W1"], inp["W3"]], dim=2).contiguous()
+        self.W2 = inp["W2"]
+        b = {}
+        b["w13_rq"], b["w13_rs"] = u8(E * H * 2 * F), u8(sb(E * H, 2 * F))
+        b["w13_cq"], b["w13_cs"] = u8(E * 2 * F * H), u8(sb(E * 2 * F, H))
+        b["w2_rq"], b["w2_rs"] = u8(E * F * H), u8(sb(E * F, H))
+        b["w2_cq"], b["w2_cs"] = u8(E * H * F), u8(sb(E * H, F))
+        b["ids"] = torch.empty((T, k), dtype=torch.int32, device=dev)
+        b["gate"] = torch.empty((T, k), dtype=torch.float32, device=dev)
+        b["counts"] = torch.empty(E, dtype=torch.int32, device=dev)
+        b["off"] = torch.empty(E + 1, dtype=torch.int32, device=dev)
+        b["dst"] = torch.empty(T * k, dtype=torch.int32, device=dev)
+        b["src"] = torch.empty(R, dtype=torch.int32, device=dev)
+        self.map_ws_bytes = int(self.L.moe_permute_map_workspace_size(T, k, E))
+        b["map_ws"] = u8(max(self.map_ws_bytes, 16))
+        b["xq"], b["xs"] = u8(R * H), u8(sb(R, H))
+        b["ab"] = torch.empty((R, 2 * F), dtype=torch.bfloat16, device=dev)
+        b["hq"], b["hs"] = u8(R * F), u8(sb(R, F))
+        b["y"] = torch.empty((R, H), dtype=torch.bfloat16, device=dev)
+        b["out"] = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+        b["d_gate"] = torch.empty((T, k), dtype=torch.float32, device=dev)
+        b["dy_rq"], b["dy_rs"] = u8(R * H), u8(sb(R, H))
+        b["dy_cq"], b["dy_cs"] = u8(H * R), u8(sb(H, R))
+        b["dh"] = torch.empty((R, F), dtype=torch.float32, device=dev)
+        b["dab_rq"], b["dab_rs"] = u8(R * 2 * F), u8(sb(R, 2 * F))
+        b["dab_cq"], b["dab_cs"] = u8(2 * F * R), u8(sb(2 * F, R))
+        b["h_cq"], b["h_cs"] = u8(F * R), u8(sb(F, R))
+        b["dW2"] = torch.empty((E, F, H), dtype=torch.float32, device=dev)
+        b["dxp"] = torch.empty((R, H), dtype=torch.bfloat16, device=dev)
+        b["xp_cq"], b["xp_cs"] = u8(H * R), u8(sb(H, R))
+        b["dW13"] = torch.empty((E, H, 2 * F), dtype=torch.float32, device=dev)
+        b["dX"] = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+        b["status"] = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.b = b
+        self.p = {n: t.data_ptr() for n, t in b.items()}
+        # (name, kind, algorithmic work) of every launch, in order
+        self.launches = []
+
+    def run(self, stream, events=None):
+        """Enqueue one step; if ``events`` is a list, record an event after
+        every launch (events[0] before the first)."""
+        L, p, d, m = self.L, self.p, self.d, self.m
+        T, H, F, E, k, R = d.T, d.H, d.F, d.E, d.k, self.R
+        s = stream.cuda_stream
+        x = self.inp["x"].data_ptr()
+        dOut = self.inp["dOut"].data_ptr()
+        logits = self.inp["logits"].data_ptr()
+        st = p["status"]
+        ev = events
+
+        def mark():
+            if ev is not None:
+                e = torch.cuda.Event(enable_timing=True)
+                e.record(stream)
+                ev.append(e)
+
+        def chk(code, what):
+            if code != 0:
+                raise RuntimeError(f"{what}: {L.mx_status_string(code).decode()}")
+
+        mark()
+        chk(L.mx_quantize(self.W13.data_ptr(), E, H, 2 * F, 3, 1, p["w13_rq"], p["w13_rs"], p["w13_cq"], p["w13_cs"], s), "q W13"); mark()
+        chk(L.mx_quantize(self.W2.data_ptr(), E, F, H, 3, 1, p["w2_rq"], p["w2_rs"], p["w2_cq"], p["w2_cs"], s), "q W2"); mark()
+        chk(L.moe_route(logits, T, E, k, p["ids"], p["gate"], s), "route"); mark()
+        chk(L.moe_permute_map(p["ids"], T, k, E, R, p["counts"], p["off"], p["dst"], p["src"], p["map_ws"],
+                              self.map_ws_bytes, st, s), "map"); mark()
+        chk(L.moe_permute(2, x, None, T, H, k, p["dst"], p["src"], R, p["xq"], p["xs"], 1, s), "permute"); mark()
+        chk(L.moe_gemm1_swiglu(p["xq"], p["xs"], p["w13_cq"], p["w13_cs"], p["off"], E, R, F, H, p["ab"], p["hq"],
+                               p["hs"], st, s), "gemm1"); mark()
+        chk(L.mx_grouped_gemm(0, p["hq"], p["hs"], p["w2_cq"], p["w2_cs"], p["off"], E, R, H, F, p["y"], 0, st, s),
+            "gemm2"); mark()
+        chk(L.moe_unpermute(p["y"], p["dst"], p["gate"], T, H, k, p["out"], s), "combine"); mark()
+        chk(L.moe_gate_grad(dOut, p["y"], p["dst"], T, H, k, p["d_gate"], s), "gate grad"); mark()
+        chk(L.moe_gather_quant(dOut, p["gate"], p["src"], T, H, k, R, 3, p["dy_rq"], p["dy_rs"], p["dy_cq"],
+                               p["dy_cs"], s), "dY quant"); mark()
+        chk(L.mx_grouped_gemm(1, p["dy_rq"], p["dy_rs"], p["w2_rq"], p["w2_rs"], p["off"], E, R, F, H, p["dh"], 1, st,
+                              s), "dgrad2"); mark()
+        chk(L.moe_swiglu_bwd(p["dh"], p["ab"], R, F, p["dab_rq"], p["dab_rs"], p["dab_cq"], p["dab_cs"], p["h_cq"],
+                             p["h_cs"], s), "swiglu bwd"); mark()
+        chk(L.mx_grouped_gemm(2, p["h_cq"], p["h_cs"], p["dy_cq"], p["dy_cs"], p["off"], E, R, F, H, p["dW2"], 1, st,
+                              s), "wgrad2"); mark()
+        chk(L.mx_grouped_gemm(1, p["dab_rq"], p["dab_rs"], p["w13_rq"], p["w13_rs"], p["off"], E, R, H, 2 * F,
+                              p["dxp"], 0, st, s), "dgrad1"); mark()
+        chk(L.moe_gather_quant(x, None, p["src"], T, H, k, R, 2, None, None, p["xp_cq"], p["xp_cs"], s), "x col quant"); mark()
+        chk(L.mx_grouped_gemm(2, p["xp_cq"], p["xp_cs"], p["dab_cq"], p["dab_cs"], p["off"], E, R, H, 2 * F,
+                              p["dW13"], 1, st, s), "wgrad1"); mark()
+        chk(L.moe_unpermute(p["dxp"], p["dst"], None, T, H, k, p["dX"], s), "combine dX"); mark()
+
+    NAMES = ["quantize W13", "quantize W2", "route", "map", "permute+quant", "gemm1+swiglu", "gemm2", "combine",
+             "gate grad", "dY gather+quant", "dgrad2", "swiglu bwd", "wgrad2", "dgrad1", "x col quant", "wgrad1",
+             "combine dX"]
+    # our kernel launches per entry (the map is three kernels)
+    KERNELS = [1, 1, 1, 3, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1]
+
+
+def _gemm_flops(d, routed):
+    T, H, F = routed, d.H, d.F
+    g1 = 2 * T * H * 2 * F
+    g2 = 2 * T * F * H
+    return {"gemm1+swiglu": g1, "gemm2": g2, "dgrad2": g2, "wgrad2": g2, "dgrad1": g1, "wgrad1": g1}
+
+
+def _quant_bench(dev, iters=20):
+    """MXFP8 quantize, BOTH mode, bf16 [16384, 7168] with swizzled scales."""
+    import mxfp8_mixture_experts_gb300 as m
+    R, C = workloads.QUANTIZE_SHAPE
+    x = workloads.quantize_input(R, C, seed=0, device=dev)
+    outs = [torch.empty(R * C, dtype=torch.uint8, device=dev) for _ in range(2)]
+    sc = [torch.empty(m.mx_scale_bytes(R, C, 1), dtype=torch.uint8, device=dev) for _ in range(2)]
+    L = m.lib()
+    s = torch.cuda.current_stream(dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    times = []
+    for i in range(iters + 3):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        code = L.mx_quantize(x.data_ptr(), 1, R, C, 3, 1, outs[0].data_ptr(), sc[0].data_ptr(), outs[1].data_ptr(),
+                             sc[1].data_ptr(), s.cuda_stream)
+        e1.record(s)
+        assert code == 0
+        torch.cuda.synchronize()
+        if i >= 3:
+            times.append(e0.elapsed_time(e1) * 1e-3)
+    t = statistics.median(times)
+    nbytes = R * C * 2 + 2 * (R * C + R * C // 32)
+    return {"GB/s": nbytes / t / 1e9, "us": t * 1e6, "bytes": nbytes, "l2": "flushed (256 MiB write) before each launch"}
+
+
+def _cpu_baseline(d_full, seconds_hint=20.0):
+    """The oracle (numpy, fp64) on a bounded sample of the full-layer workload:
+    one expert at the full hidden size H, a 512-wide slice of its FFN width
+    (W1/W3 columns and W2 rows, quantized both ways as a step does) and 128
+    routed tokens, through forward and backward.  Returns TFLOP/s over the
+    GEMM FLOPs of the sample."""
+    from oracle import moe
+    n, f_s = 256, 1024
+    d = workloads.LayerDims(T=n, H=d_full.H, E=1, F=f_s, k=1)
+    g = workloads.generator(0, "cpu")
+    x = workloads.randn_bf16((n, d.H), 1.0, g, "cpu")
+    W1 = workloads.randn_bf16((1, d.H, d.F), 0.02, g, "cpu")
+    W3 = workloads.randn_bf16((1, d.H, d.F), 0.02, g, "cpu")
+    W2 = workloads.randn_bf16((1, d.F, d.H), 0.02, g, "cpu")
+    dOut = workloads.randn_bf16((n, d.H), 1.0, g, "cpu")
+    ids = np.zeros((n, 1), np.int32)
+    gate = np.ones((n, 1), np.float32)
+    bits = {k_: workloads.bf16_bits(v) for k_, v in dict(x=x, W1=W1, W3=W3, W2=W2, dOut=dOut).items()}
+    t0 = time.perf_counter()
+    f = moe.layer_forward(bits["x"], bits["W1"], bits["W3"], bits["W2"], ids, gate, quant=True)
+    moe.layer_backward(f, bits["x"], bits["W1"], bits["W3"], bits["W2"], bits["dOut"])
+    t = time.perf_counter() - t0
+    flops = moe.layer_flops(n, d.H, d.F)["total"]
+    cores = len(os.sched_getaffinity(0))
+    return {"value": flops / t / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"oracle layer fwd+bwd (numpy fp64, MXFP8 semantics): one expert, H={d.H}, a {f_s}-wide "
+                      f"slice of F={d_full.F} (weights quantized both ways), {n} routed tokens; {t:.1f} s",
+            "seconds": t}
+
+
+def _dist():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    rank, world, local = _dist()
+
+    dims = workloads.FULL_LAYER
+    config = {"workload": f"full MoE SwiGLU layer fwd+bwd: T={dims.T} tokens, H={dims.H}, E={dims.E} experts, "
+                          f"F={dims.F}, top-{dims.k} softmax router on N(0,1) logits, MXFP8 on all expert GEMMs",
+              "T": dims.T, "H": dims.H, "E": dims.E, "F": dims.F, "k": dims.k,
+              "l2": "inputs larger than L2 (weights 4 GB, activations 168 MB per tensor); no flush",
+              "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"}
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        vals = []
+        for i in range(args.warmup + args.steps):
+            r = _cpu_baseline(dims)
+            if i >= args.warmup:
+                vals.append(r)
+        v = statistics.median([r["value"] for r in vals])
+        secs = sum(r["seconds"] for r in vals)
+        line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOP/s", "n_gpus": 1,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / len(vals),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic (seeded)", "config": config,
+                "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": vals[0]["cores"], "kind": "oracle",
+                                 "sample": vals[0]["sample"]},
+                "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    import mxfp8_mixture_experts_gb300 as m
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    d = m.MoELayerDims(T=dims.T, H=dims.H, F=dims.F, E=dims.E, k=dims.k)
+    inp = workloads.layer_inputs(dims, seed=rank, device=dev, router="logits")
+    step = LayerStep(d, inp, dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        step.run(stream)
+    torch.cuda.synchronize()
+    assert int(step.b["status"].item()) == 0, "device status set during warm-up"
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier()
+    torch.cuda.synchronize()
+    all_events = []
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(args.steps):
+        evs = []
+        step.run(stream, evs)
+        all_events.append(evs)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clk = clocks.stop()
+    elapsed = t0.elapsed_time(t1) * 1e-3
+    if world > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([elapsed], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        elapsed = float(tt.item())
+    assert int(step.b["status"].item()) == 0, "device status set during the timed steps"
+
+    per = {n: [] for n in LayerStep.NAMES}
+    for evs in all_events:
+        for i, n in enumerate(LayerStep.NAMES):
+            per[n].append(evs[i].elapsed_time(evs[i + 1]) * 1e-3)
+    avg = {n: sum(v) / len(v) for n, v in per.items()}
+    routed = int(step.b["counts"].sum().item())
+    gf = _gemm_flops(d, routed)
+    total_flops = sum(gf.values())
+    ms = elapsed / args.steps * 1e3
+    value = world * total_flops * args.steps / elapsed / 1e12
+
+    peaks, src = _peaks()
+    bf16 = _peak_val(peaks, "bf16_tflops_sustained", "bf16_tflops") or FALLBACK["bf16_tflops_sustained"]
+    fp8_peak = bf16 * FP8_PER_BF16
+    gemm_time = sum(avg[n] for n in gf)
+    gemm_tflops = total_flops / gemm_time / 1e12
+    hbm = _peak_val(peaks, "hbm_gbs") or FALLBACK["hbm_gbs"]
+
+    quant = _quant_bench(dev)
+    quant["frac"] = quant["GB/s"] / hbm
+    quant["peak"] = hbm
+
+    line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "fp8xfp8->f32 (MXFP8 E4M3, E8M0 scales)",
+            "data": "synthetic (seeded, random-init weights)", "config": config,
+            "gpu_launches": args.steps * sum(LayerStep.KERNELS) * 1,
+            "clocks": clk,
+            "roofline": {"bound": "tensor", "kernel": "k_grouped_gemm (6 launches per step)",
+                         "achieved": gemm_tflops, "peak": fp8_peak, "unit": "TFLOP/s", "frac": gemm_tflops / fp8_peak,
+                         "traffic": None,
+                         "peak_source": f"{src}: bf16 {'sustained' if 'sustained' in str(peaks) else ''} x {FP8_PER_BF16} (nominal fp8/bf16)"},
+            "value_excl_weight_prep": total_flops / (ms * 1e-3 - avg['quantize W13'] - avg['quantize W2']) / 1e12,
+            "kernels_ms": {n: round(v * 1e3, 4) for n, v in avg.items()},
+            "gemm_tflops": {n: round(gf[n] / avg[n] / 1e12, 1) for n in gf},
+            "quantize": quant,
+            "routed_rows": routed}
+
+    if not args.no_e2e:
+        line["e2e"] = _e2e(m, d, dims, inp, dev, args, world)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = {k_: v for k_, v in _cpu_baseline(dims).items() if k_ != "seconds"}
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def _e2e(m, d, dims, inp, dev, args, world):
+    """The same step through the layer entry points (moe_layer_prep_weights,
+    moe_layer_fwd, moe_layer_bwd), with this step's inputs (x, logits, dOut)
+    copied in from pinned host memory and its results (out, dX, d_gate) read
+    back, inside the timed region."""
+    W13 = torch.cat([inp["W1"], inp["W3"]], dim=2).contiguous()
+    W2 = inp["W2"]
+    wq = torch.empty(m.moe_layer_weights_size(d.H, d.F, d.E), dtype=torch.uint8, device=dev)
+    ws = torch.empty(m.moe_layer_workspace_size(d), dtype=torch.uint8, device=dev)
+    h_x = inp["x"].cpu().pin_memory()
+    h_l = inp["logits"].cpu().pin_memory()
+    h_d = inp["dOut"].cpu().pin_memory()
+    x = torch.empty_like(inp["x"])
+    lg = torch.empty_like(inp["logits"])
+    dO = torch.empty_like(inp["dOut"])
+    ids = torch.empty((d.T, d.k), dtype=torch.int32, device=dev)
+    gate = torch.empty((d.T, d.k), dtype=torch.float32, device=dev)
+    out = torch.empty((d.T, d.H), dtype=torch.bfloat16, device=dev)
+    dX = torch.empty_like(out)
+    dW13 = torch.empty((d.E, d.H, 2 * d.F), dtype=torch.float32, device=dev)
+    dW2 = torch.empty((d.E, d.F, d.H), dtype=torch.float32, device=dev)
+    dg = torch.empty((d.T, d.k), dtype=torch.float32, device=dev)
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h_dX = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h_dg = torch.empty(dg.shape, dtype=dg.dtype).pin_memory()
+
+    def one():
+        x.copy_(h_x, non_blocking=True)
+        lg.copy_(h_l, non_blocking=True)
+        dO.copy_(h_d, non_blocking=True)
+        m.moe_layer_prep_weights(W13, W2, wq)
+        m.moe_layer_fwd(x, wq, d, ws, logits=lg, ids=ids, gate=gate, out=out)
+        m.moe_layer_bwd(x, dO, gate, wq, d, ws, dX=dX, dW13=dW13, dW2=dW2, d_gate=dg)
+        h_out.copy_(out, non_blocking=True)
+        h_dX.copy_(dX, non_blocking=True)
+        h_dg.copy_(dg, non_blocking=True)
+
+    for _ in range(args.warmup):
+        one()
+    torch.cuda.synchronize()
+    s = torch.cuda.current_stream(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    for _ in range(args.steps):
+        one()
+    e1.record(s)
+    torch.cuda.synchronize()
+    el = e0.elapsed_time(e1) * 1e-3
+    routed = d.T * d.k
+    flops = sum(_gemm_flops(d, routed).values())
+    h2d = sum(t.numel() * t.element_size() for t in (h_x, h_l, h_d))
+    d2h = sum(t.numel() * t.element_size() for t in (h_out, h_dX, h_dg))
+    return {"value": world * flops * args.steps / el / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": el / args.steps * 1e3}
+
+
+if __name__ == "__main__":
+    main()

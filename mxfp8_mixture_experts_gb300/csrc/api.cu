@@ -1,0 +1,50 @@
+// Library-level entry points: status strings, ABI version, device check.
+#include "common.cuh"
+
+#include <mutex>
+
+namespace mxmoe {
+
+static std::mutex g_dev_mu;
+static int g_dev_ok[64];  // 0 unknown, 1 ok, 2 unsupported
+
+mx_status check_device_cached() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MX_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  if (g_dev_ok[dev] == 0) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return MX_ERR_CUDA;
+    // the binary carries sm_103a code only
+    g_dev_ok[dev] = (major == 10 && minor == 3) ? 1 : 2;
+  }
+  return g_dev_ok[dev] == 1 ? MX_OK : MX_ERR_UNSUPPORTED_DEVICE;
+}
+
+mx_status launch_status() {
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? MX_OK : MX_ERR_CUDA;
+}
+
+}  // namespace mxmoe
+
+extern "C" const char *mx_status_string(mx_status s) {
+  switch (s) {
+    case MX_OK: return "MX_OK";
+    case MX_ERR_INVALID_ARG: return "MX_ERR_INVALID_ARG: null pointer, unknown enum or negative size";
+    case MX_ERR_SHAPE: return "MX_ERR_SHAPE: a dimension breaks the multiple-of-32/128/256 rule";
+    case MX_ERR_ALIGNMENT: return "MX_ERR_ALIGNMENT: a device pointer is not 16-byte aligned";
+    case MX_ERR_UNSUPPORTED_DEVICE: return "MX_ERR_UNSUPPORTED_DEVICE: the current device is not sm_103";
+    case MX_ERR_CUDA: return "MX_ERR_CUDA: a CUDA call failed";
+    case MX_ERR_DEVICE: return "MX_ERR_DEVICE: the device found an expert id out of range or bad group offsets";
+    case MX_ERR_TIMEOUT: return "MX_ERR_TIMEOUT: a bounded pipeline wait expired on the device";
+    case MX_ERR_WORKSPACE: return "MX_ERR_WORKSPACE: workspace smaller than the size query returned";
+    default: return "unknown mx_status";
+  }
+}
+
+extern "C" int32_t mx_abi_version(void) { return 1; }
+
+extern "C" mx_status mx_check_device(void) { return mxmoe::check_device_cached(); }

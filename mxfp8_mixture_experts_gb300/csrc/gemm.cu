@@ -1,0 +1,539 @@
+// Block-scaled MXFP8 grouped GEMM on the sm_100-family 5th-generation tensor
+// cores (tcgen05), written for GB300 (sm_103a).
+//
+// "1.5x faster MoE training on Blackwell with MXFP8 kernels built from
+// scratch", Key Questions Answered: the tcgen05.mma block-scaled MMA
+// accumulates in tensor memory (TMEM) and runs asynchronously; moving data
+// between TMEM and registers costs latency and the fp32 CUDA cores are far
+// slower than the tensor cores, so the scales are applied inside the MMA (no
+// software dequantize) and the epilogue reads TMEM exactly once.
+// pytorch/ao "mxfp8 moe training" PR, Next steps: the grouped GEMM takes
+// pre-quantized operands together with their E8M0 scales.
+//
+// Kernel structure (one persistent CTA per SM, 320 threads):
+//   warp 0      TMA producer: per 128-wide K step, one 128x128 A tile, two
+//               128x128 B tiles (128-byte swizzle) and the matching E8M0
+//               scale chunks (512 B each, already in the MMA's tile layout)
+//               into a 4-stage shared-memory ring.
+//   warp 1      allocates TMEM; one thread copies the scale chunks into TMEM
+//               (tcgen05.cp 32x128b.warpx4) and issues 4 block-scaled MMAs
+//               (M=128, N=256, K=32 each) per stage; tcgen05.commit frees the
+//               stage and, after the last K step, signals the epilogue.
+//   warps 2..9  epilogue: tcgen05.ld of the 128x256 fp32 accumulator (each
+//               warp a 32-lane quarter x 128 columns), release of the
+//               accumulator to the MMA warp, then the conversion and global
+//               stores (bf16, fp32, or the fused SwiGLU + MXFP8 quantize).
+// Group offsets stay on the device: every CTA walks the same static tile
+// schedule derived from them (no host synchronization).
+#include "common.cuh"
+
+#include <mutex>
+
+namespace mxmoe {
+namespace gemm {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 128;  // fp8 elements (= bytes) per row per stage
+constexpr int STAGES = 4;
+constexpr int A_TILE = BM * BK;          // 16 KB
+constexpr int B_HALF = 128 * BK;         // 16 KB (one TMA box)
+constexpr int B_TILE = BN * BK;          // 32 KB
+constexpr int SF_STAGE = 512 + 1024;     // SFA chunk + two SFB chunks
+constexpr uint32_t STAGE_TX = A_TILE + B_TILE + SF_STAGE;
+constexpr int NUM_THREADS = 320;
+constexpr int NUM_EPI_WARPS = 8;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t ACC_COL = 0;
+constexpr uint32_t SF_COL = 256;  // per stage: SFA 4 columns, SFB 8 columns
+constexpr int MAX_E = 1024;
+constexpr uint64_t WAIT_TIMEOUT_NS = 2000000000ull;
+
+constexpr int SMEM_A = 0;
+constexpr int SMEM_B = SMEM_A + STAGES * A_TILE;
+constexpr int SMEM_SF = SMEM_B + STAGES * B_TILE;
+constexpr int SMEM_BAR = SMEM_SF + STAGES * SF_STAGE;
+constexpr int SMEM_OFFS = SMEM_BAR + 256;
+constexpr int SMEM_TOTAL = SMEM_OFFS + (MAX_E + 1) * 4;
+constexpr int SMEM_ALLOC = SMEM_TOTAL + 1024;  // slack to align the base to 1024
+
+enum { EPI_BF16 = 0, EPI_F32 = 1, EPI_GLU = 2 };
+enum { OP_ROWS = 0, OP_TOKENS = 1 };
+
+struct Params {
+  int op, epi, E;
+  int64_t M_cap, N, K;  // see mx_grouped_gemm; for EPI_GLU N = F (output pairs)
+  const int32_t *offsets;
+  const uint8_t *sA, *sB;
+  void *C;
+  uint16_t *ab;
+  uint8_t *hq, *hs;
+  int32_t *dev_status;
+};
+
+// Instruction descriptor, kind::mxf8f6f4 with block scales: E4M3 x E4M3,
+// both operands K-major, UE8M0 scales, M=128, N=256; bits 4-5 and 29-30 pick
+// the byte (= 32-wide K block) of the 32-bit scale column.
+__host__ __device__ constexpr uint32_t idesc_base() {
+  return (0u << 7) | (0u << 10) | ((uint32_t)(BN >> 3) << 17) | (1u << 23) | ((uint32_t)(BM >> 4) << 24);
+}
+
+struct Tile {
+  int64_t a_row, b_row0, b_row1;  // TMA row coordinates
+  int64_t k0;                     // first contraction coordinate
+  int num_k;                      // 128-wide K steps (0: empty wgrad group)
+  int64_t sfa_base, sfb_base0, sfb_base1;  // byte offsets of the k=0 scale chunks
+  int64_t out_row, out_col;       // output position of the tile's top-left
+  int e;
+};
+
+__device__ __forceinline__ int find_group(const int32_t *off, int E, int64_t row) {
+  int lo = 0, hi = E;  // largest e with off[e] <= row
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (off[mid] <= row) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
+__device__ __forceinline__ int64_t num_tiles(const Params &p, const int32_t *off) {
+  if (p.op == OP_ROWS) {
+    const int64_t n_tiles = p.epi == EPI_GLU ? p.N / 128 : p.N / BN;
+    return (int64_t)(off[p.E] / BM) * n_tiles;
+  }
+  return (int64_t)p.E * (p.N / BM) * (p.K / BN);
+}
+
+__device__ __forceinline__ Tile decode_tile(const Params &p, const int32_t *off, int64_t t) {
+  Tile tl;
+  if (p.op == OP_ROWS) {
+    const int64_t n_tiles = p.epi == EPI_GLU ? p.N / 128 : p.N / BN;
+    const int64_t mt = t / n_tiles, nt = t % n_tiles;
+    const int64_t row = mt * BM;
+    const int e = find_group(off, p.E, row);
+    const int64_t kblocks = p.K / BK;
+    tl.e = e;
+    tl.a_row = row;
+    if (p.epi == EPI_GLU) {  // B rows: W1 part then W3 part of the same 128 output features
+      tl.b_row0 = (int64_t)e * 2 * p.N + nt * 128;
+      tl.b_row1 = tl.b_row0 + p.N;
+      tl.out_col = nt * 128;
+    } else {
+      tl.b_row0 = (int64_t)e * p.N + nt * BN;
+      tl.b_row1 = tl.b_row0 + 128;
+      tl.out_col = nt * BN;
+    }
+    tl.k0 = 0;
+    tl.num_k = (int)kblocks;
+    tl.sfa_base = (row / 128) * kblocks * 512;
+    tl.sfb_base0 = (tl.b_row0 / 128) * kblocks * 512;
+    tl.sfb_base1 = (tl.b_row1 / 128) * kblocks * 512;
+    tl.out_row = row;
+  } else {
+    const int64_t rt_n = p.N / BM, ct_n = p.K / BN;
+    const int64_t per_e = rt_n * ct_n;
+    const int e = (int)(t / per_e);
+    const int64_t rem = t % per_e;
+    const int64_t rt = rem / ct_n, ct = rem % ct_n;
+    const int64_t kblocks = p.M_cap / BK;  // scale chunks per row tile
+    tl.e = e;
+    tl.a_row = rt * BM;
+    tl.b_row0 = ct * BN;
+    tl.b_row1 = tl.b_row0 + 128;
+    tl.k0 = off[e];
+    tl.num_k = (off[e + 1] - off[e]) / BK;
+    tl.sfa_base = (rt * kblocks + off[e] / BK) * 512;
+    tl.sfb_base0 = ((tl.b_row0 / 128) * kblocks + off[e] / BK) * 512;
+    tl.sfb_base1 = ((tl.b_row1 / 128) * kblocks + off[e] / BK) * 512;
+    tl.out_row = (int64_t)e * p.N + rt * BM;
+    tl.out_col = ct * BN;
+  }
+  return tl;
+}
+
+__device__ __forceinline__ float silu_f(float a) { return a / (1.0f + expf(-a)); }
+
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    k_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + SMEM_BAR);
+  uint64_t *empty = full + STAGES;
+  uint64_t *tmem_full = empty + STAGES;
+  uint64_t *tmem_empty = tmem_full + 1;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tmem_empty + 1);
+  int32_t *s_flag = reinterpret_cast<int32_t *>(tmem_slot + 1);
+  int32_t *s_off = reinterpret_cast<int32_t *>(smem + SMEM_OFFS);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // group offsets -> shared memory, validated identically by every CTA
+  for (int i = threadIdx.x; i <= p.E; i += NUM_THREADS) s_off[i] = p.offsets[i];
+  if (threadIdx.x == 0) {
+    int ok = 1;
+    for (int i = 0; i < p.E; ++i)
+      if (s_off[i + 1] < s_off[i] || (s_off[i] & (BM - 1))) ok = 0;
+    if (s_off[0] < 0 || (s_off[p.E] & (BM - 1)) || s_off[p.E] > p.M_cap) ok = 0;
+    *s_flag = ok;
+    if (!ok && blockIdx.x == 0) set_status(p.dev_status, MX_ERR_DEVICE);
+  }
+  if (warp == 0 && lane == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(tmem_full, 1);
+    mbar_init(tmem_empty, NUM_EPI_WARPS);
+    fence_mbar_init();
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+  }
+  __syncthreads();
+  if (!*s_flag) return;
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int64_t ntiles = num_tiles(p, s_off);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool dead = false;
+      for (int64_t t = blockIdx.x; t < ntiles && !dead; t += gridDim.x) {
+        const Tile tl = decode_tile(p, s_off, t);
+        for (int kb = 0; kb < tl.num_k; ++kb) {
+          if (!mbar_wait_bounded(&empty[stage], phase ^ 1, WAIT_TIMEOUT_NS)) {
+            set_status(p.dev_status, MX_ERR_TIMEOUT);
+            dead = true;
+            break;
+          }
+          uint8_t *sa = smem + SMEM_A + stage * A_TILE;
+          uint8_t *sb = smem + SMEM_B + stage * B_TILE;
+          uint8_t *sf = smem + SMEM_SF + stage * SF_STAGE;
+          const int32_t kc = (int32_t)(tl.k0 + (int64_t)kb * BK);
+          mbar_arrive_expect_tx(&full[stage], STAGE_TX);
+          tma_load_2d(sa, &tmA, &full[stage], kc, (int32_t)tl.a_row);
+          tma_load_2d(sb, &tmB, &full[stage], kc, (int32_t)tl.b_row0);
+          tma_load_2d(sb + B_HALF, &tmB, &full[stage], kc, (int32_t)tl.b_row1);
+          bulk_load(sf, p.sA + tl.sfa_base + (int64_t)kb * 512, 512, &full[stage]);
+          bulk_load(sf + 512, p.sB + tl.sfb_base0 + (int64_t)kb * 512, 512, &full[stage]);
+          bulk_load(sf + 1024, p.sB + tl.sfb_base1 + (int64_t)kb * 512, 512, &full[stage]);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool dead = false;
+      const uint32_t d_tmem = tmem_base + ACC_COL;
+      for (int64_t t = blockIdx.x; t < ntiles && !dead; t += gridDim.x) {
+        const Tile tl = decode_tile(p, s_off, t);
+        if (tl.num_k == 0) continue;
+        if (!mbar_wait_bounded(tmem_empty, acc_phase ^ 1, WAIT_TIMEOUT_NS)) {
+          set_status(p.dev_status, MX_ERR_TIMEOUT);
+          break;
+        }
+        tc_fence_after();
+        for (int kb = 0; kb < tl.num_k; ++kb) {
+          if (!mbar_wait_bounded(&full[stage], phase, WAIT_TIMEOUT_NS)) {
+            set_status(p.dev_status, MX_ERR_TIMEOUT);
+            dead = true;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + SMEM_A + stage * A_TILE);
+          const uint32_t sb = smem_u32(smem + SMEM_B + stage * B_TILE);
+          const uint32_t sf = smem_u32(smem + SMEM_SF + stage * SF_STAGE);
+          const uint32_t sfa_t = tmem_base + SF_COL + stage * 12;
+          const uint32_t sfb_t = sfa_t + 4;
+          tc_cp_32x128b_warpx4(sfa_t, smem_desc(sf, 0, 128, 0));
+          tc_cp_32x128b_warpx4(sfb_t, smem_desc(sf + 512, 0, 128, 0));
+          tc_cp_32x128b_warpx4(sfb_t + 4, smem_desc(sf + 1024, 0, 128, 0));
+#pragma unroll
+          for (int kk = 0; kk < BK / 32; ++kk) {
+            const uint64_t ad = smem_desc(sa + kk * 32, 16, 1024, 2);
+            const uint64_t bd = smem_desc(sb + kk * 32, 16, 1024, 2);
+            const uint32_t id = idesc_base() | ((uint32_t)kk << 4) | ((uint32_t)kk << 29);
+            tc_mma_mxf8(d_tmem, ad, bd, id, sfa_t, sfb_t, (kb | kk) != 0);
+          }
+          tc_commit(&empty[stage]);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (dead) break;
+        tc_commit(tmem_full);
+        acc_phase ^= 1;
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;             // TMEM lane quarter this warp may read
+    const int h = (warp - 2) >> 2;      // which half of the columns
+    const int row_in_tile = q * 32 + lane;
+    const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16) + ACC_COL;
+    uint32_t acc_phase = 0;
+    for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
+      const Tile tl = decode_tile(p, s_off, t);
+      const int64_t orow = tl.out_row + row_in_tile;
+      if (tl.num_k == 0) {  // empty wgrad group: the output block is zero
+        float *c = static_cast<float *>(p.C) + orow * p.K + tl.out_col + h * 128;
+        if (p.epi == EPI_F32) {
+          for (int j = 0; j < 32; ++j) reinterpret_cast<float4 *>(c)[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+        } else {
+          uint16_t *cb = static_cast<uint16_t *>(p.C) + orow * p.K + tl.out_col + h * 128;
+          for (int j = 0; j < 16; ++j) reinterpret_cast<uint4 *>(cb)[j] = make_uint4(0, 0, 0, 0);
+        }
+        continue;
+      }
+      if (!mbar_wait_bounded(tmem_full, acc_phase, WAIT_TIMEOUT_NS)) {
+        set_status(p.dev_status, MX_ERR_TIMEOUT);
+        break;
+      }
+      tc_fence_after();
+      uint32_t r[128];
+      if (p.epi == EPI_GLU) {
+        // a columns [h*64, h*64+64), b columns [128 + h*64, ...)
+        MX_TMEM_LD_32x32b_x32(t_row + h * 64, r);
+        MX_TMEM_LD_32x32b_x32(t_row + h * 64 + 32, (r + 32));
+        MX_TMEM_LD_32x32b_x32(t_row + 128 + h * 64, (r + 64));
+        MX_TMEM_LD_32x32b_x32(t_row + 128 + h * 64 + 32, (r + 96));
+      } else {
+        MX_TMEM_LD_32x32b_x32(t_row + h * 128, r);
+        MX_TMEM_LD_32x32b_x32(t_row + h * 128 + 32, (r + 32));
+        MX_TMEM_LD_32x32b_x32(t_row + h * 128 + 64, (r + 64));
+        MX_TMEM_LD_32x32b_x32(t_row + h * 128 + 96, (r + 96));
+      }
+      tc_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tmem_empty);
+      acc_phase ^= 1;
+
+      if (p.epi == EPI_F32) {
+        const int64_t ldc = p.op == OP_ROWS ? p.N : p.K;
+        float4 *c = reinterpret_cast<float4 *>(static_cast<float *>(p.C) + orow * ldc + tl.out_col + h * 128);
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          c[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]), __uint_as_float(r[4 * j + 2]),
+                             __uint_as_float(r[4 * j + 3]));
+      } else if (p.epi == EPI_BF16) {
+        const int64_t ldc = p.op == OP_ROWS ? p.N : p.K;
+        uint4 *c = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.C) + orow * ldc + tl.out_col + h * 128);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const uint32_t *v = r + 8 * j;
+          c[j] = make_uint4(pack_bf16x2(__uint_as_float(v[0]), __uint_as_float(v[1])),
+                            pack_bf16x2(__uint_as_float(v[2]), __uint_as_float(v[3])),
+                            pack_bf16x2(__uint_as_float(v[4]), __uint_as_float(v[5])),
+                            pack_bf16x2(__uint_as_float(v[6]), __uint_as_float(v[7])));
+        }
+      } else {
+        // fused SwiGLU: a, b -> bf16 (saved), h = silu(a) * b -> MXFP8 (blocks along F)
+        const int64_t F = p.N;
+        const int64_t f0 = tl.out_col + h * 64;
+        uint4 *pa = reinterpret_cast<uint4 *>(p.ab + orow * 2 * F + f0);
+        uint4 *pb = reinterpret_cast<uint4 *>(p.ab + orow * 2 * F + F + f0);
+        uint4 *ph = reinterpret_cast<uint4 *>(p.hq + orow * F + f0);
+#pragma unroll
+        for (int blk = 0; blk < 2; ++blk) {
+          float hv[32];
+          uint32_t am = 0;
+#pragma unroll
+          for (int j = 0; j < 32; j += 8) {
+            float av[8], bv[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              av[i] = round_bf16(__uint_as_float(r[blk * 32 + j + i]));
+              bv[i] = round_bf16(__uint_as_float(r[64 + blk * 32 + j + i]));
+              hv[j + i] = silu_f(av[i]) * bv[i];
+              am = max(am, abs_bits(hv[j + i]));
+            }
+            pa[(blk * 32 + j) / 8] = make_uint4(pack_bf16x2(av[0], av[1]), pack_bf16x2(av[2], av[3]),
+                                                pack_bf16x2(av[4], av[5]), pack_bf16x2(av[6], av[7]));
+            pb[(blk * 32 + j) / 8] = make_uint4(pack_bf16x2(bv[0], bv[1]), pack_bf16x2(bv[2], bv[3]),
+                                                pack_bf16x2(bv[4], bv[5]), pack_bf16x2(bv[6], bv[7]));
+          }
+          const MxScale s = mx_scale_from_amax_bits(am);
+          uint32_t w[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            w[i] = s.bad ? 0x7f7f7f7fu
+                         : pack_e4m3x4(hv[4 * i] * s.inv, hv[4 * i + 1] * s.inv, hv[4 * i + 2] * s.inv,
+                                       hv[4 * i + 3] * s.inv);
+          ph[blk * 2] = make_uint4(w[0], w[1], w[2], w[3]);
+          ph[blk * 2 + 1] = make_uint4(w[4], w[5], w[6], w[7]);
+          p.hs[sf_swizzle_offset(orow, f0 / 32 + blk, round_up(F / 32, 4))] = (uint8_t)s.byte;
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+// 2-D uint8 map over [outer, inner] (inner contiguous), 128x128 boxes, 128-byte swizzle
+static mx_status make_map(CUtensorMap *m, const void *base, int64_t inner, int64_t outer) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return MX_ERR_CUDA;
+  cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
+  cuuint64_t strides[1] = {(cuuint64_t)inner};
+  cuuint32_t box[2] = {128, 128};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MX_OK : MX_ERR_CUDA;
+}
+
+static std::mutex g_mu;
+static int g_smem_set[64];
+static int g_num_sms[64];
+
+static mx_status prepare(int *num_sms) {
+  int dev = 0;
+  MX_CUDA_TRY(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= 64) return MX_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_smem_set[dev]) {
+    MX_CUDA_TRY(cudaFuncSetAttribute(k_grouped_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC));
+    MX_CUDA_TRY(cudaDeviceGetAttribute(&g_num_sms[dev], cudaDevAttrMultiProcessorCount, dev));
+    g_smem_set[dev] = 1;
+  }
+  *num_sms = g_num_sms[dev];
+  return MX_OK;
+}
+
+mx_status launch(const Params &p, const uint8_t *A, int64_t a_inner, int64_t a_outer, const uint8_t *B,
+                 int64_t b_inner, int64_t b_outer, int64_t max_tiles, mx_stream stream) {
+  int sms = 0;
+  mx_status st = prepare(&sms);
+  if (st != MX_OK) return st;
+  CUtensorMap ma, mb;
+  st = make_map(&ma, A, a_inner, a_outer);
+  if (st != MX_OK) return st;
+  st = make_map(&mb, B, b_inner, b_outer);
+  if (st != MX_OK) return st;
+  int64_t grid = max_tiles < sms ? max_tiles : sms;
+  if (grid < 1) grid = 1;
+  k_grouped_gemm<<<(unsigned)grid, NUM_THREADS, SMEM_ALLOC, stream>>>(ma, mb, p);
+  return launch_status();
+}
+
+}  // namespace gemm
+}  // namespace mxmoe
+
+using namespace mxmoe;
+
+extern "C" mx_status mx_grouped_gemm(int32_t op, const uint8_t *A, const uint8_t *sA, const uint8_t *B,
+                                     const uint8_t *sB, const int32_t *offsets, int32_t E, int64_t M_cap, int64_t N,
+                                     int64_t K, void *C, int32_t c_dtype, int32_t *dev_status, mx_stream stream) {
+  MX_HOST_CHECK(op == MX_GEMM_FWD || op == MX_GEMM_DGRAD || op == MX_GEMM_WGRAD, MX_ERR_INVALID_ARG);
+  MX_HOST_CHECK(A && sA && B && sB && offsets && C, MX_ERR_INVALID_ARG);
+  MX_HOST_CHECK(c_dtype == MX_OUT_BF16 || c_dtype == MX_OUT_F32, MX_ERR_INVALID_ARG);
+  MX_HOST_CHECK(E >= 1 && E <= gemm::MAX_E && M_cap >= 0 && N > 0 && K > 0, MX_ERR_INVALID_ARG);
+  MX_HOST_CHECK(M_cap % 128 == 0 && N % 256 == 0 && K % 128 == 0, MX_ERR_SHAPE);
+  MX_HOST_CHECK(M_cap < (int64_t)1 << 31 && N < (int64_t)1 << 31 && K < (int64_t)1 << 31, MX_ERR_SHAPE);
+  MX_HOST_CHECK(aligned16(A) && aligned16(B) && aligned16(sA) && aligned16(sB) && aligned16(C), MX_ERR_ALIGNMENT);
+  mx_status st = check_device_cached();
+  if (st != MX_OK) return st;
+  gemm::Params p;
+  p.E = E;
+  p.M_cap = M_cap;
+  p.N = N;
+  p.offsets = offsets;
+  p.sA = sA;
+  p.sB = sB;
+  p.C = C;
+  p.ab = nullptr;
+  p.hq = nullptr;
+  p.hs = nullptr;
+  p.dev_status = dev_status;
+  p.epi = c_dtype == MX_OUT_F32 ? gemm::EPI_F32 : gemm::EPI_BF16;
+  if (op == MX_GEMM_WGRAD) {
+    MX_HOST_CHECK(N % 128 == 0 && K % 256 == 0, MX_ERR_SHAPE);
+    p.op = gemm::OP_TOKENS;
+    p.K = K;
+    if (M_cap == 0) return cudaMemsetAsync(C, 0, (size_t)E * N * K * (c_dtype == MX_OUT_F32 ? 4 : 2), stream) ==
+                                   cudaSuccess ? MX_OK : MX_ERR_CUDA;
+    const int64_t tiles = (int64_t)E * (N / 128) * (K / 256);
+    return gemm::launch(p, A, M_cap, N, B, M_cap, K, tiles, stream);
+  }
+  if (M_cap == 0) return MX_OK;
+  p.op = gemm::OP_ROWS;
+  p.K = K;
+  const int64_t tiles = (M_cap / 128) * (N / 256);
+  return gemm::launch(p, A, K, M_cap, B, K, (int64_t)E * N, tiles, stream);
+}
+
+extern "C" mx_status moe_gemm1_swiglu(const uint8_t *A, const uint8_t *sA, const uint8_t *B, const uint8_t *sB,
+                                      const int32_t *offsets, int32_t E, int64_t M_cap, int64_t F, int64_t H,
+                                      void *ab, uint8_t *hq, uint8_t *hs, int32_t *dev_status, mx_stream stream) {
+  MX_HOST_CHECK(A && sA && B && sB && offsets && ab && hq && hs, MX_ERR_INVALID_ARG);
+  MX_HOST_CHECK(E >= 1 && E <= gemm::MAX_E && M_cap >= 0 && F > 0 && H > 0, MX_ERR_INVALID_ARG);
+  MX_HOST_CHECK(M_cap % 128 == 0 && F % 128 == 0 && H % 128 == 0, MX_ERR_SHAPE);
+  MX_HOST_CHECK(aligned16(A) && aligned16(B) && aligned16(sA) && aligned16(sB) && aligned16(ab) && aligned16(hq),
+                MX_ERR_ALIGNMENT);
+  mx_status st = check_device_cached();
+  if (st != MX_OK) return st;
+  if (M_cap == 0) return MX_OK;
+  gemm::Params p;
+  p.op = gemm::OP_ROWS;
+  p.epi = gemm::EPI_GLU;
+  p.E = E;
+  p.M_cap = M_cap;
+  p.N = F;
+  p.K = H;
+  p.offsets = offsets;
+  p.sA = sA;
+  p.sB = sB;
+  p.C = nullptr;
+  p.ab = static_cast<uint16_t *>(ab);
+  p.hq = hq;
+  p.hs = hs;
+  p.dev_status = dev_status;
+  const int64_t tiles = (M_cap / 128) * (F / 128);
+  return gemm::launch(p, A, H, M_cap, B, H, (int64_t)E * 2 * F, tiles, stream);
+}

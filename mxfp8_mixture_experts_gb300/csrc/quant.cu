@@ -1,0 +1,333 @@
+// MXFP8 quantize kernels.
+//
+// Block quantization per OCP Microscaling Formats (MX) v1.0, section 6.3
+// (32-element blocks, E8M0 scale 2^(floor(log2 amax) - 8), E4M3 elements cast
+// with round-to-nearest-even and saturation), row-wise and column-wise, as the
+// "1.5x faster MoE training on Blackwell with MXFP8 kernels built from
+// scratch" article (Key Questions Answered: microscaling; Common Pitfalls:
+// quantization overhead) and the pytorch/ao "mxfp8 moe training" PR stack
+// (Stacked PRs: quant kernels) describe.
+//
+// HBM-bound.  One CTA owns a tile of 128 rows x 64 columns of the input:
+//   phase 1  coalesced 16-byte loads; each 32-element row block lives in 4
+//            consecutive lanes, so the ROW result needs only two shuffles;
+//            the tile is staged in shared memory for the column pass;
+//   phase 2  each thread walks 32 rows of one column in shared memory
+//            (conflict-free: a warp reads 64 contiguous bytes per row) and
+//            writes the 32 E4M3 bytes of that column block contiguously into
+//            the transposed COL output.
+#include "common.cuh"
+
+namespace mxmoe {
+
+constexpr int QT_ROWS = 128;
+constexpr int QT_COLS = 64;
+constexpr int QT_THREADS = 256;
+
+struct QuantArgs {
+  const uint16_t *x;
+  int64_t rows, cols;
+  // gather mode: output row r takes input row src[r] / k (zero when src[r] < 0),
+  // multiplied by gate[src[r]] (fp32 product rounded to bf16) when gate != NULL
+  const int32_t *src;
+  const float *gate;
+  int k;
+  uint8_t *q_row, *s_row, *q_col, *s_col;
+  int64_t s_row_stride, s_col_stride;  // bytes per batch entry
+  int32_t swizzled;
+};
+
+__device__ __forceinline__ void store_scale(uint8_t *s, int64_t r, int64_t c, int64_t ncols_blocks, bool swz,
+                                            uint32_t v) {
+  int64_t off = swz ? sf_swizzle_offset(r, c, round_up(ncols_blocks, 4)) : r * ncols_blocks + c;
+  s[off] = (uint8_t)v;
+}
+
+// Quantize 32 values that one thread holds; writes 32 bytes to dst (16-B aligned).
+__device__ __forceinline__ uint32_t quant32_store(const float *v, uint8_t *dst) {
+  uint32_t am = 0;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) am = max(am, abs_bits(v[i]));
+  MxScale s = mx_scale_from_amax_bits(am);
+  uint32_t w[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    w[i] = s.bad ? 0x7f7f7f7fu
+                 : pack_e4m3x4(v[4 * i] * s.inv, v[4 * i + 1] * s.inv, v[4 * i + 2] * s.inv, v[4 * i + 3] * s.inv);
+  reinterpret_cast<uint4 *>(dst)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+  reinterpret_cast<uint4 *>(dst)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+  return s.byte;
+}
+
+template <bool ROW, bool COL, bool GATHER>
+__global__ void __launch_bounds__(QT_THREADS) k_quantize_bf16(QuantArgs a) {
+  __shared__ __align__(16) uint16_t tile[QT_ROWS][QT_COLS];
+  const int tid = threadIdx.x;
+  const int64_t b = blockIdx.z;
+  const int64_t row0 = (int64_t)blockIdx.y * QT_ROWS;
+  const int64_t col0 = (int64_t)blockIdx.x * QT_COLS;
+  const uint16_t *x = a.x + b * a.rows * a.cols;
+  const int64_t cblocks = a.cols / 32, rblocks = a.rows / 32;
+
+  // ---- phase 1: load, ROW quant, stage ----
+#pragma unroll
+  for (int it = 0; it < (QT_ROWS * QT_COLS / 8) / QT_THREADS; ++it) {
+    const int c = it * QT_THREADS + tid;
+    const int r = c >> 3, ch = c & 7;
+    const int64_t gr = row0 + r, gc = col0 + ch * 8;
+    const bool valid = gr < a.rows && gc < a.cols;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (GATHER) {
+      const int32_t sidx = valid ? a.src[gr] : -1;
+      if (sidx >= 0) {
+        v = __ldg(reinterpret_cast<const uint4 *>(a.x + (int64_t)(sidx / a.k) * a.cols + gc));
+        if (a.gate) {
+          const float g = a.gate[sidx];
+          v.x = pack_bf16x2(g * bf16_lo(v.x), g * bf16_hi(v.x));
+          v.y = pack_bf16x2(g * bf16_lo(v.y), g * bf16_hi(v.y));
+          v.z = pack_bf16x2(g * bf16_lo(v.z), g * bf16_hi(v.z));
+          v.w = pack_bf16x2(g * bf16_lo(v.w), g * bf16_hi(v.w));
+        }
+      }
+    } else if (valid) {
+      v = __ldg(reinterpret_cast<const uint4 *>(x + gr * a.cols + gc));
+    }
+    if (COL) *reinterpret_cast<uint4 *>(&tile[r][ch * 8]) = v;
+    if (ROW) {
+      float f[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
+                    bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
+      uint32_t am = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) am = max(am, abs_bits(f[i]));
+      am = max(am, __shfl_xor_sync(0xffffffffu, am, 1));
+      am = max(am, __shfl_xor_sync(0xffffffffu, am, 2));
+      MxScale s = mx_scale_from_amax_bits(am);
+      uint2 o;
+      o.x = s.bad ? 0x7f7f7f7fu : pack_e4m3x4(f[0] * s.inv, f[1] * s.inv, f[2] * s.inv, f[3] * s.inv);
+      o.y = s.bad ? 0x7f7f7f7fu : pack_e4m3x4(f[4] * s.inv, f[5] * s.inv, f[6] * s.inv, f[7] * s.inv);
+      if (valid) {
+        *reinterpret_cast<uint2 *>(a.q_row + b * a.rows * a.cols + gr * a.cols + gc) = o;
+        if ((ch & 3) == 0) store_scale(a.s_row + b * a.s_row_stride, gr, gc / 32, cblocks, a.swizzled, s.byte);
+      }
+    }
+  }
+  if (!COL) return;
+  __syncthreads();
+
+  // ---- phase 2: COL quant from shared memory ----
+  const int col = tid & (QT_COLS - 1);
+  const int rb = tid / QT_COLS;  // 0..3
+  const int64_t gc = col0 + col, gr = row0 + rb * 32;
+  if (gc >= a.cols || gr >= a.rows) return;
+  float v[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float((uint32_t)tile[rb * 32 + i][col] << 16);
+  uint8_t *dst = a.q_col + b * a.rows * a.cols + gc * a.rows + gr;
+  uint32_t sb = quant32_store(v, dst);
+  store_scale(a.s_col + b * a.s_col_stride, gc, gr / 32, rblocks, a.swizzled, sb);
+}
+
+// ---------------------------------------------------------------------------
+// SwiGLU backward + quantization (see moe_swiglu_bwd in mxmoe.h).
+// Tile: 64 rows x 32 columns of F.  Phase 1: per (row, 8-column chunk)
+// compute da, db, h in fp32, ROW-quantize da and db (4 lanes per block), and
+// stage da, db, h in shared memory; phase 2: COL-quantize the three matrices.
+// ---------------------------------------------------------------------------
+constexpr int SB_ROWS = 64;
+constexpr int SB_COLS = 32;
+
+__device__ __forceinline__ float sigmoidf_(float a) { return 1.0f / (1.0f + expf(-a)); }
+
+__global__ void __launch_bounds__(256) k_swiglu_bwd(const float *__restrict__ dh, const uint16_t *__restrict__ ab,
+                                                    int64_t rows, int64_t F, uint8_t *dab_rq, uint8_t *dab_rs,
+                                                    uint8_t *dab_cq, uint8_t *dab_cs, uint8_t *h_cq,
+                                                    uint8_t *h_cs) {
+  __shared__ float s_da[SB_ROWS][SB_COLS + 1];
+  __shared__ float s_db[SB_ROWS][SB_COLS + 1];
+  __shared__ float s_h[SB_ROWS][SB_COLS + 1];
+  const int tid = threadIdx.x;
+  const int64_t row0 = (int64_t)blockIdx.y * SB_ROWS;
+  const int64_t f0 = (int64_t)blockIdx.x * SB_COLS;
+  const int64_t twoF = 2 * F;
+  const int64_t cb2 = twoF / 32;
+
+#pragma unroll
+  for (int it = 0; it < 1; ++it) {
+    const int c = it * 256 + tid;  // 256 chunks: 64 rows x 4 chunks of 8
+    const int r = c >> 2, ch = c & 3;
+    const int64_t gr = row0 + r, gf = f0 + ch * 8;
+    const float4 d0 = *reinterpret_cast<const float4 *>(dh + gr * F + gf);
+    const float4 d1 = *reinterpret_cast<const float4 *>(dh + gr * F + gf + 4);
+    const uint4 av = *reinterpret_cast<const uint4 *>(ab + gr * twoF + gf);
+    const uint4 bv = *reinterpret_cast<const uint4 *>(ab + gr * twoF + F + gf);
+    const float d[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
+    const float A[8] = {bf16_lo(av.x), bf16_hi(av.x), bf16_lo(av.y), bf16_hi(av.y),
+                        bf16_lo(av.z), bf16_hi(av.z), bf16_lo(av.w), bf16_hi(av.w)};
+    const float B[8] = {bf16_lo(bv.x), bf16_hi(bv.x), bf16_lo(bv.y), bf16_hi(bv.y),
+                        bf16_lo(bv.z), bf16_hi(bv.z), bf16_lo(bv.w), bf16_hi(bv.w)};
+    float da[8], db[8];
+    uint32_t ama = 0, amb = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float s = sigmoidf_(A[i]);
+      const float silu = A[i] * s;
+      da[i] = d[i] * B[i] * s * (1.0f + A[i] * (1.0f - s));
+      db[i] = d[i] * silu;
+      s_da[r][ch * 8 + i] = da[i];
+      s_db[r][ch * 8 + i] = db[i];
+      s_h[r][ch * 8 + i] = silu * B[i];
+      ama = max(ama, abs_bits(da[i]));
+      amb = max(amb, abs_bits(db[i]));
+    }
+    ama = max(ama, __shfl_xor_sync(0xffffffffu, ama, 1));
+    ama = max(ama, __shfl_xor_sync(0xffffffffu, ama, 2));
+    amb = max(amb, __shfl_xor_sync(0xffffffffu, amb, 1));
+    amb = max(amb, __shfl_xor_sync(0xffffffffu, amb, 2));
+    const MxScale sa = mx_scale_from_amax_bits(ama), sbb = mx_scale_from_amax_bits(amb);
+    uint2 oa, ob;
+    oa.x = sa.bad ? 0x7f7f7f7fu : pack_e4m3x4(da[0] * sa.inv, da[1] * sa.inv, da[2] * sa.inv, da[3] * sa.inv);
+    oa.y = sa.bad ? 0x7f7f7f7fu : pack_e4m3x4(da[4] * sa.inv, da[5] * sa.inv, da[6] * sa.inv, da[7] * sa.inv);
+    ob.x = sbb.bad ? 0x7f7f7f7fu : pack_e4m3x4(db[0] * sbb.inv, db[1] * sbb.inv, db[2] * sbb.inv, db[3] * sbb.inv);
+    ob.y = sbb.bad ? 0x7f7f7f7fu : pack_e4m3x4(db[4] * sbb.inv, db[5] * sbb.inv, db[6] * sbb.inv, db[7] * sbb.inv);
+    *reinterpret_cast<uint2 *>(dab_rq + gr * twoF + gf) = oa;
+    *reinterpret_cast<uint2 *>(dab_rq + gr * twoF + F + gf) = ob;
+    if (ch == 0) {
+      dab_rs[sf_swizzle_offset(gr, gf / 32, round_up(cb2, 4))] = (uint8_t)sa.byte;
+      dab_rs[sf_swizzle_offset(gr, (F + gf) / 32, round_up(cb2, 4))] = (uint8_t)sbb.byte;
+    }
+  }
+  __syncthreads();
+
+  // COL: 3 matrices x 32 columns x 2 row blocks = 192 items
+  const int64_t rblocks_total = rows / 32;
+  for (int item = tid; item < 3 * SB_COLS * (SB_ROWS / 32); item += 256) {
+    const int m = item / (SB_COLS * (SB_ROWS / 32));
+    const int rem = item % (SB_COLS * (SB_ROWS / 32));
+    const int col = rem % SB_COLS, rb = rem / SB_COLS;
+    float v[32];
+    const float(*src)[SB_COLS + 1] = m == 0 ? s_da : (m == 1 ? s_db : s_h);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = src[rb * 32 + i][col];
+    const int64_t gr = row0 + rb * 32;
+    if (m < 2) {
+      const int64_t orow = (m == 0 ? 0 : F) + f0 + col;  // row of the transposed [2F, rows] output
+      const uint32_t sb = quant32_store(v, dab_cq + orow * rows + gr);
+      dab_cs[sf_swizzle_offset(orow, gr / 32, round_up(rblocks_total, 4))] = (uint8_t)sb;
+    } else {
+      const int64_t orow = f0 + col;
+      const uint32_t sb = quant32_store(v, h_cq + orow * rows + gr);
+      h_cs[sf_swizzle_offset(orow, gr / 32, round_up(rblocks_total, 4))] = (uint8_t)sb;
+    }
+  }
+}
+
+}  // namespace mxmoe
+
+using namespace mxmoe;
+
+extern "C" int64_t mx_scale_bytes(int64_t rows, int64_t cols, int32_t layout) {
+  if (rows < 0 || cols < 0 || cols % 32) return -1;
+  if (layout == MX_SCALE_SWIZZLED) return round_up(rows, 128) * round_up(cols / 32, 4);
+  return rows * (cols / 32);
+}
+
+extern "C" mx_status mx_quantize(const void *x, int64_t batch, int64_t rows, int64_t cols, int32_t mode,
+                                 int32_t scale_layout, uint8_t *q_row, uint8_t *s_row, uint8_t *q_col,
+                                 uint8_t *s_col, mx_stream stream) {
+  MX_HOST_CHECK(x != nullptr, MX_ERR_INVALID_ARG);
+  MX_HOST_CHECK(mode == MX_MODE_ROW || mode == MX_MODE_COL || mode == MX_MODE_BOTH, MX_ERR_INVALID_ARG);
+  MX_HOST_CHECK(scale_layout == MX_SCALE_PLAIN || scale_layout == MX_SCALE_SWIZZLED, MX_ERR_INVALID_ARG);
+  MX_HOST_CHECK(batch >= 1 && rows >= 1 && cols >= 1, MX_ERR_INVALID_ARG);
+  const bool row = mode & MX_MODE_ROW, col = mode & MX_MODE_COL;
+  MX_HOST_CHECK(!row || (q_row && s_row), MX_ERR_INVALID_ARG);
+  MX_HOST_CHECK(!col || (q_col && s_col), MX_ERR_INVALID_ARG);
+  MX_HOST_CHECK(cols % 32 == 0 && rows % 32 == 0, MX_ERR_SHAPE);
+  MX_HOST_CHECK(aligned16(x) && (!row || aligned16(q_row)) && (!col || aligned16(q_col)), MX_ERR_ALIGNMENT);
+  MX_HOST_CHECK(rows / QT_ROWS < 65535 && batch < 65535, MX_ERR_SHAPE);
+  mx_status st = check_device_cached();
+  if (st != MX_OK) return st;
+  QuantArgs a;
+  a.src = nullptr;
+  a.gate = nullptr;
+  a.k = 1;
+  a.x = static_cast<const uint16_t *>(x);
+  a.rows = rows;
+  a.cols = cols;
+  a.q_row = q_row;
+  a.s_row = s_row;
+  a.q_col = q_col;
+  a.s_col = s_col;
+  a.s_row_stride = mx_scale_bytes(rows, cols, scale_layout);
+  a.s_col_stride = mx_scale_bytes(cols, rows, scale_layout);
+  a.swizzled = scale_layout == MX_SCALE_SWIZZLED;
+  // swizzled layouts carry zero padding that the kernel does not visit
+  if (a.swizzled) {
+    if (row && (rows % 128 || (cols / 32) % 4))
+      MX_CUDA_TRY(cudaMemsetAsync(s_row, 0, a.s_row_stride * batch, stream));
+    if (col && (cols % 128 || (rows / 32) % 4))
+      MX_CUDA_TRY(cudaMemsetAsync(s_col, 0, a.s_col_stride * batch, stream));
+  }
+  dim3 grid((unsigned)((cols + QT_COLS - 1) / QT_COLS), (unsigned)((rows + QT_ROWS - 1) / QT_ROWS), (unsigned)batch);
+  if (row && col)
+    k_quantize_bf16<true, true, false><<<grid, QT_THREADS, 0, stream>>>(a);
+  else if (row)
+    k_quantize_bf16<true, false, false><<<grid, QT_THREADS, 0, stream>>>(a);
+  else
+    k_quantize_bf16<false, true, false><<<grid, QT_THREADS, 0, stream>>>(a);
+  return launch_status();
+}
+
+extern "C" mx_status moe_gather_quant(const void *x, const float *gate, const int32_t *src, int64_t T, int64_t H,
+                                      int32_t k, int64_t rows_cap, int32_t mode, uint8_t *q_row, uint8_t *s_row,
+                                      uint8_t *q_col, uint8_t *s_col, mx_stream stream) {
+  MX_HOST_CHECK(x && src, MX_ERR_INVALID_ARG);
+  MX_HOST_CHECK(mode == MX_MODE_ROW || mode == MX_MODE_COL || mode == MX_MODE_BOTH, MX_ERR_INVALID_ARG);
+  MX_HOST_CHECK(T >= 0 && H > 0 && k >= 1 && rows_cap >= 0, MX_ERR_INVALID_ARG);
+  const bool row = mode & MX_MODE_ROW, col = mode & MX_MODE_COL;
+  MX_HOST_CHECK(!row || (q_row && s_row), MX_ERR_INVALID_ARG);
+  MX_HOST_CHECK(!col || (q_col && s_col), MX_ERR_INVALID_ARG);
+  MX_HOST_CHECK(H % 128 == 0 && rows_cap % 128 == 0, MX_ERR_SHAPE);
+  MX_HOST_CHECK(aligned16(x) && (!row || aligned16(q_row)) && (!col || aligned16(q_col)), MX_ERR_ALIGNMENT);
+  mx_status st = check_device_cached();
+  if (st != MX_OK) return st;
+  if (rows_cap == 0) return MX_OK;
+  QuantArgs a;
+  a.x = static_cast<const uint16_t *>(x);
+  a.rows = rows_cap;
+  a.cols = H;
+  a.src = src;
+  a.gate = gate;
+  a.k = k;
+  a.q_row = q_row;
+  a.s_row = s_row;
+  a.q_col = q_col;
+  a.s_col = s_col;
+  a.s_row_stride = 0;
+  a.s_col_stride = 0;
+  a.swizzled = 1;
+  dim3 grid((unsigned)(H / QT_COLS), (unsigned)(rows_cap / QT_ROWS), 1);
+  if (row && col)
+    k_quantize_bf16<true, true, true><<<grid, QT_THREADS, 0, stream>>>(a);
+  else if (row)
+    k_quantize_bf16<true, false, true><<<grid, QT_THREADS, 0, stream>>>(a);
+  else
+    k_quantize_bf16<false, true, true><<<grid, QT_THREADS, 0, stream>>>(a);
+  return launch_status();
+}
+
+extern "C" mx_status moe_swiglu_bwd(const float *dh, const void *ab, int64_t rows, int64_t F, uint8_t *dab_rq,
+                                    uint8_t *dab_rs, uint8_t *dab_cq, uint8_t *dab_cs, uint8_t *h_cq,
+                                    uint8_t *h_cs, mx_stream stream) {
+  MX_HOST_CHECK(dh && ab && dab_rq && dab_rs && dab_cq && dab_cs && h_cq && h_cs, MX_ERR_INVALID_ARG);
+  MX_HOST_CHECK(rows >= 0 && F > 0, MX_ERR_INVALID_ARG);
+  MX_HOST_CHECK(rows % SB_ROWS == 0 && F % SB_COLS == 0, MX_ERR_SHAPE);
+  MX_HOST_CHECK(aligned16(dh) && aligned16(ab) && aligned16(dab_rq) && aligned16(dab_cq) && aligned16(h_cq),
+                MX_ERR_ALIGNMENT);
+  mx_status st = check_device_cached();
+  if (st != MX_OK) return st;
+  if (rows == 0) return MX_OK;
+  dim3 grid((unsigned)(F / SB_COLS), (unsigned)(rows / SB_ROWS));
+  k_swiglu_bwd<<<grid, 256, 0, stream>>>(dh, static_cast<const uint16_t *>(ab), rows, F, dab_rq, dab_rs, dab_cq,
+                                         dab_cs, h_cq, h_cs);
+  return launch_status();
+}

@@ -1,0 +1,106 @@
+"""The C ABI library loads, exports every function include/mxmoe.h declares,
+and rejects bad arguments on the host before touching a device.  CPU only:
+no call here launches work."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mxmoe.h")
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return set(re.findall(r"^\s*(?:const\s+)?(?:mx_status|int64_t|int32_t|char)\s*\*?\s*(\w+)\s*\(", text, re.M))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from mxfp8_mixture_experts_gb300 import _lib, build
+    build.build()
+    return _lib.load()
+
+
+def test_header_declares_the_scope_entry_points():
+    names = _declared()
+    for n in ("mx_quantize", "moe_route", "moe_permute_map", "moe_permute", "moe_unpermute", "mx_grouped_gemm",
+              "moe_gemm1_swiglu", "moe_swiglu_bwd", "moe_layer_fwd", "moe_layer_bwd", "moe_layer_prep_weights"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported_and_bound(lib):
+    from mxfp8_mixture_experts_gb300 import _lib
+    names = _declared()
+    assert names == set(_lib.SIGNATURES), names ^ set(_lib.SIGNATURES)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    for code in range(0, 9):
+        s = lib.mx_status_string(code).decode()
+        assert s.startswith("MX_")
+    assert lib.mx_abi_version() == 1
+
+
+def test_size_queries(lib):
+    assert lib.mx_scale_bytes(256, 7168, 0) == 256 * 224
+    assert lib.mx_scale_bytes(130, 96, 1) == 256 * 4
+    assert lib.mx_scale_bytes(10, 33, 0) == -1
+    assert lib.moe_rows_cap(32768, 4, 16) == (32768 * 4 + 16 * 127 + 127) // 128 * 128
+    assert lib.moe_layer_workspace_size(512, 256, 512, 4, 1) > 0
+    assert lib.moe_layer_weights_size(256, 512, 4) >= 4 * 256 * 512 * 3
+
+
+def test_host_side_argument_errors(lib):
+    from mxfp8_mixture_experts_gb300 import _lib
+    fake = C.c_void_p(1 << 20)        # never dereferenced: the checks fail first
+    odd = C.c_void_p((1 << 20) + 4)
+    # null input
+    assert lib.mx_quantize(None, 1, 64, 64, 1, 0, fake, fake, None, None, None) == _lib.MX_ERR_INVALID_ARG
+    # unknown mode / layout
+    assert lib.mx_quantize(fake, 1, 64, 64, 7, 0, fake, fake, None, None, None) == _lib.MX_ERR_INVALID_ARG
+    assert lib.mx_quantize(fake, 1, 64, 64, 1, 5, fake, fake, None, None, None) == _lib.MX_ERR_INVALID_ARG
+    # cols not a multiple of 32
+    assert lib.mx_quantize(fake, 1, 64, 48, 1, 0, fake, fake, None, None, None) == _lib.MX_ERR_SHAPE
+    # misaligned
+    assert lib.mx_quantize(odd, 1, 64, 64, 1, 0, fake, fake, None, None, None) == _lib.MX_ERR_ALIGNMENT
+    # GEMM shape rules
+    assert lib.mx_grouped_gemm(0, fake, fake, fake, fake, fake, 4, 256, 200, 256, fake, 1, None, None) == \
+        _lib.MX_ERR_SHAPE
+    assert lib.mx_grouped_gemm(0, fake, fake, fake, fake, fake, 4, 100, 256, 256, fake, 1, None, None) == \
+        _lib.MX_ERR_SHAPE
+    assert lib.mx_grouped_gemm(9, fake, fake, fake, fake, fake, 4, 256, 256, 256, fake, 1, None, None) == \
+        _lib.MX_ERR_INVALID_ARG
+    assert lib.mx_grouped_gemm(0, fake, fake, fake, fake, fake, 0, 256, 256, 256, fake, 1, None, None) == \
+        _lib.MX_ERR_INVALID_ARG
+    # permute map: rows_cap too small, workspace too small
+    assert lib.moe_permute_map(fake, 100, 2, 4, 128, fake, fake, fake, fake, fake, 1 << 20, None, None) == \
+        _lib.MX_ERR_SHAPE
+    assert lib.moe_permute_map(fake, 100, 2, 4, 1024, fake, fake, fake, fake, fake, 0, None, None) == \
+        _lib.MX_ERR_WORKSPACE
+    # layer: H must be a multiple of 256
+    assert lib.moe_layer_fwd(fake, None, fake, None, fake, 16, 128, 256, 4, 1, fake, 1 << 40, fake, None, None) == \
+        _lib.MX_ERR_SHAPE
+    # route: k > E
+    assert lib.moe_route(fake, 16, 4, 5, fake, fake, None) == _lib.MX_ERR_INVALID_ARG
+
+
+def test_package_imports_and_fails_loudly_without_library(tmp_path):
+    from mxfp8_mixture_experts_gb300 import _lib
+    with pytest.raises(ImportError):
+        _lib.load.__wrapped__(str(tmp_path / "nope.so")) if hasattr(_lib.load, "__wrapped__") else \
+            _load_fresh(str(tmp_path / "nope.so"))
+
+
+def _load_fresh(path):
+    from mxfp8_mixture_experts_gb300 import _lib
+    saved = _lib._lib
+    try:
+        _lib._lib = None
+        return _lib.load(path)
+    finally:
+        _lib._lib = saved

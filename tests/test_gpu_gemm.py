@@ -1,0 +1,243 @@
+"""Block-scaled grouped GEMM (tcgen05) on the GPU vs the oracle.
+
+* small-integer operands with unit scales and all-ones data with varied
+  scales: every product and sum is exact in fp32, so the GPU must be
+  bit-exact (pins operand and scale layouts, group boundaries, K steps);
+* random MXFP8 operands: relative Frobenius error <= 1e-4 against the fp64
+  product of the dequantized operands (fp32 outputs); bf16 outputs within
+  one bf16 ulp of the fp64 result;
+* wgrad with an empty group (exact zeros) and the fused SwiGLU epilogue;
+* the full-size grouped GEMM workload (E=8, 32768 rows, K=7168, N=2048) on
+  sampled outputs, in the launch configuration the bench times."""
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from oracle import moe, mx
+from tests.helpers import (assert_bf16_within_one_ulp, assert_bytes_equal, bits, cuda_device, quant_mismatches_outside_margin,
+                           rel_frob, to_dev_u8, u8)
+
+pytestmark = pytest.mark.gpu
+TOL = 1e-4
+
+
+@pytest.fixture(scope="module")
+def dev():
+    return cuda_device()
+
+
+def _offsets(sizes):
+    return np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+
+
+def _quant_operand(vals):
+    """[..., R, K] values -> (codes [.., R, K], swizzled scales of (prod lead * R, K)), via the oracle."""
+    v = np.asarray(vals, np.float64)
+    R, K = v.shape[-2:]
+    q, s = mx.quantize_rows(v.reshape(-1, K))
+    return q.reshape(v.shape), mx.swizzle_scales(s)
+
+
+def _deq(q, s_swz):
+    q2 = q.reshape(-1, q.shape[-1])
+    s = mx.unswizzle_scales(s_swz, q2.shape[0], q2.shape[1] // 32)
+    return mx.dequantize_rows(q2, s).reshape(q.shape)
+
+
+def _run_rows(dev, op, Aq, As, Bq, Bs, sizes, M_cap, N, K, out_dtype):
+    import mxfp8_mixture_experts_gb300 as m
+    E = len(sizes)
+    off = torch.from_numpy(_offsets(sizes)).to(dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    C = m.mx_grouped_gemm(op, to_dev_u8(Aq, dev), to_dev_u8(As, dev), to_dev_u8(Bq, dev), to_dev_u8(Bs, dev), off,
+                          E, M_cap, N, K, out_dtype, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    return C
+
+
+def _ref_rows(Aq, As, Bq, Bs, sizes, M_cap):
+    off = _offsets(sizes)
+    return moe.grouped_gemm_rows(_deq(Aq, As), _deq(Bq, Bs), off)
+
+
+SMALL_CODES = np.array([0x00, 0x30, 0x38, 0x40, 0xB0, 0xB8, 0xC0], np.uint8)   # 0, +-0.5, +-1, +-2
+
+
+@pytest.mark.parametrize("sizes,N,K", [([128], 256, 128), ([128, 0, 256], 256, 256), ([256, 384, 128], 512, 640)])
+def test_small_integer_operands_bit_exact(dev, sizes, N, K):
+    g = np.random.default_rng(sum(sizes) + N + K)
+    E = len(sizes)
+    M_cap = sum(sizes) + 128
+    Aq = g.choice(SMALL_CODES, (M_cap, K))
+    Bq = g.choice(SMALL_CODES, (E, N, K))
+    As = mx.swizzle_scales(np.full((M_cap, K // 32), 127, np.uint8))
+    Bs = mx.swizzle_scales(np.full((E * N, K // 32), 127, np.uint8))
+    C = _run_rows(dev, 0, Aq, As, Bq, Bs, sizes, M_cap, N, K, 1).cpu().numpy()
+    ref = _ref_rows(Aq, As, Bq, Bs, sizes, M_cap)
+    P = sum(sizes)
+    assert_bytes_equal(C[:P].view(np.uint32), ref[:P].astype(np.float32).view(np.uint32), "C")
+
+
+def test_scale_layout_bit_exact(dev):
+    """All-ones data, every (row, 32-block) scale drawn from 2^-3..2^3: C is a
+    sum of K/32 powers of two, exact in fp32; a misplaced scale shows."""
+    g = np.random.default_rng(2)
+    sizes, N, K = [256, 128], 512, 512
+    E, M_cap = 2, 384
+    Aq = np.full((M_cap, K), 0x38, np.uint8)
+    Bq = np.full((E, N, K), 0x38, np.uint8)
+    As = mx.swizzle_scales(g.integers(124, 131, (M_cap, K // 32)).astype(np.uint8))
+    Bs = mx.swizzle_scales(g.integers(124, 131, (E * N, K // 32)).astype(np.uint8))
+    C = _run_rows(dev, 0, Aq, As, Bq, Bs, sizes, M_cap, N, K, 1).cpu().numpy()
+    ref = _ref_rows(Aq, As, Bq, Bs, sizes, M_cap)
+    assert_bytes_equal(C[:384].view(np.uint32), ref[:384].astype(np.float32).view(np.uint32), "C")
+
+
+@pytest.mark.parametrize("out_dtype", [1, 0])
+@pytest.mark.parametrize("sizes,N,K", [([384, 0, 128, 256], 256, 1024), ([128, 512], 768, 384)])
+def test_random_operands(dev, out_dtype, sizes, N, K):
+    g = np.random.default_rng(7)
+    E = len(sizes)
+    M_cap = sum(sizes) + 256
+    A = mx.bf16_to_f64(mx.f64_to_bf16_bits(g.standard_normal((M_cap, K))))
+    W = mx.bf16_to_f64(mx.f64_to_bf16_bits(g.standard_normal((E, N, K)) * 0.02))
+    Aq, As = _quant_operand(A)
+    Bq, Bs = _quant_operand(W)
+    C = _run_rows(dev, 0, Aq, As, Bq, Bs, sizes, M_cap, N, K, out_dtype)
+    ref = _ref_rows(Aq, As, Bq, Bs, sizes, M_cap)
+    P = sum(sizes)
+    if out_dtype == 1:
+        assert rel_frob(C.cpu().numpy()[:P], ref[:P]) <= TOL
+    else:
+        assert_bf16_within_one_ulp(bits(C)[:P], ref[:P], "C bf16")
+
+
+def test_wgrad_with_empty_group(dev):
+    import mxfp8_mixture_experts_gb300 as m
+    g = np.random.default_rng(3)
+    sizes = [256, 0, 128, 384]
+    E, N, K = 4, 256, 512
+    M_cap = sum(sizes) + 128
+    X = mx.bf16_to_f64(mx.f64_to_bf16_bits(g.standard_normal((M_cap, N))))
+    Y = mx.bf16_to_f64(mx.f64_to_bf16_bits(g.standard_normal((M_cap, K))))
+    Xq, Xs = _quant_operand(X.T.copy())     # [N, M_cap], blocks along tokens
+    Yq, Ys = _quant_operand(Y.T.copy())     # [K, M_cap]
+    off = torch.from_numpy(_offsets(sizes)).to(dev)
+    C = m.mx_grouped_gemm(m.MX_GEMM_WGRAD, to_dev_u8(Xq, dev), to_dev_u8(Xs, dev), to_dev_u8(Yq, dev),
+                          to_dev_u8(Ys, dev), off, E, M_cap, N, K, m.MX_OUT_F32)
+    torch.cuda.synchronize()
+    ref = moe.grouped_gemm_tokens(_deq(Xq, Xs), _deq(Yq, Ys), _offsets(sizes))
+    Ch = C.cpu().numpy()
+    assert np.all(Ch[1] == 0)
+    for e in (0, 2, 3):
+        assert rel_frob(Ch[e], ref[e]) <= TOL
+
+
+def test_bad_offsets_set_device_status(dev):
+    import mxfp8_mixture_experts_gb300 as m
+    A = torch.zeros((256, 128), dtype=torch.uint8, device=dev)
+    As = torch.zeros(256 * 4, dtype=torch.uint8, device=dev)
+    B = torch.zeros((1, 256, 128), dtype=torch.uint8, device=dev)
+    Bs = torch.zeros(256 * 4, dtype=torch.uint8, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    off = torch.tensor([0, 100], dtype=torch.int32, device=dev)      # not a multiple of 128
+    C = torch.full((256, 256), 7.0, device=dev)
+    m.mx_grouped_gemm(0, A, As, B, Bs, off, 1, 256, 256, 128, m.MX_OUT_F32, out=C, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == m._lib.MX_ERR_DEVICE
+    assert torch.all(C == 7.0)
+
+
+def test_gemm1_swiglu_fused(dev):
+    import mxfp8_mixture_experts_gb300 as m
+    g = np.random.default_rng(5)
+    sizes, F, H = [256, 0, 128], 256, 512
+    E = len(sizes)
+    M_cap = sum(sizes) + 128
+    x = mx.bf16_to_f64(mx.f64_to_bf16_bits(g.standard_normal((M_cap, H))))
+    W13 = mx.bf16_to_f64(mx.f64_to_bf16_bits(g.standard_normal((E, H, 2 * F)) * 0.05))
+    Aq, As = _quant_operand(x)
+    Bq, Bs = _quant_operand(np.swapaxes(W13, 1, 2).copy())     # [E, 2F, H], blocks along H
+    off = torch.from_numpy(_offsets(sizes)).to(dev)
+    ab, hq, hs = m.moe_gemm1_swiglu(to_dev_u8(Aq, dev), to_dev_u8(As, dev), to_dev_u8(Bq, dev), to_dev_u8(Bs, dev),
+                                    off, E, M_cap, F, H)
+    torch.cuda.synchronize()
+    P = sum(sizes)
+    ref = moe.grouped_gemm_rows(_deq(Aq, As), _deq(Bq, Bs), _offsets(sizes))[:P]
+    abb = bits(ab)[:P]
+    assert_bf16_within_one_ulp(abb, ref, "a|b")
+    # h from the GPU's own a, b (teacher forcing), fp64 SwiGLU, then the quantizer
+    abv = mx.bf16_to_f64(abb)
+    h = moe.swiglu(abv[:, :F], abv[:, F:])
+    hs_plain = mx.unswizzle_scales(u8(hs), M_cap, F // 32)[:P]
+    quant_mismatches_outside_margin(u8(hq)[:P], hs_plain, h, "h")
+
+
+def _full_gemm_case(dev):
+    d = workloads.GEMM_DIMS
+    sizes = workloads.gemm_group_sizes(d["E"], d["M"], seed=0)
+    inp = workloads.gemm_inputs(d["E"], d["M"], d["K"], d["N"], sizes, seed=0, device=dev)
+    return d, sizes, inp
+
+
+def test_full_size_grouped_gemm_sampled(dev):
+    """E=8, 32768 routed rows in Zipf-sized groups (one empty), K=7168,
+    N=2048: forward, dgrad and wgrad on the GPU-quantized operands; 256 x 256
+    sampled outputs of each (all groups covered) against fp64."""
+    import mxfp8_mixture_experts_gb300 as m
+    d, sizes, inp = _full_gemm_case(dev)
+    E, M, K, N = d["E"], d["M"], d["K"], d["N"]
+    off_np = _offsets(sizes)
+    off = torch.from_numpy(off_np).to(dev)
+    g = np.random.default_rng(0)
+    # forward: A [M, K] rows quantized along K; B = W^T [E, N, K] along K
+    a_rq, a_rs, a_cq, a_cs = m.mx_quantize(inp["A"], m.MX_MODE_BOTH, m.MX_SCALE_SWIZZLED)
+    w_rq, w_rs, w_cq, w_cs = m.mx_quantize(inp["W"], m.MX_MODE_BOTH, m.MX_SCALE_SWIZZLED)   # [E,K,N] / [E,N,K]
+    c_rq, c_rs, c_cq, c_cs = m.mx_quantize(inp["dC"], m.MX_MODE_BOTH, m.MX_SCALE_SWIZZLED)
+    C = m.mx_grouped_gemm(m.MX_GEMM_FWD, a_rq, a_rs, w_cq, w_cs, off, E, M, N, K, m.MX_OUT_F32)
+    dA = m.mx_grouped_gemm(m.MX_GEMM_DGRAD, c_rq, c_rs, w_rq, w_rs, off, E, M, K, N, m.MX_OUT_F32)
+    dW = m.mx_grouped_gemm(m.MX_GEMM_WGRAD, c_cq, c_cs, a_cq, a_cs, off, E, M, N, K, m.MX_OUT_F32)
+    torch.cuda.synchronize()
+
+    def deq_rows(q, s, rows, inner):
+        """dequantize selected rows of a row-quantized [R, inner] operand (swizzled scales)"""
+        qh = u8(q.reshape(-1, inner)[torch.from_numpy(rows).to(dev)])
+        sf = u8(s)
+        rr, cc = np.meshgrid(rows, np.arange(inner // 32), indexing="ij")
+        return mx.dequantize_rows(qh, sf[mx.swizzled_offset(rr, cc, inner // 32)])
+
+    rows = np.sort(g.choice(M, 256, replace=False))
+    grp = np.searchsorted(off_np, rows, side="right") - 1
+    cols_n = np.sort(g.choice(N, 256, replace=False))
+    cols_k = np.sort(g.choice(K, 256, replace=False))
+    # forward
+    Ar = deq_rows(a_rq, a_rs, rows, K)
+    ref = np.empty((256, 256))
+    for i, (r, e) in enumerate(zip(rows, grp)):
+        Bsel = deq_rows(w_cq, w_cs, e * N + cols_n, K)
+        ref[i] = Bsel @ Ar[i]
+    rt = torch.from_numpy(rows).to(dev)
+    got = C[rt][:, torch.from_numpy(cols_n).to(dev)].cpu().numpy()
+    assert rel_frob(got, ref) <= TOL
+    # dgrad: dA[r, k] = sum_n dC[r, n] W[e, k, n]
+    Cr = deq_rows(c_rq, c_rs, rows, N)
+    ref = np.empty((256, 256))
+    for i, (r, e) in enumerate(zip(rows, grp)):
+        Wsel = deq_rows(w_rq, w_rs, e * K + cols_k, N)
+        ref[i] = Wsel @ Cr[i]
+    got = dA[rt][:, torch.from_numpy(cols_k).to(dev)].cpu().numpy()
+    assert rel_frob(got, ref) <= TOL
+    # wgrad: dW[e, n, k] = sum over tokens of group e of dC[t, n] A[t, k]
+    dWh = dW.cpu().numpy()
+    for e in range(E):
+        lo, hi = off_np[e], off_np[e + 1]
+        if hi == lo:
+            assert np.all(dWh[e] == 0)
+            continue
+        n_s = cols_n[:32]
+        k_s = cols_k[:32]
+        X = deq_rows(c_cq, c_cs, n_s, M)[:, lo:hi]
+        Y = deq_rows(a_cq, a_cs, k_s, M)[:, lo:hi]
+        assert rel_frob(dWh[e][np.ix_(n_s, k_s)], X @ Y.T) <= TOL

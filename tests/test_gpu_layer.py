@@ -1,0 +1,231 @@
+"""The MXFP8 MoE SwiGLU layer on the GPU vs the oracle.
+
+Stage-wise teacher forcing: each GPU stage is checked against the oracle run
+on the GPU's own inputs to that stage (an independent fp64 chain would flip
+E4M3 roundings wherever fp32 and fp64 land on different sides of a rounding
+boundary).  Integer/byte stages are bit-exact, GEMM stages meet the 1e-4
+relative Frobenius bound (fp32 outputs) or one bf16 ulp (bf16 outputs), and
+quantized SwiGLU values match except at elements within a few fp32 ulps of a
+rounding decision.  The layer entry points must reproduce the staged pipeline
+bit for bit, and the end-to-end result is reported against the independent
+oracle and as SQNR against the unquantized layer."""
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from oracle import moe, mx
+from tests.helpers import (assert_bf16_within_one_ulp, assert_bytes_equal, bits, cuda_device,
+                           quant_mismatches_outside_margin, rel_frob, u8)
+
+pytestmark = pytest.mark.gpu
+TOL = 1e-4
+
+
+@pytest.fixture(scope="module")
+def dev():
+    return cuda_device()
+
+
+def _deq_swz(q, s, rows, cols):
+    qh = u8(q).reshape(rows, cols)
+    return mx.dequantize_rows(qh, mx.unswizzle_scales(u8(s), rows, cols // 32))
+
+
+def _staged(dev, inp, d, logits):
+    """Run the layer op by op (the same calls moe_layer_fwd/bwd make) and
+    keep every intermediate."""
+    import mxfp8_mixture_experts_gb300 as m
+    T, H, F, E, k = d.T, d.H, d.F, d.E, d.k
+    W13 = torch.cat([inp["W1"], inp["W3"]], dim=2).contiguous()
+    w13_rq, w13_rs, w13_cq, w13_cs = m.mx_quantize(W13, m.MX_MODE_BOTH, m.MX_SCALE_SWIZZLED)
+    w2_rq, w2_rs, w2_cq, w2_cs = m.mx_quantize(inp["W2"], m.MX_MODE_BOTH, m.MX_SCALE_SWIZZLED)
+    if logits is not None:
+        ids, gate = m.moe_route(logits, k)
+    else:
+        ids, gate = inp["ids"], inp["gate"]
+    counts, off, dst, src = m.moe_permute_map(ids, E)
+    R = src.numel()
+    xq, xs = m.moe_permute(m.MX_PERMUTE_BF16_QUANT, inp["x"], dst, src, k, scale_layout=m.MX_SCALE_SWIZZLED)
+    ab, hq, hs = m.moe_gemm1_swiglu(xq, xs, w13_cq, w13_cs, off, E, R, F, H)
+    y = m.mx_grouped_gemm(m.MX_GEMM_FWD, hq, hs, w2_cq, w2_cs, off, E, R, H, F, m.MX_OUT_BF16)
+    out = m.moe_unpermute(y, dst, gate, T, k)
+    d_gate = m.moe_gate_grad(inp["dOut"], y, dst, k)
+    dy_rq, dy_rs, dy_cq, dy_cs = m.moe_gather_quant(inp["dOut"], gate, src, k, m.MX_MODE_BOTH)
+    dh = m.mx_grouped_gemm(m.MX_GEMM_DGRAD, dy_rq, dy_rs, w2_rq, w2_rs, off, E, R, F, H, m.MX_OUT_F32)
+    dab_rq, dab_rs, dab_cq, dab_cs, h_cq, h_cs = m.moe_swiglu_bwd(dh, ab)
+    dW2 = m.mx_grouped_gemm(m.MX_GEMM_WGRAD, h_cq, h_cs, dy_cq, dy_cs, off, E, R, F, H, m.MX_OUT_F32)
+    dxp = m.mx_grouped_gemm(m.MX_GEMM_DGRAD, dab_rq, dab_rs, w13_rq, w13_rs, off, E, R, H, 2 * F, m.MX_OUT_BF16)
+    _, _, xp_cq, xp_cs = m.moe_gather_quant(inp["x"], None, src, k, m.MX_MODE_COL)
+    dW13 = m.mx_grouped_gemm(m.MX_GEMM_WGRAD, xp_cq, xp_cs, dab_cq, dab_cs, off, E, R, H, 2 * F, m.MX_OUT_F32)
+    dX = m.moe_unpermute(dxp, dst, None, T, k)
+    torch.cuda.synchronize()
+    return {k_: v for k_, v in locals().items() if isinstance(v, torch.Tensor)} | {"R": R}
+
+
+CASES = {
+    # the tiny layer workload: T=512, H=256, E=4, F=512, top-1 uniform ids, gate 1
+    "tiny": (workloads.TINY_LAYER, "uniform"),
+    # top-2 with a softmax router over N(0,1) logits
+    "top2_router": (workloads.LayerDims(T=384, H=256, E=4, F=256, k=2), "logits"),
+}
+
+
+@pytest.mark.parametrize("case", list(CASES))
+def test_layer_stagewise(dev, case):
+    import mxfp8_mixture_experts_gb300 as m
+    dims, router = CASES[case]
+    d = m.MoELayerDims(T=dims.T, H=dims.H, F=dims.F, E=dims.E, k=dims.k)
+    inp = workloads.layer_inputs(dims, seed=3, device=dev, router=router)
+    s = _staged(dev, inp, d, inp["logits"])
+    T, H, F, E, k, R = d.T, d.H, d.F, d.E, d.k, s["R"]
+    xb, W1b, W3b, W2b, dOb = (bits(inp[n]) for n in ("x", "W1", "W3", "W2", "dOut"))
+
+    # router + map (bit-exact ids; fp32 softmax gate to a few ulps)
+    if router == "logits":
+        ids_ref, gate_ref = moe.route(inp["logits"].cpu().numpy(), k)
+        assert_bytes_equal(s["ids"].cpu().numpy(), ids_ref, "ids")
+        np.testing.assert_allclose(s["gate"].cpu().numpy(), gate_ref, rtol=2e-6)
+    ids_np = s["ids"].cpu().numpy()
+    gate_np = s["gate"].cpu().numpy()
+    counts, off, dst, src = moe.permute_map(ids_np, E)
+    assert_bytes_equal(s["off"].cpu().numpy(), off, "offsets")
+    assert_bytes_equal(s["dst"].cpu().numpy(), dst, "dst")
+    src_full = np.concatenate([src, -np.ones(R - len(src), np.int32)])
+    P = int(off[-1])
+
+    # permute + quantize x
+    xq_ref, xs_ref = mx.quantize_rows(mx.bf16_to_f64(xb))
+    assert_bytes_equal(u8(s["xq"]), moe.permute_rows(xq_ref, src_full, k), "xq")
+    assert_bytes_equal(u8(s["xs"]), mx.swizzle_scales(moe.permute_rows(xs_ref, src_full, k)), "xs")
+
+    # GEMM1 (+ SwiGLU): a|b within one bf16 ulp of fp64 on the GPU's own operands
+    W13 = np.concatenate([mx.bf16_to_f64(W1b), mx.bf16_to_f64(W3b)], axis=2)
+    w13c_q, w13c_s = mx.quantize_cols(W13)                       # [E, 2F, H]
+    xp = _deq_swz(s["xq"], s["xs"], R, H)
+    ab_ref = moe.grouped_gemm_rows(xp, mx.dequantize_rows(w13c_q, w13c_s), off)
+    ab_b = bits(s["ab"])
+    assert_bf16_within_one_ulp(ab_b[:P], ab_ref[:P], "a|b")
+    abv = mx.bf16_to_f64(ab_b[:P])
+    h = moe.swiglu(abv[:, :F], abv[:, F:])
+    quant_mismatches_outside_margin(u8(s["hq"])[:P], mx.unswizzle_scales(u8(s["hs"]), R, F // 32)[:P], h, "hq")
+
+    # GEMM2
+    w2c_q, w2c_s = mx.quantize_cols(mx.bf16_to_f64(W2b))          # [E, H, F]
+    hp = _deq_swz(s["hq"], s["hs"], R, F)
+    y_ref = moe.grouped_gemm_rows(hp, mx.dequantize_rows(w2c_q, w2c_s), off)
+    assert_bf16_within_one_ulp(bits(s["y"])[:P], y_ref[:P], "y")
+
+    # combine
+    assert_bytes_equal(bits(s["out"]), moe.unpermute(bits(s["y"]), dst, gate_np, T, k), "out")
+
+    # backward: gate gradient (fp32 dot products of H terms)
+    yv = mx.bf16_to_f64(bits(s["y"]))
+    dov = mx.bf16_to_f64(dOb)
+    rows = dst.reshape(T, k)
+    dg_ref = np.stack([np.sum(dov * yv[rows[:, j]], axis=1) for j in range(k)], axis=1)
+    dg_bound = H * 2.0 ** -24 * np.stack([np.sum(np.abs(dov * yv[rows[:, j]]), axis=1) for j in range(k)], axis=1)
+    assert np.all(np.abs(s["d_gate"].cpu().numpy() - dg_ref) <= dg_bound + 1e-30)
+
+    # dY = bf16(gate * dOut) permuted, quantized both ways (bit-exact)
+    dY = np.zeros((R, H), np.float32)
+    for j in range(k):
+        dY[rows[:, j]] = (gate_np[:, j:j + 1] * dov.astype(np.float32)).astype(np.float32)
+    dY = mx.bf16_to_f64(mx.f32_to_bf16_bits(dY))
+    q, sc = mx.quantize_rows(dY)
+    assert_bytes_equal(u8(s["dy_rq"]), q, "dY row q")
+    assert_bytes_equal(u8(s["dy_rs"]), mx.swizzle_scales(sc), "dY row s")
+    q, sc = mx.quantize_cols(dY)
+    assert_bytes_equal(u8(s["dy_cq"]), q, "dY col q")
+    assert_bytes_equal(u8(s["dy_cs"]), mx.swizzle_scales(sc), "dY col s")
+
+    # dgrad2: dh (fp32) on the GPU's quantized dY
+    w2r_q, w2r_s = mx.quantize_rows(mx.bf16_to_f64(W2b))          # [E, F, H]
+    dh_ref = moe.grouped_gemm_rows(_deq_swz(s["dy_rq"], s["dy_rs"], R, H), mx.dequantize_rows(w2r_q, w2r_s), off)
+    dh = s["dh"].cpu().numpy()
+    assert rel_frob(dh[:P], dh_ref[:P]) <= TOL
+
+    # SwiGLU backward on the GPU's dh, a, b
+    da, db = moe.swiglu_bwd(dh[:P].astype(np.float64), abv[:, :F], abv[:, F:])
+    dab = np.concatenate([da, db], axis=1)
+    quant_mismatches_outside_margin(u8(s["dab_rq"])[:P], mx.unswizzle_scales(u8(s["dab_rs"]), R, 2 * F // 32)[:P],
+                                    dab, "dab rows")
+    dab_cq_plain = u8(s["dab_cq"])[:, :P]
+    dab_cs_plain = mx.unswizzle_scales(u8(s["dab_cs"]), 2 * F, R // 32)[:, :P // 32]
+    quant_mismatches_outside_margin(dab_cq_plain, dab_cs_plain, dab.T.copy(), "dab cols")
+    quant_mismatches_outside_margin(u8(s["h_cq"])[:, :P], mx.unswizzle_scales(u8(s["h_cs"]), F, R // 32)[:, :P // 32],
+                                    h.T.copy(), "h cols")
+
+    # wgrad2 on the GPU's column-quantized h and dY
+    dW2_ref = moe.grouped_gemm_tokens(_deq_swz(s["h_cq"], s["h_cs"], F, R), _deq_swz(s["dy_cq"], s["dy_cs"], H, R), off)
+    dW2 = s["dW2"].cpu().numpy()
+    for e in range(E):
+        assert rel_frob(dW2[e], dW2_ref[e]) <= TOL if counts[e] else np.all(dW2[e] == 0)
+
+    # dgrad1
+    w13r_q, w13r_s = mx.quantize_rows(W13)                       # [E, H, 2F]
+    dxp_ref = moe.grouped_gemm_rows(_deq_swz(s["dab_rq"], s["dab_rs"], R, 2 * F), mx.dequantize_rows(w13r_q, w13r_s), off)
+    assert_bf16_within_one_ulp(bits(s["dxp"])[:P], dxp_ref[:P], "dxp")
+
+    # x permuted, column-quantized (bit-exact)
+    q, sc = mx.quantize_cols(moe.permute_rows(mx.bf16_to_f64(xb), src_full, k))
+    assert_bytes_equal(u8(s["xp_cq"]), q, "xp col q")
+    assert_bytes_equal(u8(s["xp_cs"]), mx.swizzle_scales(sc), "xp col s")
+
+    # wgrad1
+    dW13_ref = moe.grouped_gemm_tokens(_deq_swz(s["xp_cq"], s["xp_cs"], H, R),
+                                       _deq_swz(s["dab_cq"], s["dab_cs"], 2 * F, R), off)
+    dW13 = s["dW13"].cpu().numpy()
+    for e in range(E):
+        assert rel_frob(dW13[e], dW13_ref[e]) <= TOL if counts[e] else np.all(dW13[e] == 0)
+
+    # combine of the routed input gradients
+    assert_bytes_equal(bits(s["dX"]), moe.unpermute(bits(s["dxp"]), dst, None, T, k), "dX")
+
+    # the layer entry points reproduce the staged pipeline bit for bit
+    W13t = torch.cat([inp["W1"], inp["W3"]], dim=2).contiguous()
+    wq = m.moe_layer_prep_weights(W13t, inp["W2"])
+    ws = torch.empty(m.moe_layer_workspace_size(d), dtype=torch.uint8, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    if router == "logits":
+        out, ids2, gate2 = m.moe_layer_fwd(inp["x"], wq, d, ws, logits=inp["logits"], dev_status=st)
+    else:
+        out, ids2, gate2 = m.moe_layer_fwd(inp["x"], wq, d, ws, ids=inp["ids"], gate=inp["gate"], dev_status=st)
+    dX, dW13l, dW2l, dgl = m.moe_layer_bwd(inp["x"], inp["dOut"], gate2, wq, d, ws, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert torch.equal(out, s["out"]) and torch.equal(dX, s["dX"])
+    assert torch.equal(dW13l, s["dW13"]) and torch.equal(dW2l, s["dW2"]) and torch.equal(dgl, s["d_gate"])
+
+
+def test_layer_end_to_end_vs_independent_oracle(dev):
+    """No teacher forcing: the GPU layer against the oracle's own MXFP8 chain
+    (relative error reported, bounded by the rare E4M3 rounding flips), and the
+    MXFP8 error against the unquantized fp64 layer, as SQNR."""
+    import mxfp8_mixture_experts_gb300 as m
+    dims = workloads.TINY_LAYER
+    d = m.MoELayerDims(T=dims.T, H=dims.H, F=dims.F, E=dims.E, k=dims.k)
+    inp = workloads.layer_inputs(dims, seed=0, device=dev)
+    W13t = torch.cat([inp["W1"], inp["W3"]], dim=2).contiguous()
+    wq = m.moe_layer_prep_weights(W13t, inp["W2"])
+    ws = torch.empty(m.moe_layer_workspace_size(d), dtype=torch.uint8, device=dev)
+    out, _, _ = m.moe_layer_fwd(inp["x"], wq, d, ws, ids=inp["ids"], gate=inp["gate"])
+    dX, dW13, dW2, dg = m.moe_layer_bwd(inp["x"], inp["dOut"], inp["gate"], wq, d, ws)
+    torch.cuda.synchronize()
+    b = {n: bits(inp[n]) for n in ("x", "W1", "W3", "W2", "dOut")}
+    ids = inp["ids"].cpu().numpy()
+    gate = inp["gate"].cpu().numpy()
+    fq = moe.layer_forward(b["x"], b["W1"], b["W3"], b["W2"], ids, gate, quant=True)
+    bq = moe.layer_backward(fq, b["x"], b["W1"], b["W3"], b["W2"], b["dOut"])
+    fr = moe.layer_forward(b["x"], b["W1"], b["W3"], b["W2"], ids, gate, quant=False)
+    br = moe.layer_backward(fr, b["x"], b["W1"], b["W3"], b["W2"], b["dOut"])
+    got = {"out": out.float().cpu().numpy(), "dX": dX.float().cpu().numpy(),
+           "dW13": dW13.cpu().numpy(), "dW2": dW2.cpu().numpy()}
+    refq = {"out": fq["out"], "dX": bq["dX"], "dW13": np.concatenate([bq["dW1"], bq["dW3"]], 2), "dW2": bq["dW2"]}
+    refr = {"out": fr["out"], "dX": br["dX"], "dW13": np.concatenate([br["dW1"], br["dW3"]], 2), "dW2": br["dW2"]}
+    for n in got:
+        e = rel_frob(got[n], refq[n])
+        sqnr = 10 * np.log10(np.sum(refr[n] ** 2) / np.sum((refr[n] - got[n]) ** 2))
+        print(f"{n}: rel err vs MXFP8 oracle {e:.2e}, SQNR vs unquantized layer {sqnr:.1f} dB")
+        assert e < 1e-2, n
+        assert sqnr > 20, n
