@@ -254,6 +254,53 @@ def _quant_bench(dev, iters=20):
     return {"GB/s": nbytes / t / 1e9, "us": t * 1e6, "bytes": nbytes, "l2": "flushed (256 MiB write) before each launch"}
 
 
+def _gemm_bench(dev, args):
+    """Grouped GEMM workload: E=8, 32768 routed rows in Zipf-sized groups (one
+    empty), K=7168, N=2048; forward (bf16 out), dgrad (bf16 out) and wgrad
+    (fp32 out), each timed with CUDA events after warm-up, L2 flushed before
+    each launch."""
+    import mxfp8_mixture_experts_gb300 as m
+    d = workloads.GEMM_DIMS
+    E, M, K, N = d["E"], d["M"], d["K"], d["N"]
+    sizes = workloads.gemm_group_sizes(E, M, seed=0)
+    inp = workloads.gemm_inputs(E, M, K, N, sizes, seed=0, device=dev)
+    off = torch.tensor(np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32), device=dev)
+    a_rq, a_rs, a_cq, a_cs = m.mx_quantize(inp["A"], m.MX_MODE_BOTH, m.MX_SCALE_SWIZZLED)
+    w_rq, w_rs, w_cq, w_cs = m.mx_quantize(inp["W"], m.MX_MODE_BOTH, m.MX_SCALE_SWIZZLED)
+    c_rq, c_rs, c_cq, c_cs = m.mx_quantize(inp["dC"], m.MX_MODE_BOTH, m.MX_SCALE_SWIZZLED)
+    del inp
+    C = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    dA = torch.empty((M, K), dtype=torch.bfloat16, device=dev)
+    dW = torch.empty((E, N, K), dtype=torch.float32, device=dev)
+    ops = {
+        "fwd": lambda: m.mx_grouped_gemm(m.MX_GEMM_FWD, a_rq, a_rs, w_cq, w_cs, off, E, M, N, K, m.MX_OUT_BF16, out=C),
+        "dgrad": lambda: m.mx_grouped_gemm(m.MX_GEMM_DGRAD, c_rq, c_rs, w_rq, w_rs, off, E, M, K, N, m.MX_OUT_BF16,
+                                           out=dA),
+        "wgrad": lambda: m.mx_grouped_gemm(m.MX_GEMM_WGRAD, c_cq, c_cs, a_cq, a_cs, off, E, M, N, K, m.MX_OUT_F32,
+                                           out=dW),
+    }
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    s = torch.cuda.current_stream(dev)
+    flops = 2 * M * N * K
+    res = {}
+    for name, fn in ops.items():
+        times = []
+        for i in range(max(args.warmup, 1) + max(args.steps, 1)):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s)
+            fn()
+            e1.record(s)
+            torch.cuda.synchronize()
+            if i >= max(args.warmup, 1):
+                times.append(e0.elapsed_time(e1) * 1e-3)
+        t = statistics.median(times)
+        res[name] = {"TFLOP/s": flops / t / 1e12, "us": t * 1e6}
+    res["sizes"] = sizes
+    res["flops_per_op"] = flops
+    return res
+
+
 def _cpu_baseline(d_full, seconds_hint=20.0):
     """The oracle (numpy, fp64) on a bounded sample of the full-layer workload:
     one expert at the full hidden size H, a 512-wide slice of its FFN width
@@ -299,8 +346,17 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--workload", default="layer", choices=["layer", "gemm", "quantize"],
+                    help="layer: the full training step (the bench line); gemm / quantize: one kernel family "
+                         "on its own workload, for profiling")
     args = ap.parse_args()
     rank, world, local = _dist()
+    if args.workload != "layer":
+        dev = torch.device("cuda", local)
+        torch.cuda.set_device(dev)
+        r = _gemm_bench(dev, args) if args.workload == "gemm" else _quant_bench(dev, max(args.steps, 1))
+        print(json.dumps({"workload": args.workload, **r}))
+        return
 
     dims = workloads.FULL_LAYER
     config = {"workload": f"full MoE SwiGLU layer fwd+bwd: T={dims.T} tokens, H={dims.H}, E={dims.E} experts, "

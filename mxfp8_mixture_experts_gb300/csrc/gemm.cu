@@ -25,16 +25,15 @@
 //               stores (bf16, fp32, or the fused SwiGLU + MXFP8 quantize).
 // Group offsets stay on the device: every CTA walks the same static tile
 // schedule derived from them (no host synchronization).
-#include "common.cuh"
+#include "gemm_shared.cuh"
+#include <cstdlib>
 
 #include <mutex>
 
 namespace mxmoe {
 namespace gemm {
 
-constexpr int BM = 128;
-constexpr int BN = 256;
-constexpr int BK = 128;  // fp8 elements (= bytes) per row per stage
+// one-CTA variant: 128 x 256 tile per CTA, 4-stage ring
 constexpr int STAGES = 4;
 constexpr int A_TILE = BM * BK;          // 16 KB
 constexpr int B_HALF = 128 * BK;         // 16 KB (one TMA box)
@@ -42,12 +41,9 @@ constexpr int B_TILE = BN * BK;          // 32 KB
 constexpr int SF_STAGE = 512 + 1024;     // SFA chunk + two SFB chunks
 constexpr uint32_t STAGE_TX = A_TILE + B_TILE + SF_STAGE;
 constexpr int NUM_THREADS = 320;
-constexpr int NUM_EPI_WARPS = 8;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t ACC_COL = 0;
 constexpr uint32_t SF_COL = 256;  // per stage: SFA 4 columns, SFB 8 columns
-constexpr int MAX_E = 1024;
-constexpr uint64_t WAIT_TIMEOUT_NS = 2000000000ull;
 
 constexpr int SMEM_A = 0;
 constexpr int SMEM_B = SMEM_A + STAGES * A_TILE;
@@ -57,26 +53,7 @@ constexpr int SMEM_OFFS = SMEM_BAR + 256;
 constexpr int SMEM_TOTAL = SMEM_OFFS + (MAX_E + 1) * 4;
 constexpr int SMEM_ALLOC = SMEM_TOTAL + 1024;  // slack to align the base to 1024
 
-enum { EPI_BF16 = 0, EPI_F32 = 1, EPI_GLU = 2 };
-enum { OP_ROWS = 0, OP_TOKENS = 1 };
-
-struct Params {
-  int op, epi, E;
-  int64_t M_cap, N, K;  // see mx_grouped_gemm; for EPI_GLU N = F (output pairs)
-  const int32_t *offsets;
-  const uint8_t *sA, *sB;
-  void *C;
-  uint16_t *ab;
-  uint8_t *hq, *hs;
-  int32_t *dev_status;
-};
-
-// Instruction descriptor, kind::mxf8f6f4 with block scales: E4M3 x E4M3,
-// both operands K-major, UE8M0 scales, M=128, N=256; bits 4-5 and 29-30 pick
-// the byte (= 32-wide K block) of the 32-bit scale column.
-__host__ __device__ constexpr uint32_t idesc_base() {
-  return (0u << 7) | (0u << 10) | ((uint32_t)(BN >> 3) << 17) | (1u << 23) | ((uint32_t)(BM >> 4) << 24);
-}
+__host__ __device__ constexpr uint32_t idesc_base() { return idesc_mxf8(BM, BN); }
 
 struct Tile {
   int64_t a_row, b_row0, b_row1;  // TMA row coordinates
@@ -86,15 +63,6 @@ struct Tile {
   int64_t out_row, out_col;       // output position of the tile's top-left
   int e;
 };
-
-__device__ __forceinline__ int find_group(const int32_t *off, int E, int64_t row) {
-  int lo = 0, hi = E;  // largest e with off[e] <= row
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (off[mid] <= row) lo = mid; else hi = mid;
-  }
-  return lo;
-}
 
 __device__ __forceinline__ int64_t num_tiles(const Params &p, const int32_t *off) {
   if (p.op == OP_ROWS) {
@@ -110,7 +78,7 @@ __device__ __forceinline__ Tile decode_tile(const Params &p, const int32_t *off,
     const int64_t n_tiles = p.epi == EPI_GLU ? p.N / 128 : p.N / BN;
     const int64_t mt = t / n_tiles, nt = t % n_tiles;
     const int64_t row = mt * BM;
-    const int e = find_group(off, p.E, row);
+    const int e = upper_group(off, p.E, row);
     const int64_t kblocks = p.K / BK;
     tl.e = e;
     tl.a_row = row;
@@ -151,8 +119,6 @@ __device__ __forceinline__ Tile decode_tile(const Params &p, const int32_t *off,
   return tl;
 }
 
-__device__ __forceinline__ float silu_f(float a) { return a / (1.0f + expf(-a)); }
-
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     k_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, Params p) {
   extern __shared__ uint8_t smem_raw[];
@@ -169,11 +135,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   // group offsets -> shared memory, validated identically by every CTA
   for (int i = threadIdx.x; i <= p.E; i += NUM_THREADS) s_off[i] = p.offsets[i];
+  __syncthreads();
   if (threadIdx.x == 0) {
-    int ok = 1;
-    for (int i = 0; i < p.E; ++i)
-      if (s_off[i + 1] < s_off[i] || (s_off[i] & (BM - 1))) ok = 0;
-    if (s_off[0] < 0 || (s_off[p.E] & (BM - 1)) || s_off[p.E] > p.M_cap) ok = 0;
+    const int ok = offsets_ok(s_off, p.E, p.M_cap);
     *s_flag = ok;
     if (!ok && blockIdx.x == 0) set_status(p.dev_status, MX_ERR_DEVICE);
   }
@@ -293,13 +257,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const Tile tl = decode_tile(p, s_off, t);
       const int64_t orow = tl.out_row + row_in_tile;
       if (tl.num_k == 0) {  // empty wgrad group: the output block is zero
-        float *c = static_cast<float *>(p.C) + orow * p.K + tl.out_col + h * 128;
-        if (p.epi == EPI_F32) {
-          for (int j = 0; j < 32; ++j) reinterpret_cast<float4 *>(c)[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-        } else {
-          uint16_t *cb = static_cast<uint16_t *>(p.C) + orow * p.K + tl.out_col + h * 128;
-          for (int j = 0; j < 16; ++j) reinterpret_cast<uint4 *>(cb)[j] = make_uint4(0, 0, 0, 0);
-        }
+        epi_zero(p, orow, tl.out_col + h * 128);
         continue;
       }
       if (!mbar_wait_bounded(tmem_full, acc_phase, WAIT_TIMEOUT_NS)) {
@@ -325,63 +283,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(tmem_empty);
       acc_phase ^= 1;
-
-      if (p.epi == EPI_F32) {
-        const int64_t ldc = p.op == OP_ROWS ? p.N : p.K;
-        float4 *c = reinterpret_cast<float4 *>(static_cast<float *>(p.C) + orow * ldc + tl.out_col + h * 128);
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-          c[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]), __uint_as_float(r[4 * j + 2]),
-                             __uint_as_float(r[4 * j + 3]));
-      } else if (p.epi == EPI_BF16) {
-        const int64_t ldc = p.op == OP_ROWS ? p.N : p.K;
-        uint4 *c = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.C) + orow * ldc + tl.out_col + h * 128);
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const uint32_t *v = r + 8 * j;
-          c[j] = make_uint4(pack_bf16x2(__uint_as_float(v[0]), __uint_as_float(v[1])),
-                            pack_bf16x2(__uint_as_float(v[2]), __uint_as_float(v[3])),
-                            pack_bf16x2(__uint_as_float(v[4]), __uint_as_float(v[5])),
-                            pack_bf16x2(__uint_as_float(v[6]), __uint_as_float(v[7])));
-        }
-      } else {
-        // fused SwiGLU: a, b -> bf16 (saved), h = silu(a) * b -> MXFP8 (blocks along F)
-        const int64_t F = p.N;
-        const int64_t f0 = tl.out_col + h * 64;
-        uint4 *pa = reinterpret_cast<uint4 *>(p.ab + orow * 2 * F + f0);
-        uint4 *pb = reinterpret_cast<uint4 *>(p.ab + orow * 2 * F + F + f0);
-        uint4 *ph = reinterpret_cast<uint4 *>(p.hq + orow * F + f0);
-#pragma unroll
-        for (int blk = 0; blk < 2; ++blk) {
-          float hv[32];
-          uint32_t am = 0;
-#pragma unroll
-          for (int j = 0; j < 32; j += 8) {
-            float av[8], bv[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              av[i] = round_bf16(__uint_as_float(r[blk * 32 + j + i]));
-              bv[i] = round_bf16(__uint_as_float(r[64 + blk * 32 + j + i]));
-              hv[j + i] = silu_f(av[i]) * bv[i];
-              am = max(am, abs_bits(hv[j + i]));
-            }
-            pa[(blk * 32 + j) / 8] = make_uint4(pack_bf16x2(av[0], av[1]), pack_bf16x2(av[2], av[3]),
-                                                pack_bf16x2(av[4], av[5]), pack_bf16x2(av[6], av[7]));
-            pb[(blk * 32 + j) / 8] = make_uint4(pack_bf16x2(bv[0], bv[1]), pack_bf16x2(bv[2], bv[3]),
-                                                pack_bf16x2(bv[4], bv[5]), pack_bf16x2(bv[6], bv[7]));
-          }
-          const MxScale s = mx_scale_from_amax_bits(am);
-          uint32_t w[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i)
-            w[i] = s.bad ? 0x7f7f7f7fu
-                         : pack_e4m3x4(hv[4 * i] * s.inv, hv[4 * i + 1] * s.inv, hv[4 * i + 2] * s.inv,
-                                       hv[4 * i + 3] * s.inv);
-          ph[blk * 2] = make_uint4(w[0], w[1], w[2], w[3]);
-          ph[blk * 2 + 1] = make_uint4(w[4], w[5], w[6], w[7]);
-          p.hs[sf_swizzle_offset(orow, f0 / 32 + blk, round_up(F / 32, 4))] = (uint8_t)s.byte;
-        }
-      }
+      epi_store(p, orow, tl.out_col + (p.epi == EPI_GLU ? h * 64 : h * 128), r);
     }
   }
 
@@ -415,7 +317,7 @@ static EncodeTiledFn encode_fn() {
 }
 
 // 2-D uint8 map over [outer, inner] (inner contiguous), 128x128 boxes, 128-byte swizzle
-static mx_status make_map(CUtensorMap *m, const void *base, int64_t inner, int64_t outer) {
+mx_status make_map_u8_128x128(CUtensorMap *m, const void *base, int64_t inner, int64_t outer) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return MX_ERR_CUDA;
   cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
@@ -424,6 +326,37 @@ static mx_status make_map(CUtensorMap *m, const void *base, int64_t inner, int64
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MX_OK : MX_ERR_CUDA;
+}
+
+// a swizzled scale array seen as [nchunks, 128] uint32: one box = one 512-byte
+// chunk (128 rows x 4 scale columns)
+mx_status make_map_sf_chunks(CUtensorMap *m, const void *base, int64_t nchunks) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return MX_ERR_CUDA;
+  cuuint64_t dims[2] = {128, (cuuint64_t)nchunks};
+  cuuint64_t strides[1] = {512};
+  cuuint32_t box[2] = {128, 1};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void *>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MX_OK : MX_ERR_CUDA;
+}
+
+// output store map: [rows, cols] fp32 or bf16, boxes of 32 rows x 64 bytes,
+// 64-byte swizzle (matches the epilogue's staging layout)
+mx_status make_map_store_64b(CUtensorMap *m, void *base, bool f32, int64_t cols, int64_t rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return MX_ERR_CUDA;
+  const int64_t esz = f32 ? 4 : 2;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)(cols * esz)};
+  cuuint32_t box[2] = {(cuuint32_t)(64 / esz), 32};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? MX_OK : MX_ERR_CUDA;
 }
@@ -446,20 +379,39 @@ static mx_status prepare(int *num_sms) {
   return MX_OK;
 }
 
-mx_status launch(const Params &p, const uint8_t *A, int64_t a_inner, int64_t a_outer, const uint8_t *B,
-                 int64_t b_inner, int64_t b_outer, int64_t max_tiles, mx_stream stream) {
+mx_status launch_1cta(const Params &p, const uint8_t *A, int64_t a_inner, int64_t a_outer, const uint8_t *B,
+                      int64_t b_inner, int64_t b_outer, int64_t max_tiles, mx_stream stream) {
   int sms = 0;
   mx_status st = prepare(&sms);
   if (st != MX_OK) return st;
   CUtensorMap ma, mb;
-  st = make_map(&ma, A, a_inner, a_outer);
+  st = make_map_u8_128x128(&ma, A, a_inner, a_outer);
   if (st != MX_OK) return st;
-  st = make_map(&mb, B, b_inner, b_outer);
+  st = make_map_u8_128x128(&mb, B, b_inner, b_outer);
   if (st != MX_OK) return st;
   int64_t grid = max_tiles < sms ? max_tiles : sms;
   if (grid < 1) grid = 1;
   k_grouped_gemm<<<(unsigned)grid, NUM_THREADS, SMEM_ALLOC, stream>>>(ma, mb, p);
   return launch_status();
+}
+
+// Which kernel runs: the CTA-pair kernel by default; MXMOE_GEMM_CTAS=1 selects
+// the one-CTA kernel (both compute the same values).
+static bool use_pair() {
+  static int v = -1;
+  if (v < 0) {
+    const char *e = std::getenv("MXMOE_GEMM_CTAS");
+    v = (e && e[0] == '1') ? 0 : 1;
+  }
+  return v == 1;
+}
+
+static mx_status dispatch(const Params &p, const uint8_t *A, int64_t a_inner, int64_t a_outer, const uint8_t *B,
+                          int64_t b_inner, int64_t b_outer, int64_t tiles_1cta, int64_t sfa_bytes, int64_t sfb_bytes,
+                          mx_stream stream) {
+  const bool pair_ok = p.op == OP_ROWS || (p.N % 256 == 0);
+  if (use_pair() && pair_ok) return launch_pair(p, A, a_inner, a_outer, B, b_inner, b_outer, sfa_bytes, sfb_bytes, stream);
+  return launch_1cta(p, A, a_inner, a_outer, B, b_inner, b_outer, tiles_1cta, stream);
 }
 
 }  // namespace gemm
@@ -499,13 +451,13 @@ extern "C" mx_status mx_grouped_gemm(int32_t op, const uint8_t *A, const uint8_t
     if (M_cap == 0) return cudaMemsetAsync(C, 0, (size_t)E * N * K * (c_dtype == MX_OUT_F32 ? 4 : 2), stream) ==
                                    cudaSuccess ? MX_OK : MX_ERR_CUDA;
     const int64_t tiles = (int64_t)E * (N / 128) * (K / 256);
-    return gemm::launch(p, A, M_cap, N, B, M_cap, K, tiles, stream);
+    return gemm::dispatch(p, A, M_cap, N, B, M_cap, K, tiles, N * M_cap / 32, K * M_cap / 32, stream);
   }
   if (M_cap == 0) return MX_OK;
   p.op = gemm::OP_ROWS;
   p.K = K;
   const int64_t tiles = (M_cap / 128) * (N / 256);
-  return gemm::launch(p, A, K, M_cap, B, K, (int64_t)E * N, tiles, stream);
+  return gemm::dispatch(p, A, K, M_cap, B, K, (int64_t)E * N, tiles, M_cap * K / 32, (int64_t)E * N * K / 32, stream);
 }
 
 extern "C" mx_status moe_gemm1_swiglu(const uint8_t *A, const uint8_t *sA, const uint8_t *B, const uint8_t *sB,
@@ -535,5 +487,6 @@ extern "C" mx_status moe_gemm1_swiglu(const uint8_t *A, const uint8_t *sA, const
   p.hs = hs;
   p.dev_status = dev_status;
   const int64_t tiles = (M_cap / 128) * (F / 128);
-  return gemm::launch(p, A, H, M_cap, B, H, (int64_t)E * 2 * F, tiles, stream);
+  return gemm::dispatch(p, A, H, M_cap, B, H, (int64_t)E * 2 * F, tiles, M_cap * H / 32, (int64_t)E * 2 * F * H / 32,
+                        stream);
 }

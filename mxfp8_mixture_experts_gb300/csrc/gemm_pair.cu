@@ -1,0 +1,431 @@
+// Block-scaled MXFP8 grouped GEMM, CTA-pair variant (tcgen05 cta_group::2).
+//
+// Same contraction as the one-CTA kernel in gemm.cu ("1.5x faster MoE
+// training on Blackwell with MXFP8 kernels built from scratch", Key Questions
+// Answered: block-scaled tcgen05.mma with TMEM accumulators), arranged for the
+// bandwidth of one SM: two CTAs on neighbouring SMs form a cluster and compute
+// one 256 x 256 tile with M=256 MMAs.  Each CTA stages its own 128 rows of A
+// and its own 128-row half of the B tile, so one SM takes in 64 bytes of
+// operands per MMA cycle instead of the 96 a 128 x 256 one-CTA tile needs,
+// and the ring holds 6 stages instead of 4.
+//
+// Roles per CTA (320 threads): warp 0 loads (TMA, completion counted on the
+// even CTA's barrier), warp 1 of the even CTA issues the scale copies, MMAs
+// and commits for the pair, warps 2..9 drain the CTA's own 128 x 256
+// accumulator (bf16/fp32 outputs leave through swizzled shared-memory staging
+// and TMA tensor stores, so each global write is a full 64-byte row segment).
+// Row groups are 128-row aligned; a group with an odd number of
+// 128-row tiles ends in a "lone" tile, computed by the pair with both halves on
+// the same rows and stored by the even CTA only.
+#include "gemm_shared.cuh"
+
+#include <mutex>
+
+namespace mxmoe {
+namespace gemm {
+
+constexpr int P_STAGES = 5;
+constexpr int P_A_TILE = 128 * BK;                      // 16 KB: this CTA's 128 rows of A
+constexpr int P_B_TILE = 128 * BK;                      // 16 KB: this CTA's half of B
+constexpr int P_SF_STAGE = 512 + 1024;                  // own SFA chunk + both SFB chunks
+constexpr uint32_t P_STAGE_TX = P_A_TILE + P_B_TILE + P_SF_STAGE;
+constexpr int P_THREADS = 320;
+constexpr uint32_t P_TMEM_COLS = 512;
+constexpr uint32_t P_ACC_COL = 0;
+constexpr uint32_t P_SF_COL = 256;  // per stage: SFA 4 columns, SFB 8 columns
+
+constexpr int P_SMEM_A = 0;
+constexpr int P_SMEM_B = P_SMEM_A + P_STAGES * P_A_TILE;
+constexpr int P_SMEM_SF = P_SMEM_B + P_STAGES * P_B_TILE;
+constexpr int P_EPI_BUF = 2048;                        // 32 rows x 64 bytes, 64-byte swizzle
+constexpr int P_SMEM_EPI = P_SMEM_SF + P_STAGES * P_SF_STAGE;   // 2 buffers per epilogue warp
+constexpr int P_SMEM_BAR = P_SMEM_EPI + NUM_EPI_WARPS * 2 * P_EPI_BUF;
+constexpr int P_SMEM_OFFS = P_SMEM_BAR + 256;
+constexpr int P_SMEM_PP = P_SMEM_OFFS + (MAX_E + 1) * 4;
+constexpr int P_SMEM_TOTAL = P_SMEM_PP + (MAX_E + 1) * 4;
+constexpr int P_SMEM_ALLOC = P_SMEM_TOTAL + 1024;
+
+struct PairTile {
+  int64_t a_row;           // this CTA's A rows (TMA row coordinate)
+  int64_t b_row;           // this CTA's half of B
+  int64_t b_row0, b_row1;  // both halves (for the scale chunks)
+  int64_t k0;
+  int num_k;
+  int64_t sfa_chunk, sfb_chunk0, sfb_chunk1;  // chunk index of the k=0 scales
+  int64_t out_row, out_col;                   // this CTA's output rows / first column
+  bool store;                                 // false: lone tile, odd CTA
+};
+
+__device__ __forceinline__ int64_t pair_tiles(const Params &p, const int32_t *pp) {
+  if (p.op == OP_ROWS) return (int64_t)pp[p.E] * (p.epi == EPI_GLU ? p.N / 128 : p.N / BN);
+  return (int64_t)p.E * (p.N / 256) * (p.K / BN);
+}
+
+__device__ __forceinline__ PairTile decode_pair(const Params &p, const int32_t *off, const int32_t *pp, int64_t t,
+                                                uint32_t rank) {
+  PairTile tl;
+  if (p.op == OP_ROWS) {
+    const int64_t n_tiles = p.epi == EPI_GLU ? p.N / 128 : p.N / BN;
+    const int64_t pr = t / n_tiles, nt = t % n_tiles;
+    const int e = upper_group(pp, p.E, pr);
+    const int64_t j = pr - pp[e];
+    const int64_t n_e = (off[e + 1] - off[e]) / BM;
+    const int64_t mt0 = off[e] / BM + 2 * j;
+    const bool lone = (2 * j + 1 == n_e);
+    const int64_t my_mt = mt0 + (lone ? 0 : rank);
+    const int64_t kblocks = p.K / BK;
+    tl.a_row = my_mt * BM;
+    if (p.epi == EPI_GLU) {
+      tl.b_row0 = (int64_t)e * 2 * p.N + nt * 128;
+      tl.b_row1 = tl.b_row0 + p.N;
+      tl.out_col = nt * 128;
+    } else {
+      tl.b_row0 = (int64_t)e * p.N + nt * BN;
+      tl.b_row1 = tl.b_row0 + 128;
+      tl.out_col = nt * BN;
+    }
+    tl.k0 = 0;
+    tl.num_k = (int)kblocks;
+    tl.sfa_chunk = my_mt * kblocks;
+    tl.sfb_chunk0 = (tl.b_row0 / 128) * kblocks;
+    tl.sfb_chunk1 = (tl.b_row1 / 128) * kblocks;
+    tl.out_row = (mt0 + rank) * BM;
+    tl.store = !(lone && rank == 1);
+  } else {
+    const int64_t rt_n = p.N / 256, ct_n = p.K / BN;
+    const int64_t per_e = rt_n * ct_n;
+    const int e = (int)(t / per_e);
+    const int64_t rem = t % per_e;
+    const int64_t rt = rem / ct_n, ct = rem % ct_n;
+    const int64_t kblocks = p.M_cap / BK;
+    const int64_t kc0 = off[e] / BK;
+    tl.a_row = rt * 256 + rank * 128;
+    tl.b_row0 = ct * BN;
+    tl.b_row1 = tl.b_row0 + 128;
+    tl.k0 = off[e];
+    tl.num_k = (off[e + 1] - off[e]) / BK;
+    tl.sfa_chunk = (tl.a_row / 128) * kblocks + kc0;
+    tl.sfb_chunk0 = (tl.b_row0 / 128) * kblocks + kc0;
+    tl.sfb_chunk1 = (tl.b_row1 / 128) * kblocks + kc0;
+    tl.out_row = (int64_t)e * p.N + rt * 256 + rank * 128;
+    tl.out_col = ct * BN;
+    tl.store = true;
+  }
+  tl.b_row = rank == 0 ? tl.b_row0 : tl.b_row1;
+  return tl;
+}
+
+// One warp's 32 rows x 64 bytes: wait until the store that last used `buf`
+// has read it, write the rows (16-byte chunk j of row i at chunk j ^ ((i>>1)&3),
+// the 64-byte swizzle of the store map), then one lane issues the TMA store.
+__device__ __forceinline__ void stage_and_store(const CUtensorMap *map, uint8_t *buf, const uint4 (&v)[4], int lane,
+                                                int x, int y) {
+  if (lane == 0) bulk_wait_group_read<1>();
+  __syncwarp();
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    *reinterpret_cast<uint4 *>(buf + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4)) = v[j];
+  fence_proxy_async();
+  __syncwarp();
+  if (lane == 0) {
+    tma_store_2d(map, buf, x, y);
+    bulk_commit_group();
+  }
+}
+
+__global__ void __launch_bounds__(P_THREADS, 1)
+    k_grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
+                        const __grid_constant__ CUtensorMap tmC, Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + P_SMEM_BAR);
+  uint64_t *empty = full + P_STAGES;
+  uint64_t *tmem_full = empty + P_STAGES;
+  uint64_t *tmem_empty = tmem_full + 1;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tmem_empty + 1);
+  int32_t *s_flag = reinterpret_cast<int32_t *>(tmem_slot + 1);
+  int32_t *s_off = reinterpret_cast<int32_t *>(smem + P_SMEM_OFFS);
+  int32_t *s_pp = reinterpret_cast<int32_t *>(smem + P_SMEM_PP);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const int64_t cid = cluster_id_x(), ncl = nclusters_x();
+
+  for (int i = threadIdx.x; i <= p.E; i += P_THREADS) s_off[i] = p.offsets[i];
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const int ok = offsets_ok(s_off, p.E, p.M_cap);
+    *s_flag = ok;
+    if (!ok && blockIdx.x == 0) set_status(p.dev_status, MX_ERR_DEVICE);
+    // pairs of 128-row tiles per group (a trailing odd tile is a lone pair)
+    int32_t run = 0;
+    for (int e = 0; e < p.E; ++e) {
+      s_pp[e] = run;
+      run += ok ? ((s_off[e + 1] - s_off[e]) / BM + 1) / 2 : 0;
+    }
+    s_pp[p.E] = run;
+  }
+  if (warp == 0 && lane == 0) {
+    for (int s = 0; s < P_STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(tmem_full, 1);
+    mbar_init(tmem_empty, 2 * NUM_EPI_WARPS);
+    fence_mbar_init();
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+    prefetch_tmap(&tmSFA);
+    prefetch_tmap(&tmSFB);
+    if (p.epi != EPI_GLU) prefetch_tmap(&tmC);
+  }
+  __syncthreads();
+  if (!*s_flag) return;  // identical decision in both CTAs of the pair
+  if (warp == 1) {
+    tmem_alloc_pair(tmem_slot, P_TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  cluster_sync();  // barriers of both CTAs initialised, TMEM allocated in both
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int64_t ntiles = pair_tiles(p, s_pp);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer (both CTAs)
+    if (lane == 0) {
+      const uint32_t leader_full0 = mapa_shared(smem_u32(&full[0]), 0);
+      int stage = 0;
+      uint32_t phase = 0;
+      bool dead = false;
+      for (int64_t t = cid; t < ntiles && !dead; t += ncl) {
+        const PairTile tl = decode_pair(p, s_off, s_pp, t, rank);
+        for (int kb = 0; kb < tl.num_k; ++kb) {
+          if (!mbar_wait_bounded(&empty[stage], phase ^ 1, WAIT_TIMEOUT_NS)) {
+            set_status(p.dev_status, MX_ERR_TIMEOUT);
+            dead = true;
+            break;
+          }
+          if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * P_STAGE_TX);
+          const uint32_t bar = leader_full0 + stage * 8;
+          uint8_t *sa = smem + P_SMEM_A + stage * P_A_TILE;
+          uint8_t *sb = smem + P_SMEM_B + stage * P_B_TILE;
+          uint8_t *sf = smem + P_SMEM_SF + stage * P_SF_STAGE;
+          const int32_t kc = (int32_t)(tl.k0 + (int64_t)kb * BK);
+          tma_load_2d_pair(sa, &tmA, bar, kc, (int32_t)tl.a_row);
+          tma_load_2d_pair(sb, &tmB, bar, kc, (int32_t)tl.b_row);
+          tma_load_2d_pair(sf, &tmSFA, bar, 0, (int32_t)(tl.sfa_chunk + kb));
+          tma_load_2d_pair(sf + 512, &tmSFB, bar, 0, (int32_t)(tl.sfb_chunk0 + kb));
+          tma_load_2d_pair(sf + 1024, &tmSFB, bar, 0, (int32_t)(tl.sfb_chunk1 + kb));
+          if (++stage == P_STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer (even CTA)
+    if (lane == 0 && rank == 0) {
+      int stage = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool dead = false;
+      const uint32_t d_tmem = tmem_base + P_ACC_COL;
+      const uint32_t idesc = idesc_mxf8(2 * BM, BN);
+      for (int64_t t = cid; t < ntiles && !dead; t += ncl) {
+        const PairTile tl = decode_pair(p, s_off, s_pp, t, rank);
+        if (tl.num_k == 0) continue;
+        if (!mbar_wait_bounded(tmem_empty, acc_phase ^ 1, WAIT_TIMEOUT_NS)) {
+          set_status(p.dev_status, MX_ERR_TIMEOUT);
+          break;
+        }
+        tc_fence_after();
+        for (int kb = 0; kb < tl.num_k; ++kb) {
+          if (!mbar_wait_bounded(&full[stage], phase, WAIT_TIMEOUT_NS)) {
+            set_status(p.dev_status, MX_ERR_TIMEOUT);
+            dead = true;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + P_SMEM_A + stage * P_A_TILE);
+          const uint32_t sb = smem_u32(smem + P_SMEM_B + stage * P_B_TILE);
+          const uint32_t sf = smem_u32(smem + P_SMEM_SF + stage * P_SF_STAGE);
+          const uint32_t sfa_t = tmem_base + P_SF_COL + stage * 12;
+          const uint32_t sfb_t = sfa_t + 4;
+          // scales of this stage -> TMEM (in tensor-pipe order before the MMAs that read them)
+          tc_cp_32x128b_warpx4_pair(sfa_t, smem_desc(sf, 0, 128, 0));
+          tc_cp_32x128b_warpx4_pair(sfb_t, smem_desc(sf + 512, 0, 128, 0));
+          tc_cp_32x128b_warpx4_pair(sfb_t + 4, smem_desc(sf + 1024, 0, 128, 0));
+#pragma unroll
+          for (int kk = 0; kk < BK / 32; ++kk) {
+            const uint64_t ad = smem_desc(sa + kk * 32, 16, 1024, 2);
+            const uint64_t bd = smem_desc(sb + kk * 32, 16, 1024, 2);
+            const uint32_t id = idesc | ((uint32_t)kk << 4) | ((uint32_t)kk << 29);
+            tc_mma_mxf8_pair(d_tmem, ad, bd, id, sfa_t, sfb_t, (kb | kk) != 0);
+          }
+          tc_commit_pair(&empty[stage], 0x3);
+          if (++stage == P_STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (dead) break;
+        tc_commit_pair(tmem_full, 0x3);
+        acc_phase ^= 1;
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue (both CTAs)
+    const int q = warp & 3;
+    const int h = (warp - 2) >> 2;
+    const int row_in_tile = q * 32 + lane;
+    const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16) + P_ACC_COL;
+    const uint32_t leader_tmem_empty = mapa_shared(smem_u32(tmem_empty), 0);
+    uint8_t *ebuf = smem + P_SMEM_EPI + (warp - 2) * 2 * P_EPI_BUF;
+    int nstore = 0;
+    uint32_t acc_phase = 0;
+    for (int64_t t = cid; t < ntiles; t += ncl) {
+      const PairTile tl = decode_pair(p, s_off, s_pp, t, rank);
+      const int64_t orow = tl.out_row + row_in_tile;
+      if (tl.num_k == 0) {
+        epi_zero(p, orow, tl.out_col + h * 128);
+        continue;
+      }
+      if (!mbar_wait_bounded(tmem_full, acc_phase, WAIT_TIMEOUT_NS)) {
+        set_status(p.dev_status, MX_ERR_TIMEOUT);
+        break;
+      }
+      tc_fence_after();
+      uint32_t r[128];
+      if (p.epi == EPI_GLU) {
+        MX_TMEM_LD_32x32b_x32(t_row + h * 64, r);
+        MX_TMEM_LD_32x32b_x32(t_row + h * 64 + 32, (r + 32));
+        MX_TMEM_LD_32x32b_x32(t_row + 128 + h * 64, (r + 64));
+        MX_TMEM_LD_32x32b_x32(t_row + 128 + h * 64 + 32, (r + 96));
+      } else {
+        MX_TMEM_LD_32x32b_x32(t_row + h * 128, r);
+        MX_TMEM_LD_32x32b_x32(t_row + h * 128 + 32, (r + 32));
+        MX_TMEM_LD_32x32b_x32(t_row + h * 128 + 64, (r + 64));
+        MX_TMEM_LD_32x32b_x32(t_row + h * 128 + 96, (r + 96));
+      }
+      tc_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(leader_tmem_empty);
+      acc_phase ^= 1;
+      if (!tl.store) continue;
+      if (p.epi == EPI_GLU) {
+        epi_store(p, orow, tl.out_col + h * 64, r);
+        continue;
+      }
+      // 64-byte row segments: fp32 16 columns, bf16 32 columns per chunk
+      const int y = (int)(tl.out_row + q * 32);
+      const int x0 = (int)(tl.out_col + h * 128);
+      if (p.epi == EPI_F32) {
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          uint4 v[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            v[j] = make_uint4(r[c * 16 + 4 * j], r[c * 16 + 4 * j + 1], r[c * 16 + 4 * j + 2], r[c * 16 + 4 * j + 3]);
+          stage_and_store(&tmC, ebuf + (nstore & 1) * P_EPI_BUF, v, lane, x0 + c * 16, y);
+          ++nstore;
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint4 v[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint32_t *w = r + c * 32 + 8 * j;
+            v[j] = make_uint4(pack_bf16x2(__uint_as_float(w[0]), __uint_as_float(w[1])),
+                              pack_bf16x2(__uint_as_float(w[2]), __uint_as_float(w[3])),
+                              pack_bf16x2(__uint_as_float(w[4]), __uint_as_float(w[5])),
+                              pack_bf16x2(__uint_as_float(w[6]), __uint_as_float(w[7])));
+          }
+          stage_and_store(&tmC, ebuf + (nstore & 1) * P_EPI_BUF, v, lane, x0 + c * 32, y);
+          ++nstore;
+        }
+      }
+    }
+    if (lane == 0) bulk_wait_group_all();
+    __syncwarp();
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  cluster_sync();  // no MMA reads this CTA's shared memory or TMEM after this point
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, P_TMEM_COLS);
+  }
+}
+
+static std::mutex g_pmu;
+static int g_psmem_set[64];
+static int g_pclusters[64];
+
+static void pair_config(cudaLaunchConfig_t *cfg, cudaLaunchAttribute *attr, int grid, mx_stream stream) {
+  *cfg = cudaLaunchConfig_t{};
+  cfg->gridDim = dim3(grid, 1, 1);
+  cfg->blockDim = dim3(P_THREADS, 1, 1);
+  cfg->dynamicSmemBytes = P_SMEM_ALLOC;
+  cfg->stream = stream;
+  attr->id = cudaLaunchAttributeClusterDimension;
+  attr->val.clusterDim.x = 2;
+  attr->val.clusterDim.y = 1;
+  attr->val.clusterDim.z = 1;
+  cfg->attrs = attr;
+  cfg->numAttrs = 1;
+}
+
+mx_status launch_pair(const Params &p, const uint8_t *A, int64_t a_inner, int64_t a_outer, const uint8_t *B,
+                      int64_t b_inner, int64_t b_outer, int64_t sfa_bytes, int64_t sfb_bytes, mx_stream stream) {
+  int dev = 0;
+  MX_CUDA_TRY(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= 64) return MX_ERR_CUDA;
+  int clusters = 0;
+  {
+    // the persistent grid is as many CTA pairs as can be resident at once
+    std::lock_guard<std::mutex> lk(g_pmu);
+    if (!g_psmem_set[dev]) {
+      MX_CUDA_TRY(
+          cudaFuncSetAttribute(k_grouped_gemm_pair, cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM_ALLOC));
+      int sms = 0;
+      MX_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+      cudaLaunchConfig_t cfg;
+      cudaLaunchAttribute attr;
+      pair_config(&cfg, &attr, (sms / 2) * 2, nullptr);
+      int n = 0;
+      MX_CUDA_TRY(cudaOccupancyMaxActiveClusters(&n, k_grouped_gemm_pair, &cfg));
+      if (n < 1) return MX_ERR_CUDA;
+      g_pclusters[dev] = n < sms / 2 ? n : sms / 2;
+      g_psmem_set[dev] = 1;
+    }
+    clusters = g_pclusters[dev];
+  }
+  CUtensorMap ma, mb, msa, msb, mc;
+  mx_status st = make_map_u8_128x128(&ma, A, a_inner, a_outer);
+  if (st == MX_OK) st = make_map_u8_128x128(&mb, B, b_inner, b_outer);
+  if (st == MX_OK) st = make_map_sf_chunks(&msa, p.sA, sfa_bytes / 512);
+  if (st == MX_OK) st = make_map_sf_chunks(&msb, p.sB, sfb_bytes / 512);
+  if (st == MX_OK && p.epi != EPI_GLU) {
+    const int64_t rows = p.op == OP_ROWS ? p.M_cap : (int64_t)p.E * p.N;
+    const int64_t ldc = p.op == OP_ROWS ? p.N : p.K;
+    st = make_map_store_64b(&mc, p.C, p.epi == EPI_F32, ldc, rows);
+  } else {
+    mc = ma;  // unused by the SwiGLU epilogue
+  }
+  if (st != MX_OK) return st;
+  cudaLaunchConfig_t cfg;
+  cudaLaunchAttribute attr;
+  pair_config(&cfg, &attr, 2 * clusters, stream);
+  MX_CUDA_TRY(cudaLaunchKernelEx(&cfg, k_grouped_gemm_pair, ma, mb, msa, msb, mc, p));
+  return launch_status();
+}
+
+}  // namespace gemm
+}  // namespace mxmoe

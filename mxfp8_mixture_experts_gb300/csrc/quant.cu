@@ -62,6 +62,11 @@ __device__ __forceinline__ uint32_t quant32_store(const float *v, uint8_t *dst) 
 template <bool ROW, bool COL, bool GATHER>
 __global__ void __launch_bounds__(QT_THREADS) k_quantize_bf16(QuantArgs a) {
   __shared__ __align__(16) uint16_t tile[QT_ROWS][QT_COLS];
+  // COL output staged as [64 columns][128 rows] bytes (+16 pad per row: the
+  // 16-byte writes of 8 consecutive columns then fall in distinct banks)
+  __shared__ __align__(16) uint8_t qcol[QT_COLS][QT_ROWS + 16];
+  __shared__ __align__(16) uint8_t scol[QT_COLS][4];
+  constexpr int ITERS = (QT_ROWS * QT_COLS / 8) / QT_THREADS;  // 4 chunks of 8 per thread
   const int tid = threadIdx.x;
   const int64_t b = blockIdx.z;
   const int64_t row0 = (int64_t)blockIdx.y * QT_ROWS;
@@ -69,39 +74,51 @@ __global__ void __launch_bounds__(QT_THREADS) k_quantize_bf16(QuantArgs a) {
   const uint16_t *x = a.x + b * a.rows * a.cols;
   const int64_t cblocks = a.cols / 32, rblocks = a.rows / 32;
 
-  // ---- phase 1: load, ROW quant, stage ----
+  // ---- phase 0: every load of this thread in flight at once ----
+  uint4 v[ITERS];
 #pragma unroll
-  for (int it = 0; it < (QT_ROWS * QT_COLS / 8) / QT_THREADS; ++it) {
+  for (int it = 0; it < ITERS; ++it) {
     const int c = it * QT_THREADS + tid;
     const int r = c >> 3, ch = c & 7;
     const int64_t gr = row0 + r, gc = col0 + ch * 8;
     const bool valid = gr < a.rows && gc < a.cols;
-    uint4 v = make_uint4(0, 0, 0, 0);
+    v[it] = make_uint4(0, 0, 0, 0);
     if (GATHER) {
       const int32_t sidx = valid ? a.src[gr] : -1;
-      if (sidx >= 0) {
-        v = __ldg(reinterpret_cast<const uint4 *>(a.x + (int64_t)(sidx / a.k) * a.cols + gc));
-        if (a.gate) {
-          const float g = a.gate[sidx];
-          v.x = pack_bf16x2(g * bf16_lo(v.x), g * bf16_hi(v.x));
-          v.y = pack_bf16x2(g * bf16_lo(v.y), g * bf16_hi(v.y));
-          v.z = pack_bf16x2(g * bf16_lo(v.z), g * bf16_hi(v.z));
-          v.w = pack_bf16x2(g * bf16_lo(v.w), g * bf16_hi(v.w));
-        }
-      }
+      if (sidx >= 0) v[it] = __ldg(reinterpret_cast<const uint4 *>(a.x + (int64_t)(sidx / a.k) * a.cols + gc));
     } else if (valid) {
-      v = __ldg(reinterpret_cast<const uint4 *>(x + gr * a.cols + gc));
+      v[it] = __ldg(reinterpret_cast<const uint4 *>(x + gr * a.cols + gc));
     }
-    if (COL) *reinterpret_cast<uint4 *>(&tile[r][ch * 8]) = v;
+  }
+
+  // ---- phase 1: ROW quant (a 32-element block = 4 consecutive lanes), stage ----
+#pragma unroll
+  for (int it = 0; it < ITERS; ++it) {
+    const int c = it * QT_THREADS + tid;
+    const int r = c >> 3, ch = c & 7;
+    const int64_t gr = row0 + r, gc = col0 + ch * 8;
+    const bool valid = gr < a.rows && gc < a.cols;
+    uint4 w = v[it];
+    if (GATHER && a.gate) {
+      const int32_t sidx = valid ? a.src[gr] : -1;
+      if (sidx >= 0) {
+        const float g = a.gate[sidx];
+        w.x = pack_bf16x2(g * bf16_lo(w.x), g * bf16_hi(w.x));
+        w.y = pack_bf16x2(g * bf16_lo(w.y), g * bf16_hi(w.y));
+        w.z = pack_bf16x2(g * bf16_lo(w.z), g * bf16_hi(w.z));
+        w.w = pack_bf16x2(g * bf16_lo(w.w), g * bf16_hi(w.w));
+      }
+    }
+    if (COL) *reinterpret_cast<uint4 *>(&tile[r][ch * 8]) = w;
     if (ROW) {
-      float f[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
-                    bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
+      const float f[8] = {bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y),
+                          bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w)};
       uint32_t am = 0;
 #pragma unroll
       for (int i = 0; i < 8; ++i) am = max(am, abs_bits(f[i]));
       am = max(am, __shfl_xor_sync(0xffffffffu, am, 1));
       am = max(am, __shfl_xor_sync(0xffffffffu, am, 2));
-      MxScale s = mx_scale_from_amax_bits(am);
+      const MxScale s = mx_scale_from_amax_bits(am);
       uint2 o;
       o.x = s.bad ? 0x7f7f7f7fu : pack_e4m3x4(f[0] * s.inv, f[1] * s.inv, f[2] * s.inv, f[3] * s.inv);
       o.y = s.bad ? 0x7f7f7f7fu : pack_e4m3x4(f[4] * s.inv, f[5] * s.inv, f[6] * s.inv, f[7] * s.inv);
@@ -114,17 +131,46 @@ __global__ void __launch_bounds__(QT_THREADS) k_quantize_bf16(QuantArgs a) {
   if (!COL) return;
   __syncthreads();
 
-  // ---- phase 2: COL quant from shared memory ----
-  const int col = tid & (QT_COLS - 1);
-  const int rb = tid / QT_COLS;  // 0..3
-  const int64_t gc = col0 + col, gr = row0 + rb * 32;
-  if (gc >= a.cols || gr >= a.rows) return;
-  float v[32];
+  // ---- phase 2: COL quant from shared memory into the staged output ----
+  {
+    const int col = tid & (QT_COLS - 1);
+    const int rb = tid / QT_COLS;  // 0..3
+    float f[32];
 #pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float((uint32_t)tile[rb * 32 + i][col] << 16);
-  uint8_t *dst = a.q_col + b * a.rows * a.cols + gc * a.rows + gr;
-  uint32_t sb = quant32_store(v, dst);
-  store_scale(a.s_col + b * a.s_col_stride, gc, gr / 32, rblocks, a.swizzled, sb);
+    for (int i = 0; i < 32; ++i) f[i] = __uint_as_float((uint32_t)tile[rb * 32 + i][col] << 16);
+    uint32_t am = 0;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) am = max(am, abs_bits(f[i]));
+    const MxScale s = mx_scale_from_amax_bits(am);
+    uint32_t w[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      w[i] = s.bad ? 0x7f7f7f7fu
+                   : pack_e4m3x4(f[4 * i] * s.inv, f[4 * i + 1] * s.inv, f[4 * i + 2] * s.inv, f[4 * i + 3] * s.inv);
+    uint4 *dst = reinterpret_cast<uint4 *>(&qcol[col][rb * 32]);
+    dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+    scol[col][rb] = (uint8_t)s.byte;
+  }
+  __syncthreads();
+
+  // ---- phase 3: full-line writes of the transposed output and its scales ----
+  const int64_t nrows_valid = min((int64_t)QT_ROWS, a.rows - row0);  // multiple of 32
+  uint8_t *qc = a.q_col + b * a.rows * a.cols;
+#pragma unroll
+  for (int it = 0; it < (QT_COLS * QT_ROWS / 16) / QT_THREADS; ++it) {
+    const int c = it * QT_THREADS + tid;
+    const int cc = c >> 3, part = c & 7;  // 8 x 16 bytes per staged row
+    const int64_t gc = col0 + cc;
+    if (gc < a.cols && part * 16 < nrows_valid)
+      *reinterpret_cast<uint4 *>(qc + gc * a.rows + row0 + part * 16) =
+          *reinterpret_cast<const uint4 *>(&qcol[cc][part * 16]);
+  }
+  if (tid < QT_COLS && col0 + tid < a.cols) {
+    const int64_t gc = col0 + tid;
+    uint8_t *sc = a.s_col + b * a.s_col_stride;
+    for (int i = 0; i < (int)(nrows_valid / 32); ++i) store_scale(sc, gc, row0 / 32 + i, rblocks, a.swizzled, scol[tid][i]);
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -241,7 +287,7 @@ extern "C" mx_status mx_quantize(const void *x, int64_t batch, int64_t rows, int
   const bool row = mode & MX_MODE_ROW, col = mode & MX_MODE_COL;
   MX_HOST_CHECK(!row || (q_row && s_row), MX_ERR_INVALID_ARG);
   MX_HOST_CHECK(!col || (q_col && s_col), MX_ERR_INVALID_ARG);
-  MX_HOST_CHECK(cols % 32 == 0 && rows % 32 == 0, MX_ERR_SHAPE);
+  MX_HOST_CHECK(cols % 32 == 0 && (!col || rows % 32 == 0), MX_ERR_SHAPE);
   MX_HOST_CHECK(aligned16(x) && (!row || aligned16(q_row)) && (!col || aligned16(q_col)), MX_ERR_ALIGNMENT);
   MX_HOST_CHECK(rows / QT_ROWS < 65535 && batch < 65535, MX_ERR_SHAPE);
   mx_status st = check_device_cached();
