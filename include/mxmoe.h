@@ -255,7 +255,7 @@ mx_status moe_gemm1_swiglu(const uint8_t *A, const uint8_t *sA, const uint8_t *B
  *   dab_rq / dab_rs and COL (blocks of 32 rows, transposed [2F, M_cap]) into
  *   dab_cq / dab_cs; h = silu(a) * b is recomputed and quantized COL into
  *   h_cq [F, M_cap] / h_cs.  All scales MX_SCALE_SWIZZLED.
- * `rows` = rows to process (<= M_cap, multiple of 64).  F % 32 == 0.
+ * `rows` = rows to process (<= M_cap, multiple of 128).  F % 32 == 0.
  */
 mx_status moe_swiglu_bwd(const float *dh, const void *ab, int64_t rows,
                          int64_t F, uint8_t *dab_rq, uint8_t *dab_rs,

@@ -164,6 +164,28 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
   }
 }
 
+// Warp-uniform bounded wait: every lane of the warp calls it and all get the
+// same answer.  Single-thread roles (TMA issue, MMA issue) run their loops
+// with the whole warp and let one elected lane issue: a loop whose waits run
+// in one divergent lane stalls the tensor pipe between MMA batches.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity, uint64_t timeout_ns) {
+  if (__any_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    for (int i = 0; i < 64; ++i)
+      if (__any_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+    const int expired = (globaltimer_ns() - t0) > timeout_ns;
+    if (__shfl_sync(0xffffffffu, expired, 0)) return false;
+  }
+}
+
+// true in exactly one lane of the (fully active) warp
+__device__ __forceinline__ bool elect_one_sync() {
+  uint32_t pred = 0;
+  asm volatile("{\n\t.reg .pred P;\n\telect.sync _|P, 0xffffffff;\n\tselp.u32 %0, 1, 0, P;\n\t}" : "=r"(pred));
+  return pred != 0;
+}
+
 // ---------------------------------------------------------------------------
 // clusters (CTA pairs)
 // ---------------------------------------------------------------------------

@@ -166,29 +166,33 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
+    // the whole warp runs the loop; one elected lane issues the copies
+    {
       int stage = 0;
       uint32_t phase = 0;
       bool dead = false;
       for (int64_t t = blockIdx.x; t < ntiles && !dead; t += gridDim.x) {
         const Tile tl = decode_tile(p, s_off, t);
         for (int kb = 0; kb < tl.num_k; ++kb) {
-          if (!mbar_wait_bounded(&empty[stage], phase ^ 1, WAIT_TIMEOUT_NS)) {
-            set_status(p.dev_status, MX_ERR_TIMEOUT);
+          if (!mbar_wait_warp(&empty[stage], phase ^ 1, WAIT_TIMEOUT_NS)) {
+            if (lane == 0) set_status(p.dev_status, MX_ERR_TIMEOUT);
             dead = true;
             break;
           }
-          uint8_t *sa = smem + SMEM_A + stage * A_TILE;
-          uint8_t *sb = smem + SMEM_B + stage * B_TILE;
-          uint8_t *sf = smem + SMEM_SF + stage * SF_STAGE;
-          const int32_t kc = (int32_t)(tl.k0 + (int64_t)kb * BK);
-          mbar_arrive_expect_tx(&full[stage], STAGE_TX);
-          tma_load_2d(sa, &tmA, &full[stage], kc, (int32_t)tl.a_row);
-          tma_load_2d(sb, &tmB, &full[stage], kc, (int32_t)tl.b_row0);
-          tma_load_2d(sb + B_HALF, &tmB, &full[stage], kc, (int32_t)tl.b_row1);
-          bulk_load(sf, p.sA + tl.sfa_base + (int64_t)kb * 512, 512, &full[stage]);
-          bulk_load(sf + 512, p.sB + tl.sfb_base0 + (int64_t)kb * 512, 512, &full[stage]);
-          bulk_load(sf + 1024, p.sB + tl.sfb_base1 + (int64_t)kb * 512, 512, &full[stage]);
+          if (elect_one_sync()) {
+            uint8_t *sa = smem + SMEM_A + stage * A_TILE;
+            uint8_t *sb = smem + SMEM_B + stage * B_TILE;
+            uint8_t *sf = smem + SMEM_SF + stage * SF_STAGE;
+            const int32_t kc = (int32_t)(tl.k0 + (int64_t)kb * BK);
+            mbar_arrive_expect_tx(&full[stage], STAGE_TX);
+            tma_load_2d(sa, &tmA, &full[stage], kc, (int32_t)tl.a_row);
+            tma_load_2d(sb, &tmB, &full[stage], kc, (int32_t)tl.b_row0);
+            tma_load_2d(sb + B_HALF, &tmB, &full[stage], kc, (int32_t)tl.b_row1);
+            bulk_load(sf, p.sA + tl.sfa_base + (int64_t)kb * 512, 512, &full[stage]);
+            bulk_load(sf + 512, p.sB + tl.sfb_base0 + (int64_t)kb * 512, 512, &full[stage]);
+            bulk_load(sf + 1024, p.sB + tl.sfb_base1 + (int64_t)kb * 512, 512, &full[stage]);
+          }
+          __syncwarp();
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1;
@@ -199,7 +203,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // the whole warp runs the loop and waits; one elected lane issues
+    {
       int stage = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool dead = false;
@@ -207,18 +212,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       for (int64_t t = blockIdx.x; t < ntiles && !dead; t += gridDim.x) {
         const Tile tl = decode_tile(p, s_off, t);
         if (tl.num_k == 0) continue;
-        if (!mbar_wait_bounded(tmem_empty, acc_phase ^ 1, WAIT_TIMEOUT_NS)) {
-          set_status(p.dev_status, MX_ERR_TIMEOUT);
+        if (!mbar_wait_warp(tmem_empty, acc_phase ^ 1, WAIT_TIMEOUT_NS)) {
+          if (lane == 0) set_status(p.dev_status, MX_ERR_TIMEOUT);
           break;
         }
         tc_fence_after();
         for (int kb = 0; kb < tl.num_k; ++kb) {
-          if (!mbar_wait_bounded(&full[stage], phase, WAIT_TIMEOUT_NS)) {
-            set_status(p.dev_status, MX_ERR_TIMEOUT);
+          if (!mbar_wait_warp(&full[stage], phase, WAIT_TIMEOUT_NS)) {
+            if (lane == 0) set_status(p.dev_status, MX_ERR_TIMEOUT);
             dead = true;
             break;
           }
           tc_fence_after();
+          if (elect_one_sync()) {
           const uint32_t sa = smem_u32(smem + SMEM_A + stage * A_TILE);
           const uint32_t sb = smem_u32(smem + SMEM_B + stage * B_TILE);
           const uint32_t sf = smem_u32(smem + SMEM_SF + stage * SF_STAGE);
@@ -235,13 +241,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tc_mma_mxf8(d_tmem, ad, bd, id, sfa_t, sfb_t, (kb | kk) != 0);
           }
           tc_commit(&empty[stage]);
+          }
+          __syncwarp();
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1;
           }
         }
         if (dead) break;
-        tc_commit(tmem_full);
+        if (elect_one_sync()) tc_commit(tmem_full);
+        __syncwarp();
         acc_phase ^= 1;
       }
     }
@@ -260,8 +269,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         epi_zero(p, orow, tl.out_col + h * 128);
         continue;
       }
-      if (!mbar_wait_bounded(tmem_full, acc_phase, WAIT_TIMEOUT_NS)) {
-        set_status(p.dev_status, MX_ERR_TIMEOUT);
+      if (!mbar_wait_warp(tmem_full, acc_phase, WAIT_TIMEOUT_NS)) {
+        if (lane == 0) set_status(p.dev_status, MX_ERR_TIMEOUT);
         break;
       }
       tc_fence_after();
@@ -318,6 +327,10 @@ static EncodeTiledFn encode_fn() {
 
 // 2-D uint8 map over [outer, inner] (inner contiguous), 128x128 boxes, 128-byte swizzle
 mx_status make_map_u8_128x128(CUtensorMap *m, const void *base, int64_t inner, int64_t outer) {
+  return make_map_u8_128x128_swz(m, base, inner, outer, (int)CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+mx_status make_map_u8_128x128_swz(CUtensorMap *m, const void *base, int64_t inner, int64_t outer, int swizzle) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return MX_ERR_CUDA;
   cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
@@ -325,7 +338,7 @@ mx_status make_map_u8_128x128(CUtensorMap *m, const void *base, int64_t inner, i
   cuuint32_t box[2] = {128, 128};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, (CUtensorMapSwizzle)swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? MX_OK : MX_ERR_CUDA;
 }

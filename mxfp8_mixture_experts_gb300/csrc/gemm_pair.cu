@@ -194,7 +194,8 @@ __global__ void __launch_bounds__(P_THREADS, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer (both CTAs)
-    if (lane == 0) {
+    // the whole warp runs the loop; one elected lane issues the copies
+    {
       const uint32_t leader_full0 = mapa_shared(smem_u32(&full[0]), 0);
       int stage = 0;
       uint32_t phase = 0;
@@ -202,22 +203,25 @@ __global__ void __launch_bounds__(P_THREADS, 1)
       for (int64_t t = cid; t < ntiles && !dead; t += ncl) {
         const PairTile tl = decode_pair(p, s_off, s_pp, t, rank);
         for (int kb = 0; kb < tl.num_k; ++kb) {
-          if (!mbar_wait_bounded(&empty[stage], phase ^ 1, WAIT_TIMEOUT_NS)) {
-            set_status(p.dev_status, MX_ERR_TIMEOUT);
+          if (!mbar_wait_warp(&empty[stage], phase ^ 1, WAIT_TIMEOUT_NS)) {
+            if (lane == 0) set_status(p.dev_status, MX_ERR_TIMEOUT);
             dead = true;
             break;
           }
-          if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * P_STAGE_TX);
-          const uint32_t bar = leader_full0 + stage * 8;
-          uint8_t *sa = smem + P_SMEM_A + stage * P_A_TILE;
-          uint8_t *sb = smem + P_SMEM_B + stage * P_B_TILE;
-          uint8_t *sf = smem + P_SMEM_SF + stage * P_SF_STAGE;
-          const int32_t kc = (int32_t)(tl.k0 + (int64_t)kb * BK);
-          tma_load_2d_pair(sa, &tmA, bar, kc, (int32_t)tl.a_row);
-          tma_load_2d_pair(sb, &tmB, bar, kc, (int32_t)tl.b_row);
-          tma_load_2d_pair(sf, &tmSFA, bar, 0, (int32_t)(tl.sfa_chunk + kb));
-          tma_load_2d_pair(sf + 512, &tmSFB, bar, 0, (int32_t)(tl.sfb_chunk0 + kb));
-          tma_load_2d_pair(sf + 1024, &tmSFB, bar, 0, (int32_t)(tl.sfb_chunk1 + kb));
+          if (elect_one_sync()) {
+            if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * P_STAGE_TX);
+            const uint32_t bar = leader_full0 + stage * 8;
+            uint8_t *sa = smem + P_SMEM_A + stage * P_A_TILE;
+            uint8_t *sb = smem + P_SMEM_B + stage * P_B_TILE;
+            uint8_t *sf = smem + P_SMEM_SF + stage * P_SF_STAGE;
+            const int32_t kc = (int32_t)(tl.k0 + (int64_t)kb * BK);
+            tma_load_2d_pair(sa, &tmA, bar, kc, (int32_t)tl.a_row);
+            tma_load_2d_pair(sb, &tmB, bar, kc, (int32_t)tl.b_row);
+            tma_load_2d_pair(sf, &tmSFA, bar, 0, (int32_t)(tl.sfa_chunk + kb));
+            tma_load_2d_pair(sf + 512, &tmSFB, bar, 0, (int32_t)(tl.sfb_chunk0 + kb));
+            tma_load_2d_pair(sf + 1024, &tmSFB, bar, 0, (int32_t)(tl.sfb_chunk1 + kb));
+          }
+          __syncwarp();
           if (++stage == P_STAGES) {
             stage = 0;
             phase ^= 1;
@@ -228,7 +232,8 @@ __global__ void __launch_bounds__(P_THREADS, 1)
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (even CTA)
-    if (lane == 0 && rank == 0) {
+    // the whole warp runs the loop and waits; one elected lane issues
+    if (rank == 0) {
       int stage = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool dead = false;
@@ -237,18 +242,19 @@ __global__ void __launch_bounds__(P_THREADS, 1)
       for (int64_t t = cid; t < ntiles && !dead; t += ncl) {
         const PairTile tl = decode_pair(p, s_off, s_pp, t, rank);
         if (tl.num_k == 0) continue;
-        if (!mbar_wait_bounded(tmem_empty, acc_phase ^ 1, WAIT_TIMEOUT_NS)) {
-          set_status(p.dev_status, MX_ERR_TIMEOUT);
+        if (!mbar_wait_warp(tmem_empty, acc_phase ^ 1, WAIT_TIMEOUT_NS)) {
+          if (lane == 0) set_status(p.dev_status, MX_ERR_TIMEOUT);
           break;
         }
         tc_fence_after();
         for (int kb = 0; kb < tl.num_k; ++kb) {
-          if (!mbar_wait_bounded(&full[stage], phase, WAIT_TIMEOUT_NS)) {
-            set_status(p.dev_status, MX_ERR_TIMEOUT);
+          if (!mbar_wait_warp(&full[stage], phase, WAIT_TIMEOUT_NS)) {
+            if (lane == 0) set_status(p.dev_status, MX_ERR_TIMEOUT);
             dead = true;
             break;
           }
           tc_fence_after();
+          if (elect_one_sync()) {
           const uint32_t sa = smem_u32(smem + P_SMEM_A + stage * P_A_TILE);
           const uint32_t sb = smem_u32(smem + P_SMEM_B + stage * P_B_TILE);
           const uint32_t sf = smem_u32(smem + P_SMEM_SF + stage * P_SF_STAGE);
@@ -266,13 +272,16 @@ __global__ void __launch_bounds__(P_THREADS, 1)
             tc_mma_mxf8_pair(d_tmem, ad, bd, id, sfa_t, sfb_t, (kb | kk) != 0);
           }
           tc_commit_pair(&empty[stage], 0x3);
+          }
+          __syncwarp();
           if (++stage == P_STAGES) {
             stage = 0;
             phase ^= 1;
           }
         }
         if (dead) break;
-        tc_commit_pair(tmem_full, 0x3);
+        if (elect_one_sync()) tc_commit_pair(tmem_full, 0x3);
+        __syncwarp();
         acc_phase ^= 1;
       }
     }
@@ -294,8 +303,8 @@ __global__ void __launch_bounds__(P_THREADS, 1)
         epi_zero(p, orow, tl.out_col + h * 128);
         continue;
       }
-      if (!mbar_wait_bounded(tmem_full, acc_phase, WAIT_TIMEOUT_NS)) {
-        set_status(p.dev_status, MX_ERR_TIMEOUT);
+      if (!mbar_wait_warp(tmem_full, acc_phase, WAIT_TIMEOUT_NS)) {
+        if (lane == 0) set_status(p.dev_status, MX_ERR_TIMEOUT);
         break;
       }
       tc_fence_after();

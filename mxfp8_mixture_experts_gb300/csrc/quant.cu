@@ -175,42 +175,59 @@ __global__ void __launch_bounds__(QT_THREADS) k_quantize_bf16(QuantArgs a) {
 
 // ---------------------------------------------------------------------------
 // SwiGLU backward + quantization (see moe_swiglu_bwd in mxmoe.h).
-// Tile: 64 rows x 32 columns of F.  Phase 1: per (row, 8-column chunk)
-// compute da, db, h in fp32, ROW-quantize da and db (4 lanes per block), and
-// stage da, db, h in shared memory; phase 2: COL-quantize the three matrices.
+// Tile: 128 rows x 32 columns of F, 256 threads.
+//   phase 1  two (row, 8-column) chunks per thread, all loads issued first;
+//            da, db, h in fp32; ROW quant of da and db (4 lanes per block);
+//            da, db, h staged in shared memory;
+//   phase 2  COL quant of the three staged matrices (32 x 4 column blocks
+//            each) into a staged transposed tile;
+//   phase 3  full 128-byte line writes of the transposed tiles and their
+//            scales.
 // ---------------------------------------------------------------------------
-constexpr int SB_ROWS = 64;
+constexpr int SB_ROWS = 128;
 constexpr int SB_COLS = 32;
+constexpr int SB_THREADS = 256;
+constexpr int SB_VAL_STRIDE = SB_COLS + 1;            // fp32 staging row (padded)
+constexpr int SB_Q_STRIDE = SB_ROWS + 16;             // transposed byte row (padded)
+constexpr int SB_SMEM = 3 * SB_ROWS * SB_VAL_STRIDE * 4 + 3 * SB_COLS * SB_Q_STRIDE + 3 * SB_COLS * 4;
 
 __device__ __forceinline__ float sigmoidf_(float a) { return 1.0f / (1.0f + expf(-a)); }
 
-__global__ void __launch_bounds__(256) k_swiglu_bwd(const float *__restrict__ dh, const uint16_t *__restrict__ ab,
-                                                    int64_t rows, int64_t F, uint8_t *dab_rq, uint8_t *dab_rs,
-                                                    uint8_t *dab_cq, uint8_t *dab_cs, uint8_t *h_cq,
-                                                    uint8_t *h_cs) {
-  __shared__ float s_da[SB_ROWS][SB_COLS + 1];
-  __shared__ float s_db[SB_ROWS][SB_COLS + 1];
-  __shared__ float s_h[SB_ROWS][SB_COLS + 1];
+__global__ void __launch_bounds__(SB_THREADS) k_swiglu_bwd(const float *__restrict__ dh, const uint16_t *__restrict__ ab,
+                                                           int64_t rows, int64_t F, uint8_t *dab_rq, uint8_t *dab_rs,
+                                                           uint8_t *dab_cq, uint8_t *dab_cs, uint8_t *h_cq,
+                                                           uint8_t *h_cs) {
+  extern __shared__ __align__(16) uint8_t sb_smem[];
+  float *vals = reinterpret_cast<float *>(sb_smem);                          // [3][128][33]
+  uint8_t *qst = sb_smem + 3 * SB_ROWS * SB_VAL_STRIDE * 4;                    // [3][32][144]
+  uint8_t *sst = qst + 3 * SB_COLS * SB_Q_STRIDE;                             // [3][32][4]
   const int tid = threadIdx.x;
   const int64_t row0 = (int64_t)blockIdx.y * SB_ROWS;
   const int64_t f0 = (int64_t)blockIdx.x * SB_COLS;
   const int64_t twoF = 2 * F;
   const int64_t cb2 = twoF / 32;
 
+  float4 d0[2], d1[2];
+  uint4 av[2], bv[2];
 #pragma unroll
-  for (int it = 0; it < 1; ++it) {
-    const int c = it * 256 + tid;  // 256 chunks: 64 rows x 4 chunks of 8
+  for (int it = 0; it < 2; ++it) {  // 512 chunks: 128 rows x 4 chunks of 8
+    const int c = it * SB_THREADS + tid;
+    const int64_t gr = row0 + (c >> 2), gf = f0 + (c & 3) * 8;
+    d0[it] = *reinterpret_cast<const float4 *>(dh + gr * F + gf);
+    d1[it] = *reinterpret_cast<const float4 *>(dh + gr * F + gf + 4);
+    av[it] = *reinterpret_cast<const uint4 *>(ab + gr * twoF + gf);
+    bv[it] = *reinterpret_cast<const uint4 *>(ab + gr * twoF + F + gf);
+  }
+#pragma unroll
+  for (int it = 0; it < 2; ++it) {
+    const int c = it * SB_THREADS + tid;
     const int r = c >> 2, ch = c & 3;
     const int64_t gr = row0 + r, gf = f0 + ch * 8;
-    const float4 d0 = *reinterpret_cast<const float4 *>(dh + gr * F + gf);
-    const float4 d1 = *reinterpret_cast<const float4 *>(dh + gr * F + gf + 4);
-    const uint4 av = *reinterpret_cast<const uint4 *>(ab + gr * twoF + gf);
-    const uint4 bv = *reinterpret_cast<const uint4 *>(ab + gr * twoF + F + gf);
-    const float d[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
-    const float A[8] = {bf16_lo(av.x), bf16_hi(av.x), bf16_lo(av.y), bf16_hi(av.y),
-                        bf16_lo(av.z), bf16_hi(av.z), bf16_lo(av.w), bf16_hi(av.w)};
-    const float B[8] = {bf16_lo(bv.x), bf16_hi(bv.x), bf16_lo(bv.y), bf16_hi(bv.y),
-                        bf16_lo(bv.z), bf16_hi(bv.z), bf16_lo(bv.w), bf16_hi(bv.w)};
+    const float d[8] = {d0[it].x, d0[it].y, d0[it].z, d0[it].w, d1[it].x, d1[it].y, d1[it].z, d1[it].w};
+    const float A[8] = {bf16_lo(av[it].x), bf16_hi(av[it].x), bf16_lo(av[it].y), bf16_hi(av[it].y),
+                        bf16_lo(av[it].z), bf16_hi(av[it].z), bf16_lo(av[it].w), bf16_hi(av[it].w)};
+    const float B[8] = {bf16_lo(bv[it].x), bf16_hi(bv[it].x), bf16_lo(bv[it].y), bf16_hi(bv[it].y),
+                        bf16_lo(bv[it].z), bf16_hi(bv[it].z), bf16_lo(bv[it].w), bf16_hi(bv[it].w)};
     float da[8], db[8];
     uint32_t ama = 0, amb = 0;
 #pragma unroll
@@ -219,9 +236,9 @@ __global__ void __launch_bounds__(256) k_swiglu_bwd(const float *__restrict__ dh
       const float silu = A[i] * s;
       da[i] = d[i] * B[i] * s * (1.0f + A[i] * (1.0f - s));
       db[i] = d[i] * silu;
-      s_da[r][ch * 8 + i] = da[i];
-      s_db[r][ch * 8 + i] = db[i];
-      s_h[r][ch * 8 + i] = silu * B[i];
+      vals[(0 * SB_ROWS + r) * SB_VAL_STRIDE + ch * 8 + i] = da[i];
+      vals[(1 * SB_ROWS + r) * SB_VAL_STRIDE + ch * 8 + i] = db[i];
+      vals[(2 * SB_ROWS + r) * SB_VAL_STRIDE + ch * 8 + i] = silu * B[i];
       ama = max(ama, abs_bits(da[i]));
       amb = max(amb, abs_bits(db[i]));
     }
@@ -244,25 +261,54 @@ __global__ void __launch_bounds__(256) k_swiglu_bwd(const float *__restrict__ dh
   }
   __syncthreads();
 
-  // COL: 3 matrices x 32 columns x 2 row blocks = 192 items
-  const int64_t rblocks_total = rows / 32;
-  for (int item = tid; item < 3 * SB_COLS * (SB_ROWS / 32); item += 256) {
-    const int m = item / (SB_COLS * (SB_ROWS / 32));
-    const int rem = item % (SB_COLS * (SB_ROWS / 32));
+  // COL: 3 matrices x 32 columns x 4 row blocks = 384 items
+  for (int item = tid; item < 3 * SB_COLS * 4; item += SB_THREADS) {
+    const int m = item / (SB_COLS * 4);
+    const int rem = item % (SB_COLS * 4);
     const int col = rem % SB_COLS, rb = rem / SB_COLS;
     float v[32];
-    const float(*src)[SB_COLS + 1] = m == 0 ? s_da : (m == 1 ? s_db : s_h);
 #pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = src[rb * 32 + i][col];
-    const int64_t gr = row0 + rb * 32;
+    for (int i = 0; i < 32; ++i) v[i] = vals[(m * SB_ROWS + rb * 32 + i) * SB_VAL_STRIDE + col];
+    uint32_t am = 0;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) am = max(am, abs_bits(v[i]));
+    const MxScale s = mx_scale_from_amax_bits(am);
+    uint32_t w[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      w[i] = s.bad ? 0x7f7f7f7fu
+                   : pack_e4m3x4(v[4 * i] * s.inv, v[4 * i + 1] * s.inv, v[4 * i + 2] * s.inv, v[4 * i + 3] * s.inv);
+    uint4 *dst = reinterpret_cast<uint4 *>(qst + (m * SB_COLS + col) * SB_Q_STRIDE + rb * 32);
+    dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+    sst[(m * SB_COLS + col) * 4 + rb] = (uint8_t)s.byte;
+  }
+  __syncthreads();
+
+  // full-line writes: 3 x 32 transposed rows of 128 bytes
+  const int64_t rblocks_total = rows / 32;
+#pragma unroll
+  for (int it = 0; it < (3 * SB_COLS * 8) / SB_THREADS; ++it) {
+    const int c = it * SB_THREADS + tid;
+    const int mr = c >> 3, part = c & 7;  // mr = m * 32 + col
+    const int m = mr / SB_COLS, col = mr % SB_COLS;
+    const uint4 val = *reinterpret_cast<const uint4 *>(qst + mr * SB_Q_STRIDE + part * 16);
     if (m < 2) {
-      const int64_t orow = (m == 0 ? 0 : F) + f0 + col;  // row of the transposed [2F, rows] output
-      const uint32_t sb = quant32_store(v, dab_cq + orow * rows + gr);
-      dab_cs[sf_swizzle_offset(orow, gr / 32, round_up(rblocks_total, 4))] = (uint8_t)sb;
+      const int64_t orow = (m == 0 ? 0 : F) + f0 + col;
+      *reinterpret_cast<uint4 *>(dab_cq + orow * rows + row0 + part * 16) = val;
     } else {
-      const int64_t orow = f0 + col;
-      const uint32_t sb = quant32_store(v, h_cq + orow * rows + gr);
-      h_cs[sf_swizzle_offset(orow, gr / 32, round_up(rblocks_total, 4))] = (uint8_t)sb;
+      *reinterpret_cast<uint4 *>(h_cq + (f0 + col) * rows + row0 + part * 16) = val;
+    }
+  }
+  if (tid < 3 * SB_COLS) {
+    const int m = tid / SB_COLS, col = tid % SB_COLS;
+    const uint32_t sc = *reinterpret_cast<const uint32_t *>(sst + tid * 4);
+    // 4 consecutive row blocks of one transposed row: 4 contiguous bytes of the tiled layout
+    if (m < 2) {
+      const int64_t orow = (m == 0 ? 0 : F) + f0 + col;
+      *reinterpret_cast<uint32_t *>(dab_cs + sf_swizzle_offset(orow, row0 / 32, round_up(rblocks_total, 4))) = sc;
+    } else {
+      *reinterpret_cast<uint32_t *>(h_cs + sf_swizzle_offset(f0 + col, row0 / 32, round_up(rblocks_total, 4))) = sc;
     }
   }
 }
@@ -372,8 +418,15 @@ extern "C" mx_status moe_swiglu_bwd(const float *dh, const void *ab, int64_t row
   mx_status st = check_device_cached();
   if (st != MX_OK) return st;
   if (rows == 0) return MX_OK;
+  static int smem_set[64];
+  int dev = 0;
+  MX_CUDA_TRY(cudaGetDevice(&dev));
+  if (dev >= 0 && dev < 64 && !smem_set[dev]) {
+    MX_CUDA_TRY(cudaFuncSetAttribute(k_swiglu_bwd, cudaFuncAttributeMaxDynamicSharedMemorySize, SB_SMEM));
+    smem_set[dev] = 1;
+  }
   dim3 grid((unsigned)(F / SB_COLS), (unsigned)(rows / SB_ROWS));
-  k_swiglu_bwd<<<grid, 256, 0, stream>>>(dh, static_cast<const uint16_t *>(ab), rows, F, dab_rq, dab_rs, dab_cq,
-                                         dab_cs, h_cq, h_cs);
+  k_swiglu_bwd<<<grid, SB_THREADS, SB_SMEM, stream>>>(dh, static_cast<const uint16_t *>(ab), rows, F, dab_rq, dab_rs,
+                                                      dab_cq, dab_cs, h_cq, h_cs);
   return launch_status();
 }
