@@ -57,6 +57,7 @@ typedef struct CUstream_st *mx_stream; /* same type as cudaStream_t */
 #define MX_ERR_DEVICE 6             /* device-detected: id out of range, bad offsets */
 #define MX_ERR_TIMEOUT 7            /* device-detected: a bounded pipeline wait expired */
 #define MX_ERR_WORKSPACE 8          /* workspace smaller than the size query returned */
+#define MX_ERR_SCRATCH_LIMIT 9      /* problem needs more than an allocation-free entry point's fixed scratch */
 
 /* quantize modes */
 #define MX_MODE_ROW 1   /* blocks of 32 along each row                         */
@@ -157,6 +158,34 @@ mx_status moe_permute_map(const int32_t *ids, int64_t T, int32_t k, int32_t E,
                           int32_t *dst, int32_t *src, void *workspace,
                           int64_t workspace_bytes, int32_t *dev_status,
                           mx_stream stream);
+
+/*
+ * Allocation-free variant of moe_permute_map (no counterpart on the pages: it
+ * is a packaging choice of this library).  Same arguments and results as
+ * moe_permute_map, minus the workspace: it is for callers that cannot hand
+ * the library any scratch buffer -- code that only owns the input and output
+ * buffers it was given (a plugin or callback inside another framework whose
+ * device allocator it may not call, or a runtime with a fixed memory budget
+ * decided up front).  Its scratch is a fixed array in the library's own
+ * device memory, MOE_NOALLOC_SCRATCH_BYTES bytes, which every GPU that loads
+ * the library keeps until the process exits:
+ *   - problems whose moe_permute_map_workspace_size(T, k, E) exceeds that
+ *     size are rejected with MX_ERR_SCRATCH_LIMIT before anything runs
+ *     (2 * ceil(T*k / 1024) * E * 4 bytes: e.g. E = 16 allows T*k up to 2M);
+ *   - the first call on each device looks the array's address up (a runtime
+ *     call with that device current), so make that first call before any
+ *     stream capture;
+ *   - all calls on a device share the one array: calls whose work overlaps on
+ *     the GPU (different streams, no ordering between them) race and corrupt
+ *     each other's results; order them on one stream or with events;
+ *   - every call fully rewrites the scratch it reads, so nothing in it has to
+ *     start at zero; the library itself never allocates or frees memory here.
+ */
+#define MOE_NOALLOC_SCRATCH_BYTES (256 * 1024)
+mx_status moe_permute_map_noalloc(const int32_t *ids, int64_t T, int32_t k,
+                                  int32_t E, int64_t rows_cap, int32_t *counts,
+                                  int32_t *offsets, int32_t *dst, int32_t *src,
+                                  int32_t *dev_status, mx_stream stream);
 
 /* ------------------------------------------------------------------------ */
 /* P2: token permute ([B] Next steps: an MXFP8 token shuffle)               */

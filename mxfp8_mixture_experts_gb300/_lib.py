@@ -21,6 +21,7 @@ MX_ERR_CUDA = 5
 MX_ERR_DEVICE = 6
 MX_ERR_TIMEOUT = 7
 MX_ERR_WORKSPACE = 8
+MX_ERR_SCRATCH_LIMIT = 9
 MX_MODE_ROW, MX_MODE_COL, MX_MODE_BOTH = 1, 2, 3
 MX_SCALE_PLAIN, MX_SCALE_SWIZZLED = 0, 1
 MX_GEMM_FWD, MX_GEMM_DGRAD, MX_GEMM_WGRAD = 0, 1, 2
@@ -42,6 +43,7 @@ SIGNATURES = {
     "moe_rows_cap": (_i64, [_i64, _i32, _i32]),
     "moe_permute_map_workspace_size": (_i64, [_i64, _i32, _i32]),
     "moe_permute_map": (_i32, [_p, _i64, _i32, _i32, _i64, _p, _p, _p, _p, _p, _i64, _p, _p]),
+    "moe_permute_map_noalloc": (_i32, [_p, _i64, _i32, _i32, _i64, _p, _p, _p, _p, _p, _p]),
     "moe_permute": (_i32, [_i32, _p, _p, _i64, _i64, _i32, _p, _p, _i64, _p, _p, _i32, _p]),
     "moe_unpermute": (_i32, [_p, _p, _p, _i64, _i64, _i32, _p, _p]),
     "mx_grouped_gemm": (_i32, [_i32, _p, _p, _p, _p, _p, _i32, _i64, _i64, _i64, _p, _i32, _p, _p]),

@@ -41,6 +41,8 @@ extern "C" const char *mx_status_string(mx_status s) {
     case MX_ERR_DEVICE: return "MX_ERR_DEVICE: the device found an expert id out of range or bad group offsets";
     case MX_ERR_TIMEOUT: return "MX_ERR_TIMEOUT: a bounded pipeline wait expired on the device";
     case MX_ERR_WORKSPACE: return "MX_ERR_WORKSPACE: workspace smaller than the size query returned";
+    case MX_ERR_SCRATCH_LIMIT:
+      return "MX_ERR_SCRATCH_LIMIT: the problem needs more scratch than the allocation-free entry point's fixed array";
     default: return "unknown mx_status";
   }
 }

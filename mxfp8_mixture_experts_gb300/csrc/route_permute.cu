@@ -10,6 +10,8 @@
 // All kernels here are HBM- or latency-bound; none uses tensor cores.
 #include "common.cuh"
 
+#include <mutex>
+
 namespace mxmoe {
 
 constexpr int MAP_CHUNK = 1024;  // routed pairs per CTA in the map kernels
@@ -350,6 +352,56 @@ extern "C" mx_status moe_permute_map(const int32_t *ids, int64_t T, int32_t k, i
   const int64_t nchunks = (n + MAP_CHUNK - 1) / MAP_CHUNK;
   int32_t *chunk_counts = static_cast<int32_t *>(workspace);
   int32_t *chunk_base = chunk_counts + nchunks * E;
+  if (nchunks > 0) k_map_count<<<(unsigned)nchunks, MAP_CHUNK, 0, stream>>>(ids, n, E, chunk_counts, dev_status);
+  k_map_scan<<<1, MAP_MAX_E, 0, stream>>>(chunk_counts, nchunks, E, rows_cap, chunk_base, counts, offsets, src);
+  if (nchunks > 0) k_map_assign<<<(unsigned)nchunks, MAP_CHUNK, 0, stream>>>(ids, n, E, chunk_base, dst, src);
+  return launch_status();
+}
+
+// ---------------------------------------------------------------------------
+// Allocation-free grouping map: the same three kernels, with their per-chunk
+// count/base scratch in a fixed array of this library's device memory instead
+// of a caller workspace (see moe_permute_map_noalloc in mxmoe.h).
+// ---------------------------------------------------------------------------
+static __device__ __align__(256) int32_t g_noalloc_map_scratch[MOE_NOALLOC_SCRATCH_BYTES / sizeof(int32_t)];
+
+namespace {
+std::mutex g_noalloc_mu;
+int32_t *g_noalloc_ptr[64];  // device address of the array, per device
+
+// Host code must not pass the array's name to a kernel: on the host it is a
+// stand-in symbol, not a device address.  Look the address up once per device
+// (with that device current) and hand the kernels that pointer.
+mx_status noalloc_scratch(int32_t **out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MX_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_map_scratch) != cudaSuccess || p == nullptr) return MX_ERR_CUDA;
+    g_noalloc_ptr[dev] = static_cast<int32_t *>(p);
+  }
+  *out = g_noalloc_ptr[dev];
+  return MX_OK;
+}
+}  // namespace
+
+extern "C" mx_status moe_permute_map_noalloc(const int32_t *ids, int64_t T, int32_t k, int32_t E, int64_t rows_cap,
+                                             int32_t *counts, int32_t *offsets, int32_t *dst, int32_t *src,
+                                             int32_t *dev_status, mx_stream stream) {
+  MX_HOST_CHECK(ids && counts && offsets && dst && src, MX_ERR_INVALID_ARG);
+  MX_HOST_CHECK(T >= 0 && k >= 1 && k <= 8 && E >= 1 && E <= MAP_MAX_E, MX_ERR_INVALID_ARG);
+  MX_HOST_CHECK(rows_cap >= moe_rows_cap(T, k, E), MX_ERR_SHAPE);
+  MX_HOST_CHECK(moe_permute_map_workspace_size(T, k, E) <= (int64_t)MOE_NOALLOC_SCRATCH_BYTES, MX_ERR_SCRATCH_LIMIT);
+  mx_status st = check_device_cached();
+  if (st != MX_OK) return st;
+  int32_t *scratch = nullptr;
+  st = noalloc_scratch(&scratch);
+  if (st != MX_OK) return st;
+  const int64_t n = T * k;
+  const int64_t nchunks = (n + MAP_CHUNK - 1) / MAP_CHUNK;
+  int32_t *chunk_counts = scratch;
+  int32_t *chunk_base = scratch + nchunks * E;
   if (nchunks > 0) k_map_count<<<(unsigned)nchunks, MAP_CHUNK, 0, stream>>>(ids, n, E, chunk_counts, dev_status);
   k_map_scan<<<1, MAP_MAX_E, 0, stream>>>(chunk_counts, nchunks, E, rows_cap, chunk_base, counts, offsets, src);
   if (nchunks > 0) k_map_assign<<<(unsigned)nchunks, MAP_CHUNK, 0, stream>>>(ids, n, E, chunk_base, dst, src);

@@ -40,7 +40,7 @@ def test_every_declared_symbol_is_exported_and_bound(lib):
 
 
 def test_status_strings(lib):
-    for code in range(0, 9):
+    for code in range(0, 10):
         s = lib.mx_status_string(code).decode()
         assert s.startswith("MX_")
     assert lib.mx_abi_version() == 1
