@@ -341,11 +341,14 @@ def _dist():
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-quant", action="store_true", help="skip the quantize-kernel line of the layer run")
+    ap.add_argument("--T", type=int, default=None, help="override the token count (profiling of small cases)")
+    ap.add_argument("--E", type=int, default=None, help="override the expert count (profiling of small cases)")
     ap.add_argument("--workload", default="layer", choices=["layer", "gemm", "quantize"],
                     help="layer: the full training step (the bench line); gemm / quantize: one kernel family "
                          "on its own workload, for profiling")
@@ -359,6 +362,8 @@ def main():
         return
 
     dims = workloads.FULL_LAYER
+    if args.T or args.E:
+        dims = workloads.LayerDims(T=args.T or dims.T, H=dims.H, E=args.E or dims.E, F=dims.F, k=dims.k)
     config = {"workload": f"full MoE SwiGLU layer fwd+bwd: T={dims.T} tokens, H={dims.H}, E={dims.E} experts, "
                           f"F={dims.F}, top-{dims.k} softmax router on N(0,1) logits, MXFP8 on all expert GEMMs",
               "T": dims.T, "H": dims.H, "E": dims.E, "F": dims.F, "k": dims.k,
@@ -449,9 +454,12 @@ def main():
     gemm_tflops = total_flops / gemm_time / 1e12
     hbm = _peak_val(peaks, "hbm_gbs") or FALLBACK["hbm_gbs"]
 
-    quant = _quant_bench(dev)
-    quant["frac"] = quant["GB/s"] / hbm
-    quant["peak"] = hbm
+    quant = None
+    if not args.no_quant:
+        quant = _quant_bench(dev)
+        quant["frac"] = quant["GB/s"] / hbm
+        quant["peak"] = hbm
+        quant["peak_source"] = f"{src} hbm_gbs"
 
     line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
@@ -462,7 +470,8 @@ def main():
             "roofline": {"bound": "tensor", "kernel": "k_grouped_gemm (6 launches per step)",
                          "achieved": gemm_tflops, "peak": fp8_peak, "unit": "TFLOP/s", "frac": gemm_tflops / fp8_peak,
                          "traffic": None,
-                         "peak_source": f"{src}: bf16 {'sustained' if 'sustained' in str(peaks) else ''} x {FP8_PER_BF16} (nominal fp8/bf16)"},
+                         "peak_source": f"{src} bf16_tflops_sustained {bf16} x {FP8_PER_BF16} (nominal dense "
+                                        f"fp8/bf16 ratio)"},
             "value_excl_weight_prep": total_flops / (ms * 1e-3 - avg['quantize W13'] - avg['quantize W2']) / 1e12,
             "kernels_ms": {n: round(v * 1e3, 4) for n, v in avg.items()},
             "gemm_tflops": {n: round(gf[n] / avg[n] / 1e12, 1) for n in gf},
@@ -482,58 +491,91 @@ def main():
 
 def _e2e(m, d, dims, inp, dev, args, world):
     """The same step through the layer entry points (moe_layer_prep_weights,
-    moe_layer_fwd, moe_layer_bwd), with this step's inputs (x, logits, dOut)
+    moe_layer_fwd, moe_layer_bwd), with every step's inputs (x, logits, dOut)
     copied in from pinned host memory and its results (out, dX, d_gate) read
-    back, inside the timed region."""
+    back to pinned host memory inside the timed region.  The copies run on a
+    second stream into double-buffered device tensors, so step i+1's inputs
+    and step i-1's results move while step i computes; the timed region ends
+    when the last result has reached the host."""
     W13 = torch.cat([inp["W1"], inp["W3"]], dim=2).contiguous()
     W2 = inp["W2"]
     wq = torch.empty(m.moe_layer_weights_size(d.H, d.F, d.E), dtype=torch.uint8, device=dev)
     ws = torch.empty(m.moe_layer_workspace_size(d), dtype=torch.uint8, device=dev)
-    h_x = inp["x"].cpu().pin_memory()
-    h_l = inp["logits"].cpu().pin_memory()
-    h_d = inp["dOut"].cpu().pin_memory()
-    x = torch.empty_like(inp["x"])
-    lg = torch.empty_like(inp["logits"])
-    dO = torch.empty_like(inp["dOut"])
-    ids = torch.empty((d.T, d.k), dtype=torch.int32, device=dev)
-    gate = torch.empty((d.T, d.k), dtype=torch.float32, device=dev)
-    out = torch.empty((d.T, d.H), dtype=torch.bfloat16, device=dev)
-    dX = torch.empty_like(out)
+    h_in = {"x": inp["x"].cpu().pin_memory(), "lg": inp["logits"].cpu().pin_memory(),
+            "dO": inp["dOut"].cpu().pin_memory()}
     dW13 = torch.empty((d.E, d.H, 2 * d.F), dtype=torch.float32, device=dev)
     dW2 = torch.empty((d.E, d.F, d.H), dtype=torch.float32, device=dev)
-    dg = torch.empty((d.T, d.k), dtype=torch.float32, device=dev)
-    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    h_dX = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    h_dg = torch.empty(dg.shape, dtype=dg.dtype).pin_memory()
-
-    def one():
-        x.copy_(h_x, non_blocking=True)
-        lg.copy_(h_l, non_blocking=True)
-        dO.copy_(h_d, non_blocking=True)
-        m.moe_layer_prep_weights(W13, W2, wq)
-        m.moe_layer_fwd(x, wq, d, ws, logits=lg, ids=ids, gate=gate, out=out)
-        m.moe_layer_bwd(x, dO, gate, wq, d, ws, dX=dX, dW13=dW13, dW2=dW2, d_gate=dg)
-        h_out.copy_(out, non_blocking=True)
-        h_dX.copy_(dX, non_blocking=True)
-        h_dg.copy_(dg, non_blocking=True)
-
-    for _ in range(args.warmup):
-        one()
-    torch.cuda.synchronize()
+    ids = torch.empty((d.T, d.k), dtype=torch.int32, device=dev)
+    gate = torch.empty((d.T, d.k), dtype=torch.float32, device=dev)
+    bufs = []
+    for _ in range(2):
+        b = {n: torch.empty_like(t, device=dev) for n, t in h_in.items()}
+        b["out"] = torch.empty((d.T, d.H), dtype=torch.bfloat16, device=dev)
+        b["dX"] = torch.empty_like(b["out"])
+        b["dg"] = torch.empty((d.T, d.k), dtype=torch.float32, device=dev)
+        bufs.append(b)
+    h_out = {n: torch.empty(bufs[0][n].shape, dtype=bufs[0][n].dtype).pin_memory() for n in ("out", "dX", "dg")}
     s = torch.cuda.current_stream(dev)
+    cs = torch.cuda.Stream(dev)
+    ev = lambda: torch.cuda.Event()
+    in_ready = [ev(), ev()]
+    done = [ev(), ev()]
+
+    def h2d(i):
+        b = bufs[i % 2]
+        if i >= 2:
+            cs.wait_event(done[i % 2])  # step i-2 no longer reads this buffer
+        with torch.cuda.stream(cs):
+            for n, t in h_in.items():
+                b[n].copy_(t, non_blocking=True)
+        in_ready[i % 2].record(cs)
+
+    def compute(i):
+        b = bufs[i % 2]
+        s.wait_event(in_ready[i % 2])
+        m.moe_layer_prep_weights(W13, W2, wq)
+        m.moe_layer_fwd(b["x"], wq, d, ws, logits=b["lg"], ids=ids, gate=gate, out=b["out"])
+        m.moe_layer_bwd(b["x"], b["dO"], gate, wq, d, ws, dX=b["dX"], dW13=dW13, dW2=dW2, d_gate=b["dg"])
+        done[i % 2].record(s)
+
+    def d2h(i):
+        b = bufs[i % 2]
+        cs.wait_event(done[i % 2])
+        with torch.cuda.stream(cs):
+            for n, t in h_out.items():
+                t.copy_(b[n], non_blocking=True)
+
+    def run(k, start):
+        cs.wait_event(start)
+        h2d(0)
+        if k > 1:
+            h2d(1)
+        for i in range(k):
+            compute(i)
+            d2h(i)
+            if i + 2 < k:
+                h2d(i + 2)
+        fin = ev()
+        fin.record(cs)
+        s.wait_event(fin)
+
+    st = ev()
+    st.record(s)
+    run(max(args.warmup, 1), st)
+    torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(s)
-    for _ in range(args.steps):
-        one()
+    run(args.steps, e0)
     e1.record(s)
     torch.cuda.synchronize()
     el = e0.elapsed_time(e1) * 1e-3
     routed = d.T * d.k
     flops = sum(_gemm_flops(d, routed).values())
-    h2d = sum(t.numel() * t.element_size() for t in (h_x, h_l, h_d))
-    d2h = sum(t.numel() * t.element_size() for t in (h_out, h_dX, h_dg))
-    return {"value": world * flops * args.steps / el / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "ms_per_step": el / args.steps * 1e3}
+    h2d_b = sum(t.numel() * t.element_size() for t in h_in.values())
+    d2h_b = sum(t.numel() * t.element_size() for t in h_out.values())
+    return {"value": world * flops * args.steps / el / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d_b,
+            "d2h_bytes_per_step": d2h_b, "ms_per_step": el / args.steps * 1e3,
+            "copies": "pinned host <-> device on a second stream, double-buffered, inside the timed region"}
 
 
 if __name__ == "__main__":

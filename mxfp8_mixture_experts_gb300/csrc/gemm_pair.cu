@@ -66,10 +66,19 @@ __device__ __forceinline__ PairTile decode_pair(const Params &p, const int32_t *
   PairTile tl;
   if (p.op == OP_ROWS) {
     const int64_t n_tiles = p.epi == EPI_GLU ? p.N / 128 : p.N / BN;
-    const int64_t pr = t / n_tiles, nt = t % n_tiles;
-    const int e = upper_group(pp, p.E, pr);
-    const int64_t j = pr - pp[e];
+    // tiles of group e are [pp[e] * n_tiles, pp[e+1] * n_tiles)
+    const int e = upper_group(pp, p.E, t / n_tiles);
+    const int64_t local = t - (int64_t)pp[e] * n_tiles;
+    const int64_t np_e = pp[e + 1] - pp[e];
     const int64_t n_e = (off[e + 1] - off[e]) / BM;
+    const int64_t b_rows = p.epi == EPI_GLU ? 2 * p.N : p.N;
+    // Raster within the group: when its rows are fewer than the weight rows,
+    // walk the row pairs fastest so that each weight tile is read from HBM
+    // once while the (smaller) activation slab stays in L2; otherwise walk
+    // the column tiles fastest and keep each activation row pair in L2.
+    const bool rows_fastest = n_e * BM < b_rows;
+    const int64_t j = rows_fastest ? local % np_e : local / n_tiles;
+    const int64_t nt = rows_fastest ? local / np_e : local % n_tiles;
     const int64_t mt0 = off[e] / BM + 2 * j;
     const bool lone = (2 * j + 1 == n_e);
     const int64_t my_mt = mt0 + (lone ? 0 : rank);
