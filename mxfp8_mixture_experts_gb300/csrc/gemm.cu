@@ -330,12 +330,21 @@ mx_status make_map_u8_128x128(CUtensorMap *m, const void *base, int64_t inner, i
   return make_map_u8_128x128_swz(m, base, inner, outer, (int)CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
+static mx_status make_map_u8_box_swz(CUtensorMap *m, const void *base, int64_t inner, int64_t outer, int box_rows,
+                                     int swizzle);
+
 mx_status make_map_u8_128x128_swz(CUtensorMap *m, const void *base, int64_t inner, int64_t outer, int swizzle) {
+  return make_map_u8_box_swz(m, base, inner, outer, 128, swizzle);
+}
+
+static mx_status make_map_u8_box_swz(CUtensorMap *m, const void *base, int64_t inner, int64_t outer, int box_rows,
+                                     int swizzle) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return MX_ERR_CUDA;
+  if (box_rows < 1 || box_rows > 256) return MX_ERR_INVALID_ARG;
   cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
   cuuint64_t strides[1] = {(cuuint64_t)inner};
-  cuuint32_t box[2] = {128, 128};
+  cuuint32_t box[2] = {128, (cuuint32_t)box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, (CUtensorMapSwizzle)swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,

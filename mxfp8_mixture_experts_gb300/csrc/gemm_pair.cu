@@ -4,19 +4,25 @@
 // training on Blackwell with MXFP8 kernels built from scratch", Key Questions
 // Answered: block-scaled tcgen05.mma with TMEM accumulators), arranged for the
 // bandwidth of one SM: two CTAs on neighbouring SMs form a cluster and compute
-// one 256 x 256 tile with M=256 MMAs.  Each CTA stages its own 128 rows of A
-// and its own 128-row half of the B tile, so one SM takes in 64 bytes of
-// operands per MMA cycle instead of the 96 a 128 x 256 one-CTA tile needs,
-// and the ring holds 6 stages instead of 4.
+// one 256-row tile with M=256 MMAs.  Each CTA stages its own 128 rows of A and
+// its own half of the B tile.
+//
+// One SM takes in 64 bytes of operands per MMA cycle (a 128 x 256 one-CTA
+// tile needs 96), so the pair runs close to the tensor peak; with 6 operand
+// stages in shared memory the loads run far enough ahead to cross tile
+// boundaries without starving the MMA.  (Measured alternatives that lost:
+// 256 x 128 tiles with two TMEM accumulators, which raise the L2-to-SM
+// traffic per FLOP by half; direct global stores from registers; a second
+// staging buffer per epilogue warp in place of the sixth stage.)
 //
 // Roles per CTA (320 threads): warp 0 loads (TMA, completion counted on the
 // even CTA's barrier), warp 1 of the even CTA issues the scale copies, MMAs
-// and commits for the pair, warps 2..9 drain the CTA's own 128 x 256
-// accumulator (bf16/fp32 outputs leave through swizzled shared-memory staging
-// and TMA tensor stores, so each global write is a full 64-byte row segment).
-// Row groups are 128-row aligned; a group with an odd number of
-// 128-row tiles ends in a "lone" tile, computed by the pair with both halves on
-// the same rows and stored by the even CTA only.
+// and commits for the pair, warps 2..9 drain the CTA's own 128-row slice of
+// the accumulator (bf16/fp32 outputs leave through swizzled shared-memory
+// staging and TMA tensor stores, so each global write is a full 64-byte row
+// segment).  Row groups are 128-row aligned; a group with an odd number of
+// 128-row tiles ends in a "lone" tile, computed by the pair with both halves
+// on the same rows and stored by the even CTA only.
 #include "gemm_shared.cuh"
 
 #include <mutex>
@@ -24,31 +30,39 @@
 namespace mxmoe {
 namespace gemm {
 
-constexpr int P_STAGES = 5;
-constexpr int P_A_TILE = 128 * BK;                      // 16 KB: this CTA's 128 rows of A
-constexpr int P_B_TILE = 128 * BK;                      // 16 KB: this CTA's half of B
-constexpr int P_SF_STAGE = 512 + 1024;                  // own SFA chunk + both SFB chunks
-constexpr uint32_t P_STAGE_TX = P_A_TILE + P_B_TILE + P_SF_STAGE;
 constexpr int P_THREADS = 320;
 constexpr uint32_t P_TMEM_COLS = 512;
-constexpr uint32_t P_ACC_COL = 0;
-constexpr uint32_t P_SF_COL = 256;  // per stage: SFA 4 columns, SFB 8 columns
+constexpr int P_EPI_BUF = 2048;  // 32 rows x 64 bytes, 64-byte swizzle
 
-constexpr int P_SMEM_A = 0;
-constexpr int P_SMEM_B = P_SMEM_A + P_STAGES * P_A_TILE;
-constexpr int P_SMEM_SF = P_SMEM_B + P_STAGES * P_B_TILE;
-constexpr int P_EPI_BUF = 2048;                        // 32 rows x 64 bytes, 64-byte swizzle
-constexpr int P_SMEM_EPI = P_SMEM_SF + P_STAGES * P_SF_STAGE;   // 2 buffers per epilogue warp
-constexpr int P_SMEM_BAR = P_SMEM_EPI + NUM_EPI_WARPS * 2 * P_EPI_BUF;
-constexpr int P_SMEM_OFFS = P_SMEM_BAR + 256;
-constexpr int P_SMEM_PP = P_SMEM_OFFS + (MAX_E + 1) * 4;
-constexpr int P_SMEM_TOTAL = P_SMEM_PP + (MAX_E + 1) * 4;
-constexpr int P_SMEM_ALLOC = P_SMEM_TOTAL + 1024;
+struct PairCfg {
+  static constexpr int TN = 256;                       // MMA N: tile columns
+  static constexpr int STAGES = 6;
+  static constexpr int EPI_BUFS = 1;                   // store staging buffers per epilogue warp
+  static constexpr int A_TILE = 128 * BK;              // 16 KB: this CTA's 128 rows of A
+  static constexpr int B_TILE = 128 * BK;              // 16 KB: this CTA's half of the B tile
+  static constexpr int SF_STAGE = 3 * 512;             // own SFA chunk + both SFB chunks
+  static constexpr uint32_t STAGE_TX = A_TILE + B_TILE + SF_STAGE;
+  static constexpr uint32_t ACC_COL = 0;               // accumulator: TMEM columns [0, 256)
+  static constexpr uint32_t SF_COL = 256;              // scales: 12 columns per stage from here
+  static constexpr uint32_t SF_COLS = 12;
+  static constexpr int SMEM_A = 0;
+  static constexpr int SMEM_B = SMEM_A + STAGES * A_TILE;
+  static constexpr int SMEM_SF = SMEM_B + STAGES * B_TILE;
+  static constexpr int SMEM_EPI = SMEM_SF + STAGES * SF_STAGE;
+  static constexpr int SMEM_BAR = SMEM_EPI + NUM_EPI_WARPS * EPI_BUFS * P_EPI_BUF;
+  static constexpr int SMEM_OFFS = SMEM_BAR + 256;
+  static constexpr int SMEM_PP = SMEM_OFFS + (MAX_E + 1) * 4;
+  static constexpr int SMEM_TOTAL = SMEM_PP + (MAX_E + 1) * 4;
+  static constexpr int SMEM_ALLOC = SMEM_TOTAL + 1024;
+  static_assert(SF_COL + STAGES * SF_COLS <= P_TMEM_COLS, "TMEM columns");
+  static_assert((2 * STAGES + 2) * 8 + 8 <= 256, "barrier area");
+  static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory");
+};
 
 struct PairTile {
   int64_t a_row;           // this CTA's A rows (TMA row coordinate)
-  int64_t b_row;           // this CTA's half of B
-  int64_t b_row0, b_row1;  // both halves (for the scale chunks)
+  int64_t b_row;           // this CTA's rows of the B tile
+  int64_t b_row0, b_row1;  // the two 128-row halves of the B tile (scale chunks)
   int64_t k0;
   int num_k;
   int64_t sfa_chunk, sfb_chunk0, sfb_chunk1;  // chunk index of the k=0 scales
@@ -85,6 +99,8 @@ __device__ __forceinline__ PairTile decode_pair(const Params &p, const int32_t *
     const int64_t kblocks = p.K / BK;
     tl.a_row = my_mt * BM;
     if (p.epi == EPI_GLU) {
+      // GEMM1: output features [nt*128, nt*128+128) need W1 rows (first F
+      // rows of the expert's 2F) and the matching W3 rows (F further on)
       tl.b_row0 = (int64_t)e * 2 * p.N + nt * 128;
       tl.b_row1 = tl.b_row0 + p.N;
       tl.out_col = nt * 128;
@@ -101,11 +117,18 @@ __device__ __forceinline__ PairTile decode_pair(const Params &p, const int32_t *
     tl.out_row = (mt0 + rank) * BM;
     tl.store = !(lone && rank == 1);
   } else {
+    // token-grouped (wgrad): output [e*N + 256-row tile, 256-column tile],
+    // contraction over the group's tokens [off[e], off[e+1])
     const int64_t rt_n = p.N / 256, ct_n = p.K / BN;
     const int64_t per_e = rt_n * ct_n;
     const int e = (int)(t / per_e);
     const int64_t rem = t % per_e;
-    const int64_t rt = rem / ct_n, ct = rem % ct_n;
+    // The group's A slab is N x tokens, its B slab K x tokens: walk the tiles
+    // of the smaller slab fastest, so it is the one re-read from L2 and the
+    // larger one streams from HBM once.
+    const bool rows_fastest = p.N <= p.K;
+    const int64_t rt = rows_fastest ? rem % rt_n : rem / ct_n;
+    const int64_t ct = rows_fastest ? rem / rt_n : rem % ct_n;
     const int64_t kblocks = p.M_cap / BK;
     const int64_t kc0 = off[e] / BK;
     tl.a_row = rt * 256 + rank * 128;
@@ -125,11 +148,13 @@ __device__ __forceinline__ PairTile decode_pair(const Params &p, const int32_t *
 }
 
 // One warp's 32 rows x 64 bytes: wait until the store that last used `buf`
-// has read it, write the rows (16-byte chunk j of row i at chunk j ^ ((i>>1)&3),
-// the 64-byte swizzle of the store map), then one lane issues the TMA store.
+// has read it (at most NBUF - 1 newer stores pending), write the rows (16-byte
+// chunk j of row i at chunk j ^ ((i>>1)&3), the 64-byte swizzle of the store
+// map), then one lane issues the TMA store.
+template <int NBUF>
 __device__ __forceinline__ void stage_and_store(const CUtensorMap *map, uint8_t *buf, const uint4 (&v)[4], int lane,
                                                 int x, int y) {
-  if (lane == 0) bulk_wait_group_read<1>();
+  if (lane == 0) bulk_wait_group_read<NBUF - 1>();
   __syncwarp();
 #pragma unroll
   for (int j = 0; j < 4; ++j)
@@ -146,16 +171,17 @@ __global__ void __launch_bounds__(P_THREADS, 1)
     k_grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
                         const __grid_constant__ CUtensorMap tmC, Params p) {
+  using C = PairCfg;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t *full = reinterpret_cast<uint64_t *>(smem + P_SMEM_BAR);
-  uint64_t *empty = full + P_STAGES;
-  uint64_t *tmem_full = empty + P_STAGES;
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::SMEM_BAR);
+  uint64_t *empty = full + C::STAGES;
+  uint64_t *tmem_full = empty + C::STAGES;
   uint64_t *tmem_empty = tmem_full + 1;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tmem_empty + 1);
   int32_t *s_flag = reinterpret_cast<int32_t *>(tmem_slot + 1);
-  int32_t *s_off = reinterpret_cast<int32_t *>(smem + P_SMEM_OFFS);
-  int32_t *s_pp = reinterpret_cast<int32_t *>(smem + P_SMEM_PP);
+  int32_t *s_off = reinterpret_cast<int32_t *>(smem + C::SMEM_OFFS);
+  int32_t *s_pp = reinterpret_cast<int32_t *>(smem + C::SMEM_PP);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();
@@ -176,7 +202,7 @@ __global__ void __launch_bounds__(P_THREADS, 1)
     s_pp[p.E] = run;
   }
   if (warp == 0 && lane == 0) {
-    for (int s = 0; s < P_STAGES; ++s) {
+    for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
@@ -218,11 +244,11 @@ __global__ void __launch_bounds__(P_THREADS, 1)
             break;
           }
           if (elect_one_sync()) {
-            if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * P_STAGE_TX);
+            if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * C::STAGE_TX);
             const uint32_t bar = leader_full0 + stage * 8;
-            uint8_t *sa = smem + P_SMEM_A + stage * P_A_TILE;
-            uint8_t *sb = smem + P_SMEM_B + stage * P_B_TILE;
-            uint8_t *sf = smem + P_SMEM_SF + stage * P_SF_STAGE;
+            uint8_t *sa = smem + C::SMEM_A + stage * C::A_TILE;
+            uint8_t *sb = smem + C::SMEM_B + stage * C::B_TILE;
+            uint8_t *sf = smem + C::SMEM_SF + stage * C::SF_STAGE;
             const int32_t kc = (int32_t)(tl.k0 + (int64_t)kb * BK);
             tma_load_2d_pair(sa, &tmA, bar, kc, (int32_t)tl.a_row);
             tma_load_2d_pair(sb, &tmB, bar, kc, (int32_t)tl.b_row);
@@ -231,7 +257,7 @@ __global__ void __launch_bounds__(P_THREADS, 1)
             tma_load_2d_pair(sf + 1024, &tmSFB, bar, 0, (int32_t)(tl.sfb_chunk1 + kb));
           }
           __syncwarp();
-          if (++stage == P_STAGES) {
+          if (++stage == C::STAGES) {
             stage = 0;
             phase ^= 1;
           }
@@ -246,8 +272,8 @@ __global__ void __launch_bounds__(P_THREADS, 1)
       int stage = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool dead = false;
-      const uint32_t d_tmem = tmem_base + P_ACC_COL;
-      const uint32_t idesc = idesc_mxf8(2 * BM, BN);
+      const uint32_t idesc = idesc_mxf8(2 * BM, C::TN);
+      const uint32_t d_tmem = tmem_base + C::ACC_COL;
       for (int64_t t = cid; t < ntiles && !dead; t += ncl) {
         const PairTile tl = decode_pair(p, s_off, s_pp, t, rank);
         if (tl.num_k == 0) continue;
@@ -264,26 +290,26 @@ __global__ void __launch_bounds__(P_THREADS, 1)
           }
           tc_fence_after();
           if (elect_one_sync()) {
-          const uint32_t sa = smem_u32(smem + P_SMEM_A + stage * P_A_TILE);
-          const uint32_t sb = smem_u32(smem + P_SMEM_B + stage * P_B_TILE);
-          const uint32_t sf = smem_u32(smem + P_SMEM_SF + stage * P_SF_STAGE);
-          const uint32_t sfa_t = tmem_base + P_SF_COL + stage * 12;
-          const uint32_t sfb_t = sfa_t + 4;
-          // scales of this stage -> TMEM (in tensor-pipe order before the MMAs that read them)
-          tc_cp_32x128b_warpx4_pair(sfa_t, smem_desc(sf, 0, 128, 0));
-          tc_cp_32x128b_warpx4_pair(sfb_t, smem_desc(sf + 512, 0, 128, 0));
-          tc_cp_32x128b_warpx4_pair(sfb_t + 4, smem_desc(sf + 1024, 0, 128, 0));
+            const uint32_t sa = smem_u32(smem + C::SMEM_A + stage * C::A_TILE);
+            const uint32_t sb = smem_u32(smem + C::SMEM_B + stage * C::B_TILE);
+            const uint32_t sf = smem_u32(smem + C::SMEM_SF + stage * C::SF_STAGE);
+            const uint32_t sfa_t = tmem_base + C::SF_COL + stage * C::SF_COLS;
+            const uint32_t sfb_t = sfa_t + 4;
+            // scales of this stage -> TMEM (in tensor-pipe order before the MMAs that read them)
+            tc_cp_32x128b_warpx4_pair(sfa_t, smem_desc(sf, 0, 128, 0));
+            tc_cp_32x128b_warpx4_pair(sfb_t, smem_desc(sf + 512, 0, 128, 0));
+            tc_cp_32x128b_warpx4_pair(sfb_t + 4, smem_desc(sf + 1024, 0, 128, 0));
 #pragma unroll
-          for (int kk = 0; kk < BK / 32; ++kk) {
-            const uint64_t ad = smem_desc(sa + kk * 32, 16, 1024, 2);
-            const uint64_t bd = smem_desc(sb + kk * 32, 16, 1024, 2);
-            const uint32_t id = idesc | ((uint32_t)kk << 4) | ((uint32_t)kk << 29);
-            tc_mma_mxf8_pair(d_tmem, ad, bd, id, sfa_t, sfb_t, (kb | kk) != 0);
-          }
-          tc_commit_pair(&empty[stage], 0x3);
+            for (int kk = 0; kk < BK / 32; ++kk) {
+              const uint64_t ad = smem_desc(sa + kk * 32, 16, 1024, 2);
+              const uint64_t bd = smem_desc(sb + kk * 32, 16, 1024, 2);
+              const uint32_t id = idesc | ((uint32_t)kk << 4) | ((uint32_t)kk << 29);
+              tc_mma_mxf8_pair(d_tmem, ad, bd, id, sfa_t, sfb_t, (kb | kk) != 0);
+            }
+            tc_commit_pair(&empty[stage], 0x3);
           }
           __syncwarp();
-          if (++stage == P_STAGES) {
+          if (++stage == C::STAGES) {
             stage = 0;
             phase ^= 1;
           }
@@ -297,19 +323,21 @@ __global__ void __launch_bounds__(P_THREADS, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue (both CTAs)
+    // warp w drains TMEM lanes 32*(w%4).. (its sub-partition) and one half of
+    // the accumulator's columns
+    constexpr int EC = C::TN / 2;  // columns per epilogue warp
     const int q = warp & 3;
     const int h = (warp - 2) >> 2;
     const int row_in_tile = q * 32 + lane;
-    const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16) + P_ACC_COL;
     const uint32_t leader_tmem_empty = mapa_shared(smem_u32(tmem_empty), 0);
-    uint8_t *ebuf = smem + P_SMEM_EPI + (warp - 2) * 2 * P_EPI_BUF;
+    uint8_t *ebuf = smem + C::SMEM_EPI + (warp - 2) * C::EPI_BUFS * P_EPI_BUF;
     int nstore = 0;
     uint32_t acc_phase = 0;
     for (int64_t t = cid; t < ntiles; t += ncl) {
       const PairTile tl = decode_pair(p, s_off, s_pp, t, rank);
       const int64_t orow = tl.out_row + row_in_tile;
       if (tl.num_k == 0) {
-        epi_zero(p, orow, tl.out_col + h * 128);
+        epi_zero(p, orow, tl.out_col + h * EC, EC);
         continue;
       }
       if (!mbar_wait_warp(tmem_full, acc_phase, WAIT_TIMEOUT_NS)) {
@@ -317,17 +345,17 @@ __global__ void __launch_bounds__(P_THREADS, 1)
         break;
       }
       tc_fence_after();
-      uint32_t r[128];
+      const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16) + C::ACC_COL;
+      uint32_t r[EC];
       if (p.epi == EPI_GLU) {
+        // GEMM1: columns [0,128) hold a, [128,256) the matching b
         MX_TMEM_LD_32x32b_x32(t_row + h * 64, r);
         MX_TMEM_LD_32x32b_x32(t_row + h * 64 + 32, (r + 32));
         MX_TMEM_LD_32x32b_x32(t_row + 128 + h * 64, (r + 64));
         MX_TMEM_LD_32x32b_x32(t_row + 128 + h * 64 + 32, (r + 96));
       } else {
-        MX_TMEM_LD_32x32b_x32(t_row + h * 128, r);
-        MX_TMEM_LD_32x32b_x32(t_row + h * 128 + 32, (r + 32));
-        MX_TMEM_LD_32x32b_x32(t_row + h * 128 + 64, (r + 64));
-        MX_TMEM_LD_32x32b_x32(t_row + h * 128 + 96, (r + 96));
+#pragma unroll
+        for (int c = 0; c < EC / 32; ++c) MX_TMEM_LD_32x32b_x32(t_row + h * EC + c * 32, (r + c * 32));
       }
       tc_wait_ld();
       tc_fence_before();
@@ -341,20 +369,20 @@ __global__ void __launch_bounds__(P_THREADS, 1)
       }
       // 64-byte row segments: fp32 16 columns, bf16 32 columns per chunk
       const int y = (int)(tl.out_row + q * 32);
-      const int x0 = (int)(tl.out_col + h * 128);
+      const int x0 = (int)(tl.out_col + h * EC);
       if (p.epi == EPI_F32) {
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
+        for (int c = 0; c < EC / 16; ++c) {
           uint4 v[4];
 #pragma unroll
           for (int j = 0; j < 4; ++j)
             v[j] = make_uint4(r[c * 16 + 4 * j], r[c * 16 + 4 * j + 1], r[c * 16 + 4 * j + 2], r[c * 16 + 4 * j + 3]);
-          stage_and_store(&tmC, ebuf + (nstore & 1) * P_EPI_BUF, v, lane, x0 + c * 16, y);
+          stage_and_store<C::EPI_BUFS>(&tmC, ebuf + (nstore % C::EPI_BUFS) * P_EPI_BUF, v, lane, x0 + c * 16, y);
           ++nstore;
         }
       } else {
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < EC / 32; ++c) {
           uint4 v[4];
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
@@ -364,7 +392,7 @@ __global__ void __launch_bounds__(P_THREADS, 1)
                               pack_bf16x2(__uint_as_float(w[4]), __uint_as_float(w[5])),
                               pack_bf16x2(__uint_as_float(w[6]), __uint_as_float(w[7])));
           }
-          stage_and_store(&tmC, ebuf + (nstore & 1) * P_EPI_BUF, v, lane, x0 + c * 32, y);
+          stage_and_store<C::EPI_BUFS>(&tmC, ebuf + (nstore % C::EPI_BUFS) * P_EPI_BUF, v, lane, x0 + c * 32, y);
           ++nstore;
         }
       }
@@ -390,7 +418,7 @@ static void pair_config(cudaLaunchConfig_t *cfg, cudaLaunchAttribute *attr, int 
   *cfg = cudaLaunchConfig_t{};
   cfg->gridDim = dim3(grid, 1, 1);
   cfg->blockDim = dim3(P_THREADS, 1, 1);
-  cfg->dynamicSmemBytes = P_SMEM_ALLOC;
+  cfg->dynamicSmemBytes = PairCfg::SMEM_ALLOC;
   cfg->stream = stream;
   attr->id = cudaLaunchAttributeClusterDimension;
   attr->val.clusterDim.x = 2;
@@ -410,8 +438,8 @@ mx_status launch_pair(const Params &p, const uint8_t *A, int64_t a_inner, int64_
     // the persistent grid is as many CTA pairs as can be resident at once
     std::lock_guard<std::mutex> lk(g_pmu);
     if (!g_psmem_set[dev]) {
-      MX_CUDA_TRY(
-          cudaFuncSetAttribute(k_grouped_gemm_pair, cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM_ALLOC));
+      MX_CUDA_TRY(cudaFuncSetAttribute(k_grouped_gemm_pair, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       PairCfg::SMEM_ALLOC));
       int sms = 0;
       MX_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
       cudaLaunchConfig_t cfg;

@@ -58,15 +58,16 @@ __device__ __forceinline__ int upper_group(const int32_t *pref, int E, int64_t x
   return lo;
 }
 
-// Zero the 128 output columns [col0, col0+128) of row `orow` (empty wgrad group).
-__device__ __forceinline__ void epi_zero(const Params &p, int64_t orow, int64_t col0) {
+// Zero the output columns [col0, col0 + ncols) of row `orow` (empty wgrad
+// group); ncols is a multiple of 8.
+__device__ __forceinline__ void epi_zero(const Params &p, int64_t orow, int64_t col0, int ncols = 128) {
   const int64_t ldc = p.op == OP_ROWS ? p.N : p.K;
   if (p.epi == EPI_F32) {
     float4 *c = reinterpret_cast<float4 *>(static_cast<float *>(p.C) + orow * ldc + col0);
-    for (int j = 0; j < 32; ++j) c[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j = 0; j < ncols / 4; ++j) c[j] = make_float4(0.f, 0.f, 0.f, 0.f);
   } else {
     uint4 *c = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.C) + orow * ldc + col0);
-    for (int j = 0; j < 16; ++j) c[j] = make_uint4(0, 0, 0, 0);
+    for (int j = 0; j < ncols / 8; ++j) c[j] = make_uint4(0, 0, 0, 0);
   }
 }
 
