@@ -39,6 +39,25 @@ FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1
 FP8_PER_BF16 = 2.0   # nominal dense fp8 / bf16 tensor rate (4.5 / 2.25 PFLOP/s)
 
 
+# DRAM traffic of the six grouped-GEMM launches of one full-layer step: the
+# per-launch dram__bytes_read.sum + dram__bytes_write.sum of an ncu capture of
+# the T=2048, E=2 step (1024 routed rows per expert, as in the full layer),
+# scaled by 8 to E=16 (profiles/layer_step_dram_T2048_E2.md).  Valid only for
+# the GEMM sources it was taken on; reported as null once they change.
+GEMM_TRAFFIC_BYTES_PER_STEP = 8 * 1740.847616e6
+GEMM_TRAFFIC_SOURCES = ("gemm_pair.cu", "gemm_shared.cuh", "common.cuh")
+GEMM_TRAFFIC_SHA256 = "184df6588d42d000527ca53ba26428b04bfa10c3eb809a9ab6fcd642f680f152"
+
+
+def _gemm_sources_sha256():
+    import hashlib
+    h = hashlib.sha256()
+    for f in GEMM_TRAFFIC_SOURCES:
+        with open(os.path.join(ROOT, "mxfp8_mixture_experts_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
 def _peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -225,6 +244,20 @@ def _gemm_flops(d, routed):
     g1 = 2 * T * H * 2 * F
     g2 = 2 * T * F * H
     return {"gemm1+swiglu": g1, "gemm2": g2, "dgrad2": g2, "wgrad2": g2, "dgrad1": g1, "wgrad1": g1}
+
+
+def _gemm_alg_bytes(d, R):
+    """Operands read once plus outputs written once, over the 6 GEMM launches
+    of one step (R routed rows, fp8 data with 1/32 scale bytes)."""
+    T, H, F, E = R, d.H, d.F, d.E
+    q = 1 + 1 / 32
+    g1 = (T * H + E * 2 * F * H) * q + T * 2 * F * 2 + T * F * q
+    g2 = (T * F + E * H * F) * q + T * H * 2
+    dg2 = (T * H + E * F * H) * q + T * F * 4
+    wg2 = (F * T + H * T) * q + E * F * H * 4
+    dg1 = (T * 2 * F + E * H * 2 * F) * q + T * H * 2
+    wg1 = (H * T + 2 * F * T) * q + E * H * 2 * F * 4
+    return int(g1 + g2 + dg2 + wg2 + dg1 + wg1)
 
 
 def _quant_bench(dev, iters=20):
@@ -467,9 +500,12 @@ def main():
             "data": "synthetic (seeded, random-init weights)", "config": config,
             "gpu_launches": args.steps * sum(LayerStep.KERNELS) * 1,
             "clocks": clk,
-            "roofline": {"bound": "tensor", "kernel": "k_grouped_gemm (6 launches per step)",
+            "roofline": {"bound": "tensor", "kernel": "k_grouped_gemm_pair (6 launches per step)",
                          "achieved": gemm_tflops, "peak": fp8_peak, "unit": "TFLOP/s", "frac": gemm_tflops / fp8_peak,
-                         "traffic": None,
+                         "traffic": GEMM_TRAFFIC_BYTES_PER_STEP if _gemm_sources_sha256() == GEMM_TRAFFIC_SHA256
+                         else None,
+                         "traffic_unit": "DRAM bytes per step of the 6 GEMM launches (ncu, scaled from T=2048, E=2)",
+                         "algorithmic_bytes": _gemm_alg_bytes(d, R=routed),
                          "peak_source": f"{src} bf16_tflops_sustained {bf16} x {FP8_PER_BF16} (nominal dense "
                                         f"fp8/bf16 ratio)"},
             "value_excl_weight_prep": total_flops / (ms * 1e-3 - avg['quantize W13'] - avg['quantize W2']) / 1e12,
