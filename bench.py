@@ -287,6 +287,62 @@ def _quant_bench(dev, iters=20):
     return {"GB/s": nbytes / t / 1e9, "us": t * 1e6, "bytes": nbytes, "l2": "flushed (256 MiB write) before each launch"}
 
 
+def _permute_bench(dev, iters=10):
+    """Token permute / unpermute workload: T=32768 tokens, H=5120, E=16
+    experts, top-4 Zipf(1.1) expert choice over 14 live experts (two empty).
+    MXFP8 rows (E4M3 + plain scales) are scattered into 128-row-padded expert
+    groups (swizzled scales out); the combine reads k bf16 rows per token and
+    writes one.  Each launch timed with CUDA events after an L2 flush."""
+    import mxfp8_mixture_experts_gb300 as m
+    d = workloads.PERMUTE_DIMS
+    T, H, E, k = d["T"], d["H"], d["E"], d["k"]
+    inp = workloads.permute_inputs(T, H, E, k, seed=0, device=dev)
+    xq, xs, _, _ = m.mx_quantize(inp["x"], m.MX_MODE_ROW, m.MX_SCALE_PLAIN)
+    L = m.lib()
+    counts, off, dst, src = m.moe_permute_map(inp["ids"], E)
+    R = src.numel()
+    out = torch.empty((R, H), dtype=torch.uint8, device=dev)
+    out_s = torch.empty(m.mx_scale_bytes(R, H, m.MX_SCALE_SWIZZLED), dtype=torch.uint8, device=dev)
+    y = workloads.randn_bf16((R, H), 1.0, workloads.generator(1, dev), dev)
+    comb = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    s = torch.cuda.current_stream(dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def timed(fn):
+        ts = []
+        for i in range(iters + 3):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s)
+            fn()
+            e1.record(s)
+            torch.cuda.synchronize()
+            if i >= 3:
+                ts.append(e0.elapsed_time(e1) * 1e-3)
+        return statistics.median(ts)
+
+    def perm():
+        code = L.moe_permute(m.MX_PERMUTE_FP8, xq.data_ptr(), xs.data_ptr(), T, H, k, dst.data_ptr(), src.data_ptr(),
+                             R, out.data_ptr(), out_s.data_ptr(), m.MX_SCALE_SWIZZLED, s.cuda_stream)
+        assert code == 0
+
+    def unperm():
+        code = L.moe_unpermute(y.data_ptr(), dst.data_ptr(), inp["gate"].data_ptr(), T, H, k, comb.data_ptr(),
+                               s.cuda_stream)
+        assert code == 0
+
+    t_p, t_u = timed(perm), timed(unperm)
+    padded = int(off[E].item())
+    row_b = H + H // 32
+    pb = T * row_b + padded * row_b            # read each token once, write every padded group row
+    ub = T * k * H * 2 + T * H * 2             # read k routed rows per token, write one
+    return {"permute": {"GB/s": pb / t_p / 1e9, "us": t_p * 1e6, "bytes": pb, "padded_rows": padded},
+            "unpermute": {"GB/s": ub / t_u / 1e9, "us": t_u * 1e6, "bytes": ub},
+            "workload": f"T={T}, H={H}, E={E}, top-{k} Zipf(1.1) over {E - 2} live experts; MXFP8 rows in, "
+                        f"128-row-padded groups out; combine of k bf16 rows per token",
+            "l2": "flushed (256 MiB write) before each launch"}
+
+
 def _gemm_bench(dev, args):
     """Grouped GEMM workload: E=8, 32768 routed rows in Zipf-sized groups (one
     empty), K=7168, N=2048; forward (bf16 out), dgrad (bf16 out) and wgrad
@@ -382,7 +438,7 @@ def main():
     ap.add_argument("--no-quant", action="store_true", help="skip the quantize-kernel line of the layer run")
     ap.add_argument("--T", type=int, default=None, help="override the token count (profiling of small cases)")
     ap.add_argument("--E", type=int, default=None, help="override the expert count (profiling of small cases)")
-    ap.add_argument("--workload", default="layer", choices=["layer", "gemm", "quantize"],
+    ap.add_argument("--workload", default="layer", choices=["layer", "gemm", "quantize", "permute"],
                     help="layer: the full training step (the bench line); gemm / quantize: one kernel family "
                          "on its own workload, for profiling")
     args = ap.parse_args()
@@ -390,7 +446,12 @@ def main():
     if args.workload != "layer":
         dev = torch.device("cuda", local)
         torch.cuda.set_device(dev)
-        r = _gemm_bench(dev, args) if args.workload == "gemm" else _quant_bench(dev, max(args.steps, 1))
+        if args.workload == "gemm":
+            r = _gemm_bench(dev, args)
+        elif args.workload == "permute":
+            r = _permute_bench(dev, max(args.steps, 1))
+        else:
+            r = _quant_bench(dev, max(args.steps, 1))
         print(json.dumps({"workload": args.workload, **r}))
         return
 
@@ -487,12 +548,15 @@ def main():
     gemm_tflops = total_flops / gemm_time / 1e12
     hbm = _peak_val(peaks, "hbm_gbs") or FALLBACK["hbm_gbs"]
 
-    quant = None
+    quant = perm = None
     if not args.no_quant:
         quant = _quant_bench(dev)
         quant["frac"] = quant["GB/s"] / hbm
         quant["peak"] = hbm
         quant["peak_source"] = f"{src} hbm_gbs"
+        perm = _permute_bench(dev)
+        for key in ("permute", "unpermute"):
+            perm[key]["frac"] = perm[key]["GB/s"] / hbm
 
     line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
@@ -512,6 +576,7 @@ def main():
             "kernels_ms": {n: round(v * 1e3, 4) for n, v in avg.items()},
             "gemm_tflops": {n: round(gf[n] / avg[n] / 1e12, 1) for n in gf},
             "quantize": quant,
+            "permute": perm,
             "routed_rows": routed}
 
     if not args.no_e2e:

@@ -357,10 +357,10 @@ __global__ void __launch_bounds__(P_THREADS, 1)
 #pragma unroll
         for (int c = 0; c < EC / 32; ++c) MX_TMEM_LD_32x32b_x32(t_row + h * EC + c * 32, (r + c * 32));
       }
-      tc_wait_ld();
+      tc_wait_ld();  // the accumulator is in registers: the MMA may overwrite it
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(leader_tmem_empty);
+      if (lane == 0) mbar_arrive_cluster_relaxed(leader_tmem_empty);
       acc_phase ^= 1;
       if (!tl.store) continue;
       if (p.epi == EPI_GLU) {

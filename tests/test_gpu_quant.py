@@ -42,7 +42,8 @@ def _check(xt, mode, layout):
         assert_bytes_equal(u8(sc).reshape(ref["col"][1].shape), ref["col"][1], "s_col")
 
 
-@pytest.mark.parametrize("shape", [(32, 32), (64, 96), (160, 224), (256, 512), (384, 7168)])
+@pytest.mark.parametrize("shape", [(32, 32), (64, 96), (160, 224), (160, 256), (96, 384), (256, 512),
+                                   (384, 7168)])
 @pytest.mark.parametrize("mode", [1, 2, 3])
 @pytest.mark.parametrize("layout", [0, 1])
 def test_quantize_matches_oracle(dev, shape, mode, layout):
@@ -55,6 +56,32 @@ def test_quantize_batched(dev, layout):
     g = workloads.generator(3, dev)
     x = workloads.randn_bf16((3, 128, 256), 1.0, g, dev)
     _check(x, 3, layout)
+
+
+def test_quantize_unaligned_scale_pointers(dev):
+    """Scale arrays need no alignment: outputs written through C-ABI pointers
+    one byte past an aligned address match the oracle."""
+    import ctypes
+    import mxfp8_mixture_experts_gb300 as m
+    R, Cc = 256, 512
+    x = workloads.quantize_input(R, Cc, seed=11, device=dev)
+    L = m.lib()
+    nb = L.mx_scale_bytes(R, Cc, 1)
+    nbc = L.mx_scale_bytes(Cc, R, 1)
+    qr = torch.empty(R * Cc, dtype=torch.uint8, device=dev)
+    qc = torch.empty(R * Cc, dtype=torch.uint8, device=dev)
+    sr = torch.zeros(nb + 16, dtype=torch.uint8, device=dev)
+    sc = torch.zeros(nbc + 16, dtype=torch.uint8, device=dev)
+    s = torch.cuda.current_stream(dev).cuda_stream
+    code = L.mx_quantize(x.data_ptr(), 1, R, Cc, 3, 1, qr.data_ptr(), sr.data_ptr() + 1, qc.data_ptr(),
+                         sc.data_ptr() + 1, s)
+    assert code == 0
+    torch.cuda.synchronize()
+    ref = _oracle(bits(x), 3, 1)
+    assert_bytes_equal(u8(qr).reshape(ref["row"][0].shape), ref["row"][0], "q_row")
+    assert_bytes_equal(u8(sr[1:nb + 1]), ref["row"][1].ravel(), "s_row")
+    assert_bytes_equal(u8(qc).reshape(ref["col"][0].shape), ref["col"][0], "q_col")
+    assert_bytes_equal(u8(sc[1:nbc + 1]), ref["col"][1].ravel(), "s_col")
 
 
 def test_quantize_special_values(dev):
