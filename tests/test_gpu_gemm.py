@@ -96,7 +96,8 @@ def test_scale_layout_bit_exact(dev):
 
 
 @pytest.mark.parametrize("out_dtype", [1, 0])
-@pytest.mark.parametrize("sizes,N,K", [([384, 0, 128, 256], 256, 1024), ([128, 512], 768, 384)])
+@pytest.mark.parametrize("sizes,N,K", [([384, 0, 128, 256], 256, 1024), ([128, 512], 768, 384),
+                                       ([384, 0, 640], 1024, 256)])
 def test_random_operands(dev, out_dtype, sizes, N, K):
     g = np.random.default_rng(7)
     E = len(sizes)
@@ -114,11 +115,14 @@ def test_random_operands(dev, out_dtype, sizes, N, K):
         assert_bf16_within_one_ulp(bits(C)[:P], ref[:P], "C bf16")
 
 
-def test_wgrad_with_empty_group(dev):
+@pytest.mark.parametrize("N,K", [(256, 512), (512, 768)])
+def test_wgrad_with_empty_group(dev, N, K):
+    """Two column tiles per cluster (K = 512: two CTA pairs share the A tile)
+    and an odd count (K = 768: one pair per cluster)."""
     import mxfp8_mixture_experts_gb300 as m
     g = np.random.default_rng(3)
     sizes = [256, 0, 128, 384]
-    E, N, K = 4, 256, 512
+    E = 4
     M_cap = sum(sizes) + 128
     X = mx.bf16_to_f64(mx.f64_to_bf16_bits(g.standard_normal((M_cap, N))))
     Y = mx.bf16_to_f64(mx.f64_to_bf16_bits(g.standard_normal((M_cap, K))))
@@ -150,10 +154,11 @@ def test_bad_offsets_set_device_status(dev):
     assert torch.all(C == 7.0)
 
 
-def test_gemm1_swiglu_fused(dev):
+@pytest.mark.parametrize("F", [256, 384])
+def test_gemm1_swiglu_fused(dev, F):
     import mxfp8_mixture_experts_gb300 as m
     g = np.random.default_rng(5)
-    sizes, F, H = [256, 0, 128], 256, 512
+    sizes, H = [256, 0, 128], 512
     E = len(sizes)
     M_cap = sum(sizes) + 128
     x = mx.bf16_to_f64(mx.f64_to_bf16_bits(g.standard_normal((M_cap, H))))
