@@ -246,18 +246,6 @@ __device__ __forceinline__ void tma_load_2d_pair(void *smem_dst, const CUtensorM
       "l"(reinterpret_cast<uint64_t>(map)), "r"(cluster_bar), "r"(x), "r"(y)
       : "memory");
 }
-// tma_load_2d_pair with cluster multicast: the box lands at the same offset in
-// the shared memory of every CTA in cta_mask, and the bytes that land in a
-// destination CTA are counted on the mbarrier at cluster_bar's offset in the
-// even CTA of that destination's pair.
-__device__ __forceinline__ void tma_load_2d_pair_mc(void *smem_dst, const CUtensorMap *map, uint32_t cluster_bar,
-                                                    int32_t x, int32_t y, uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster."
-      "cta_group::2 [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(smem_dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(cluster_bar), "r"(x), "r"(y), "h"(cta_mask)
-      : "memory");
-}
 __device__ __forceinline__ void bulk_load(void *smem_dst, const void *gmem_src, uint32_t bytes, uint64_t *bar) {
   asm volatile(
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(

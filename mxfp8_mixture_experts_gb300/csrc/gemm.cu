@@ -337,11 +337,6 @@ mx_status make_map_u8_128x128_swz(CUtensorMap *m, const void *base, int64_t inne
   return make_map_u8_box_swz(m, base, inner, outer, 128, swizzle);
 }
 
-// 2-D uint8 map over [outer, inner], boxes of 128 bytes x box_rows rows, 128-byte swizzle
-mx_status make_map_u8_box(CUtensorMap *m, const void *base, int64_t inner, int64_t outer, int box_rows) {
-  return make_map_u8_box_swz(m, base, inner, outer, box_rows, (int)CU_TENSOR_MAP_SWIZZLE_128B);
-}
-
 static mx_status make_map_u8_box_swz(CUtensorMap *m, const void *base, int64_t inner, int64_t outer, int box_rows,
                                      int swizzle) {
   EncodeTiledFn fn = encode_fn();

@@ -70,23 +70,16 @@ struct PairTile {
   bool store;                                 // false: lone tile, odd CTA
 };
 
-// Work items: one per cluster.  With CL = 4 the cluster's two pairs take
-// neighbouring column tiles of the same rows (NP = CL / 2 pairs per item).
-template <int CL>
 __device__ __forceinline__ int64_t pair_tiles(const Params &p, const int32_t *pp) {
-  constexpr int NP = CL / 2;
-  if (p.op == OP_ROWS) return (int64_t)pp[p.E] * ((p.epi == EPI_GLU ? p.N / 128 : p.N / BN) / NP);
-  return (int64_t)p.E * (p.N / 256) * (p.K / BN / NP);
+  if (p.op == OP_ROWS) return (int64_t)pp[p.E] * (p.epi == EPI_GLU ? p.N / 128 : p.N / BN);
+  return (int64_t)p.E * (p.N / 256) * (p.K / BN);
 }
 
-// `pi`: this CTA's pair within the cluster; `rank`: its CTA within the pair.
-template <int CL>
 __device__ __forceinline__ PairTile decode_pair(const Params &p, const int32_t *off, const int32_t *pp, int64_t t,
-                                                uint32_t pi, uint32_t rank) {
-  constexpr int NP = CL / 2;
+                                                uint32_t rank) {
   PairTile tl;
   if (p.op == OP_ROWS) {
-    const int64_t n_tiles = (p.epi == EPI_GLU ? p.N / 128 : p.N / BN) / NP;
+    const int64_t n_tiles = p.epi == EPI_GLU ? p.N / 128 : p.N / BN;
     // tiles of group e are [pp[e] * n_tiles, pp[e+1] * n_tiles)
     const int e = upper_group(pp, p.E, t / n_tiles);
     const int64_t local = t - (int64_t)pp[e] * n_tiles;
@@ -99,7 +92,7 @@ __device__ __forceinline__ PairTile decode_pair(const Params &p, const int32_t *
     // the column tiles fastest and keep each activation row pair in L2.
     const bool rows_fastest = n_e * BM < b_rows;
     const int64_t j = rows_fastest ? local % np_e : local / n_tiles;
-    const int64_t nt = (rows_fastest ? local / np_e : local % n_tiles) * NP + pi;
+    const int64_t nt = rows_fastest ? local / np_e : local % n_tiles;
     const int64_t mt0 = off[e] / BM + 2 * j;
     const bool lone = (2 * j + 1 == n_e);
     const int64_t my_mt = mt0 + (lone ? 0 : rank);
@@ -126,7 +119,7 @@ __device__ __forceinline__ PairTile decode_pair(const Params &p, const int32_t *
   } else {
     // token-grouped (wgrad): output [e*N + 256-row tile, 256-column tile],
     // contraction over the group's tokens [off[e], off[e+1])
-    const int64_t rt_n = p.N / 256, ct_n = p.K / BN / NP;
+    const int64_t rt_n = p.N / 256, ct_n = p.K / BN;
     const int64_t per_e = rt_n * ct_n;
     const int e = (int)(t / per_e);
     const int64_t rem = t % per_e;
@@ -135,7 +128,7 @@ __device__ __forceinline__ PairTile decode_pair(const Params &p, const int32_t *
     // larger one streams from HBM once.
     const bool rows_fastest = p.N <= p.K;
     const int64_t rt = rows_fastest ? rem % rt_n : rem / ct_n;
-    const int64_t ct = (rows_fastest ? rem / rt_n : rem % ct_n) * NP + pi;
+    const int64_t ct = rows_fastest ? rem / rt_n : rem % ct_n;
     const int64_t kblocks = p.M_cap / BK;
     const int64_t kc0 = off[e] / BK;
     tl.a_row = rt * 256 + rank * 128;
@@ -174,7 +167,6 @@ __device__ __forceinline__ void stage_and_store(const CUtensorMap *map, uint8_t 
   }
 }
 
-template <int CL>
 __global__ void __launch_bounds__(P_THREADS, 1)
     k_grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
@@ -192,11 +184,7 @@ __global__ void __launch_bounds__(P_THREADS, 1)
   int32_t *s_pp = reinterpret_cast<int32_t *>(smem + C::SMEM_PP);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  static_assert(CL == 2 || CL == 4, "cluster of one or two CTA pairs");
-  const uint32_t crank = cluster_ctarank();
-  const uint32_t rank = crank & 1;       // CTA within the pair (0: issues the MMAs)
-  const uint32_t pi = crank >> 1;        // pair within the cluster
-  const uint32_t leader = crank & ~1u;   // cluster rank of this pair's even CTA
+  const uint32_t rank = cluster_ctarank();
   const int64_t cid = cluster_id_x(), ncl = nclusters_x();
 
   for (int i = threadIdx.x; i <= p.E; i += P_THREADS) s_off[i] = p.offsets[i];
@@ -216,7 +204,7 @@ __global__ void __launch_bounds__(P_THREADS, 1)
   if (warp == 0 && lane == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], CL / 2);  // freed by the MMAs of every pair that reads the stage
+      mbar_init(&empty[s], 1);
     }
     mbar_init(tmem_full, 1);
     mbar_init(tmem_empty, 2 * NUM_EPI_WARPS);
@@ -228,30 +216,27 @@ __global__ void __launch_bounds__(P_THREADS, 1)
     if (p.epi != EPI_GLU) prefetch_tmap(&tmC);
   }
   __syncthreads();
-  if (!*s_flag) return;  // identical decision in every CTA of the cluster
+  if (!*s_flag) return;  // identical decision in both CTAs of the pair
   if (warp == 1) {
     tmem_alloc_pair(tmem_slot, P_TMEM_COLS);
     tmem_relinquish_pair();
   }
   tc_fence_before();
-  cluster_sync();  // barriers of every CTA initialised, TMEM allocated in both CTAs of each pair
+  cluster_sync();  // barriers of both CTAs initialised, TMEM allocated in both
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  const int64_t ntiles = pair_tiles<CL>(p, s_pp);
+  const int64_t ntiles = pair_tiles(p, s_pp);
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer (both CTAs)
     // the whole warp runs the loop; one elected lane issues the copies
     {
-      const uint32_t leader_full0 = mapa_shared(smem_u32(&full[0]), leader);
-      // CL = 4: the two pairs need the same A rows; each CTA loads 64 of its
-      // 128 rows and multicasts them to the CTA of the same role in the other pair
-      const uint16_t a_mask = (uint16_t)((1u << rank) | (1u << (rank + 2)));
+      const uint32_t leader_full0 = mapa_shared(smem_u32(&full[0]), 0);
       int stage = 0;
       uint32_t phase = 0;
       bool dead = false;
       for (int64_t t = cid; t < ntiles && !dead; t += ncl) {
-        const PairTile tl = decode_pair<CL>(p, s_off, s_pp, t, pi, rank);
+        const PairTile tl = decode_pair(p, s_off, s_pp, t, rank);
         for (int kb = 0; kb < tl.num_k; ++kb) {
           if (!mbar_wait_warp(&empty[stage], phase ^ 1, WAIT_TIMEOUT_NS)) {
             if (lane == 0) set_status(p.dev_status, MX_ERR_TIMEOUT);
@@ -265,10 +250,7 @@ __global__ void __launch_bounds__(P_THREADS, 1)
             uint8_t *sb = smem + C::SMEM_B + stage * C::B_TILE;
             uint8_t *sf = smem + C::SMEM_SF + stage * C::SF_STAGE;
             const int32_t kc = (int32_t)(tl.k0 + (int64_t)kb * BK);
-            if (CL == 2)
-              tma_load_2d_pair(sa, &tmA, bar, kc, (int32_t)tl.a_row);
-            else
-              tma_load_2d_pair_mc(sa + pi * (C::A_TILE / 2), &tmA, bar, kc, (int32_t)(tl.a_row + 64 * pi), a_mask);
+            tma_load_2d_pair(sa, &tmA, bar, kc, (int32_t)tl.a_row);
             tma_load_2d_pair(sb, &tmB, bar, kc, (int32_t)tl.b_row);
             tma_load_2d_pair(sf, &tmSFA, bar, 0, (int32_t)(tl.sfa_chunk + kb));
             tma_load_2d_pair(sf + 512, &tmSFB, bar, 0, (int32_t)(tl.sfb_chunk0 + kb));
@@ -293,7 +275,7 @@ __global__ void __launch_bounds__(P_THREADS, 1)
       const uint32_t idesc = idesc_mxf8(2 * BM, C::TN);
       const uint32_t d_tmem = tmem_base + C::ACC_COL;
       for (int64_t t = cid; t < ntiles && !dead; t += ncl) {
-        const PairTile tl = decode_pair<CL>(p, s_off, s_pp, t, pi, rank);
+        const PairTile tl = decode_pair(p, s_off, s_pp, t, rank);
         if (tl.num_k == 0) continue;
         if (!mbar_wait_warp(tmem_empty, acc_phase ^ 1, WAIT_TIMEOUT_NS)) {
           if (lane == 0) set_status(p.dev_status, MX_ERR_TIMEOUT);
@@ -324,7 +306,7 @@ __global__ void __launch_bounds__(P_THREADS, 1)
               const uint32_t id = idesc | ((uint32_t)kk << 4) | ((uint32_t)kk << 29);
               tc_mma_mxf8_pair(d_tmem, ad, bd, id, sfa_t, sfb_t, (kb | kk) != 0);
             }
-            tc_commit_pair(&empty[stage], CL == 2 ? 0x3 : 0xF);
+            tc_commit_pair(&empty[stage], 0x3);
           }
           __syncwarp();
           if (++stage == C::STAGES) {
@@ -333,7 +315,7 @@ __global__ void __launch_bounds__(P_THREADS, 1)
           }
         }
         if (dead) break;
-        if (elect_one_sync()) tc_commit_pair(tmem_full, (uint16_t)(0x3u << leader));
+        if (elect_one_sync()) tc_commit_pair(tmem_full, 0x3);
         __syncwarp();
         acc_phase ^= 1;
       }
@@ -347,12 +329,12 @@ __global__ void __launch_bounds__(P_THREADS, 1)
     const int q = warp & 3;
     const int h = (warp - 2) >> 2;
     const int row_in_tile = q * 32 + lane;
-    const uint32_t leader_tmem_empty = mapa_shared(smem_u32(tmem_empty), leader);
+    const uint32_t leader_tmem_empty = mapa_shared(smem_u32(tmem_empty), 0);
     uint8_t *ebuf = smem + C::SMEM_EPI + (warp - 2) * C::EPI_BUFS * P_EPI_BUF;
     int nstore = 0;
     uint32_t acc_phase = 0;
     for (int64_t t = cid; t < ntiles; t += ncl) {
-      const PairTile tl = decode_pair<CL>(p, s_off, s_pp, t, pi, rank);
+      const PairTile tl = decode_pair(p, s_off, s_pp, t, rank);
       const int64_t orow = tl.out_row + row_in_tile;
       if (tl.num_k == 0) {
         epi_zero(p, orow, tl.out_col + h * EC, EC);
@@ -429,10 +411,9 @@ __global__ void __launch_bounds__(P_THREADS, 1)
 }
 
 static std::mutex g_pmu;
-static int g_psmem_set[2][64];
-static int g_pclusters[2][64];
+static int g_psmem_set[64];
+static int g_pclusters[64];
 
-template <int CL>
 static void pair_config(cudaLaunchConfig_t *cfg, cudaLaunchAttribute *attr, int grid, mx_stream stream) {
   *cfg = cudaLaunchConfig_t{};
   cfg->gridDim = dim3(grid, 1, 1);
@@ -440,43 +421,40 @@ static void pair_config(cudaLaunchConfig_t *cfg, cudaLaunchAttribute *attr, int 
   cfg->dynamicSmemBytes = PairCfg::SMEM_ALLOC;
   cfg->stream = stream;
   attr->id = cudaLaunchAttributeClusterDimension;
-  attr->val.clusterDim.x = CL;
+  attr->val.clusterDim.x = 2;
   attr->val.clusterDim.y = 1;
   attr->val.clusterDim.z = 1;
   cfg->attrs = attr;
   cfg->numAttrs = 1;
 }
 
-template <int CL>
-static mx_status launch_pair_cl(const Params &p, const uint8_t *A, int64_t a_inner, int64_t a_outer, const uint8_t *B,
-                                int64_t b_inner, int64_t b_outer, int64_t sfa_bytes, int64_t sfb_bytes,
-                                mx_stream stream) {
-  constexpr int W = CL == 2 ? 0 : 1;
+mx_status launch_pair(const Params &p, const uint8_t *A, int64_t a_inner, int64_t a_outer, const uint8_t *B,
+                      int64_t b_inner, int64_t b_outer, int64_t sfa_bytes, int64_t sfb_bytes, mx_stream stream) {
   int dev = 0;
   MX_CUDA_TRY(cudaGetDevice(&dev));
   if (dev < 0 || dev >= 64) return MX_ERR_CUDA;
   int clusters = 0;
   {
-    // the persistent grid is as many clusters as can be resident at once
+    // the persistent grid is as many CTA pairs as can be resident at once
     std::lock_guard<std::mutex> lk(g_pmu);
-    if (!g_psmem_set[W][dev]) {
-      MX_CUDA_TRY(cudaFuncSetAttribute(k_grouped_gemm_pair<CL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (!g_psmem_set[dev]) {
+      MX_CUDA_TRY(cudaFuncSetAttribute(k_grouped_gemm_pair, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        PairCfg::SMEM_ALLOC));
       int sms = 0;
       MX_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
       cudaLaunchConfig_t cfg;
       cudaLaunchAttribute attr;
-      pair_config<CL>(&cfg, &attr, (sms / CL) * CL, nullptr);
+      pair_config(&cfg, &attr, (sms / 2) * 2, nullptr);
       int n = 0;
-      MX_CUDA_TRY(cudaOccupancyMaxActiveClusters(&n, k_grouped_gemm_pair<CL>, &cfg));
+      MX_CUDA_TRY(cudaOccupancyMaxActiveClusters(&n, k_grouped_gemm_pair, &cfg));
       if (n < 1) return MX_ERR_CUDA;
-      g_pclusters[W][dev] = n < sms / CL ? n : sms / CL;
-      g_psmem_set[W][dev] = 1;
+      g_pclusters[dev] = n < sms / 2 ? n : sms / 2;
+      g_psmem_set[dev] = 1;
     }
-    clusters = g_pclusters[W][dev];
+    clusters = g_pclusters[dev];
   }
   CUtensorMap ma, mb, msa, msb, mc;
-  mx_status st = CL == 2 ? make_map_u8_128x128(&ma, A, a_inner, a_outer) : make_map_u8_box(&ma, A, a_inner, a_outer, 64);
+  mx_status st = make_map_u8_128x128(&ma, A, a_inner, a_outer);
   if (st == MX_OK) st = make_map_u8_128x128(&mb, B, b_inner, b_outer);
   if (st == MX_OK) st = make_map_sf_chunks(&msa, p.sA, sfa_bytes / 512);
   if (st == MX_OK) st = make_map_sf_chunks(&msb, p.sB, sfb_bytes / 512);
@@ -490,19 +468,9 @@ static mx_status launch_pair_cl(const Params &p, const uint8_t *A, int64_t a_inn
   if (st != MX_OK) return st;
   cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attr;
-  pair_config<CL>(&cfg, &attr, CL * clusters, stream);
-  MX_CUDA_TRY(cudaLaunchKernelEx(&cfg, k_grouped_gemm_pair<CL>, ma, mb, msa, msb, mc, p));
+  pair_config(&cfg, &attr, 2 * clusters, stream);
+  MX_CUDA_TRY(cudaLaunchKernelEx(&cfg, k_grouped_gemm_pair, ma, mb, msa, msb, mc, p));
   return launch_status();
-}
-
-// Two CTA pairs per cluster (sharing the A tile through multicast) whenever
-// the column tiles come in pairs; one pair otherwise.
-mx_status launch_pair(const Params &p, const uint8_t *A, int64_t a_inner, int64_t a_outer, const uint8_t *B,
-                      int64_t b_inner, int64_t b_outer, int64_t sfa_bytes, int64_t sfb_bytes, mx_stream stream) {
-  const int64_t col_tiles = p.op == OP_TOKENS ? p.K / BN : (p.epi == EPI_GLU ? p.N / 128 : p.N / BN);
-  if (col_tiles % 2 == 0)
-    return launch_pair_cl<4>(p, A, a_inner, a_outer, B, b_inner, b_outer, sfa_bytes, sfb_bytes, stream);
-  return launch_pair_cl<2>(p, A, a_inner, a_outer, B, b_inner, b_outer, sfa_bytes, sfb_bytes, stream);
 }
 
 }  // namespace gemm

@@ -136,7 +136,6 @@ __device__ __forceinline__ void epi_store(const Params &p, int64_t orow, int64_t
 // host
 mx_status make_map_u8_128x128(CUtensorMap *m, const void *base, int64_t inner, int64_t outer);
 mx_status make_map_u8_128x128_swz(CUtensorMap *m, const void *base, int64_t inner, int64_t outer, int swizzle);
-mx_status make_map_u8_box(CUtensorMap *m, const void *base, int64_t inner, int64_t outer, int box_rows);
 mx_status make_map_sf_chunks(CUtensorMap *m, const void *base, int64_t nchunks);
 mx_status make_map_store_64b(CUtensorMap *m, void *base, bool f32, int64_t cols, int64_t rows);
 mx_status launch_1cta(const Params &p, const uint8_t *A, int64_t a_inner, int64_t a_outer, const uint8_t *B,

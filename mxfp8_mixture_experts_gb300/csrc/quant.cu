@@ -69,8 +69,12 @@ __global__ void __launch_bounds__(QT_THREADS) k_quantize_bf16(QuantArgs a) {
   constexpr int ITERS = (QT_ROWS * QT_COLS / 8) / QT_THREADS;  // 4 chunks of 8 per thread
   const int tid = threadIdx.x;
   const int64_t b = blockIdx.z;
-  const int64_t row0 = (int64_t)blockIdx.y * QT_ROWS;
-  const int64_t col0 = (int64_t)blockIdx.x * QT_COLS;
+  // COL-only mode walks row bands fastest: CTAs resident together then cover
+  // neighbouring row bands of the same columns and the transposed writes form
+  // long runs (measured 13% faster); with ROW output, column tiles fastest
+  // keep the row-major reads and writes contiguous instead.
+  const int64_t row0 = (int64_t)(ROW ? blockIdx.y : blockIdx.x) * QT_ROWS;
+  const int64_t col0 = (int64_t)(ROW ? blockIdx.x : blockIdx.y) * QT_COLS;
   const uint16_t *x = a.x + b * a.rows * a.cols;
   const int64_t cblocks = a.cols / 32, rblocks = a.rows / 32;
 
@@ -202,8 +206,8 @@ __global__ void __launch_bounds__(SB_THREADS) k_swiglu_bwd(const float *__restri
   uint8_t *qst = sb_smem + 3 * SB_ROWS * SB_VAL_STRIDE * 4;                    // [3][32][144]
   uint8_t *sst = qst + 3 * SB_COLS * SB_Q_STRIDE;                             // [3][32][4]
   const int tid = threadIdx.x;
-  const int64_t row0 = (int64_t)blockIdx.y * SB_ROWS;
-  const int64_t f0 = (int64_t)blockIdx.x * SB_COLS;
+  const int64_t row0 = (int64_t)blockIdx.x * SB_ROWS;  // row bands fastest (see k_quantize_bf16)
+  const int64_t f0 = (int64_t)blockIdx.y * SB_COLS;
   const int64_t twoF = 2 * F;
   const int64_t cb2 = twoF / 32;
 
@@ -335,7 +339,7 @@ extern "C" mx_status mx_quantize(const void *x, int64_t batch, int64_t rows, int
   MX_HOST_CHECK(!col || (q_col && s_col), MX_ERR_INVALID_ARG);
   MX_HOST_CHECK(cols % 32 == 0 && (!col || rows % 32 == 0), MX_ERR_SHAPE);
   MX_HOST_CHECK(aligned16(x) && (!row || aligned16(q_row)) && (!col || aligned16(q_col)), MX_ERR_ALIGNMENT);
-  MX_HOST_CHECK(rows / QT_ROWS < 65535 && batch < 65535, MX_ERR_SHAPE);
+  MX_HOST_CHECK(rows / QT_ROWS < 65535 && cols / QT_COLS < 65535 && batch < 65535, MX_ERR_SHAPE);
   mx_status st = check_device_cached();
   if (st != MX_OK) return st;
   QuantArgs a;
@@ -359,7 +363,8 @@ extern "C" mx_status mx_quantize(const void *x, int64_t batch, int64_t rows, int
     if (col && (cols % 128 || (rows / 32) % 4))
       MX_CUDA_TRY(cudaMemsetAsync(s_col, 0, a.s_col_stride * batch, stream));
   }
-  dim3 grid((unsigned)((cols + QT_COLS - 1) / QT_COLS), (unsigned)((rows + QT_ROWS - 1) / QT_ROWS), (unsigned)batch);
+  const unsigned nrb = (unsigned)((rows + QT_ROWS - 1) / QT_ROWS), ncb = (unsigned)((cols + QT_COLS - 1) / QT_COLS);
+  const dim3 grid = row ? dim3(ncb, nrb, (unsigned)batch) : dim3(nrb, ncb, (unsigned)batch);
   if (row && col)
     k_quantize_bf16<true, true, false><<<grid, QT_THREADS, 0, stream>>>(a);
   else if (row)
@@ -378,7 +383,7 @@ extern "C" mx_status moe_gather_quant(const void *x, const float *gate, const in
   const bool row = mode & MX_MODE_ROW, col = mode & MX_MODE_COL;
   MX_HOST_CHECK(!row || (q_row && s_row), MX_ERR_INVALID_ARG);
   MX_HOST_CHECK(!col || (q_col && s_col), MX_ERR_INVALID_ARG);
-  MX_HOST_CHECK(H % 128 == 0 && rows_cap % 128 == 0, MX_ERR_SHAPE);
+  MX_HOST_CHECK(H % 128 == 0 && rows_cap % 128 == 0 && H / QT_COLS < 65535, MX_ERR_SHAPE);
   MX_HOST_CHECK(aligned16(x) && (!row || aligned16(q_row)) && (!col || aligned16(q_col)), MX_ERR_ALIGNMENT);
   mx_status st = check_device_cached();
   if (st != MX_OK) return st;
@@ -397,7 +402,9 @@ extern "C" mx_status moe_gather_quant(const void *x, const float *gate, const in
   a.s_row_stride = 0;
   a.s_col_stride = 0;
   a.swizzled = 1;
-  dim3 grid((unsigned)(H / QT_COLS), (unsigned)(rows_cap / QT_ROWS), 1);
+  const unsigned nrb = (unsigned)(rows_cap / QT_ROWS), ncb = (unsigned)(H / QT_COLS);
+  MX_HOST_CHECK(nrb < 65535 || !row, MX_ERR_SHAPE);
+  const dim3 grid = row ? dim3(ncb, nrb, 1) : dim3(nrb, ncb, 1);
   if (row && col)
     k_quantize_bf16<true, true, true><<<grid, QT_THREADS, 0, stream>>>(a);
   else if (row)
@@ -412,7 +419,7 @@ extern "C" mx_status moe_swiglu_bwd(const float *dh, const void *ab, int64_t row
                                     uint8_t *h_cs, mx_stream stream) {
   MX_HOST_CHECK(dh && ab && dab_rq && dab_rs && dab_cq && dab_cs && h_cq && h_cs, MX_ERR_INVALID_ARG);
   MX_HOST_CHECK(rows >= 0 && F > 0, MX_ERR_INVALID_ARG);
-  MX_HOST_CHECK(rows % SB_ROWS == 0 && F % SB_COLS == 0, MX_ERR_SHAPE);
+  MX_HOST_CHECK(rows % SB_ROWS == 0 && F % SB_COLS == 0 && F / SB_COLS < 65535, MX_ERR_SHAPE);
   MX_HOST_CHECK(aligned16(dh) && aligned16(ab) && aligned16(dab_rq) && aligned16(dab_cq) && aligned16(h_cq),
                 MX_ERR_ALIGNMENT);
   mx_status st = check_device_cached();
@@ -425,7 +432,7 @@ extern "C" mx_status moe_swiglu_bwd(const float *dh, const void *ab, int64_t row
     MX_CUDA_TRY(cudaFuncSetAttribute(k_swiglu_bwd, cudaFuncAttributeMaxDynamicSharedMemorySize, SB_SMEM));
     smem_set[dev] = 1;
   }
-  dim3 grid((unsigned)(F / SB_COLS), (unsigned)(rows / SB_ROWS));
+  dim3 grid((unsigned)(rows / SB_ROWS), (unsigned)(F / SB_COLS));
   k_swiglu_bwd<<<grid, SB_THREADS, SB_SMEM, stream>>>(dh, static_cast<const uint16_t *>(ab), rows, F, dab_rq, dab_rs,
                                                       dab_cq, dab_cs, h_cq, h_cs);
   return launch_status();

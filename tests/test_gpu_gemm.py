@@ -117,8 +117,8 @@ def test_random_operands(dev, out_dtype, sizes, N, K):
 
 @pytest.mark.parametrize("N,K", [(256, 512), (512, 768)])
 def test_wgrad_with_empty_group(dev, N, K):
-    """Two column tiles per cluster (K = 512: two CTA pairs share the A tile)
-    and an odd count (K = 768: one pair per cluster)."""
+    """An even (K = 512) and an odd (K = 768) number of 256-wide column
+    tiles, with an empty group in the middle."""
     import mxfp8_mixture_experts_gb300 as m
     g = np.random.default_rng(3)
     sizes = [256, 0, 128, 384]
