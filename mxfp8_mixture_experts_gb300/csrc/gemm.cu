@@ -383,6 +383,19 @@ mx_status make_map_store_64b(CUtensorMap *m, void *base, bool f32, int64_t cols,
   return r == CUDA_SUCCESS ? MX_OK : MX_ERR_CUDA;
 }
 
+// uint8 variant: [rows, cols] bytes, boxes of 32 rows x 64 bytes, 64-byte swizzle
+mx_status make_map_store_64b_u8(CUtensorMap *m, void *base, int64_t cols, int64_t rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return MX_ERR_CUDA;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols};
+  cuuint32_t box[2] = {64, 32};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MX_OK : MX_ERR_CUDA;
+}
+
 static std::mutex g_mu;
 static int g_smem_set[64];
 static int g_num_sms[64];

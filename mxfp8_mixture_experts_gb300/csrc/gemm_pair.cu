@@ -167,10 +167,58 @@ __device__ __forceinline__ void stage_and_store(const CUtensorMap *map, uint8_t 
   }
 }
 
+// SwiGLU epilogue of GEMM1 for one thread's row: r[0..63] = a, r[64..127] =
+// b for features [f0, f0 + 64).  a and b are rounded to bf16 and saved; h =
+// silu(a) * b in fp32 is quantized in two 32-element blocks.  The warp's 32
+// rows leave as five 64-byte-wide TMA stores (two of a, two of b, one of h);
+// the two scale bytes of the row are stored directly.
+template <int NBUF>
+__device__ __forceinline__ void glu_epilogue(const Params &p, const CUtensorMap *tmAB, const CUtensorMap *tmH,
+                                             uint8_t *ebuf, int &nstore, int lane, int64_t orow, int y, int f0,
+                                             const uint32_t (&r)[128]) {
+  const int64_t F = p.N;
+  uint4 hv4[4];
+#pragma unroll
+  for (int blk = 0; blk < 2; ++blk) {
+    float hv[32];
+    uint32_t am = 0;
+    uint4 va[4], vb[4];
+#pragma unroll
+    for (int j = 0; j < 32; j += 8) {
+      float av[8], bv[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        av[i] = round_bf16(__uint_as_float(r[blk * 32 + j + i]));
+        bv[i] = round_bf16(__uint_as_float(r[64 + blk * 32 + j + i]));
+        hv[j + i] = silu_f(av[i]) * bv[i];
+        am = max(am, abs_bits(hv[j + i]));
+      }
+      va[j / 8] = make_uint4(pack_bf16x2(av[0], av[1]), pack_bf16x2(av[2], av[3]), pack_bf16x2(av[4], av[5]),
+                             pack_bf16x2(av[6], av[7]));
+      vb[j / 8] = make_uint4(pack_bf16x2(bv[0], bv[1]), pack_bf16x2(bv[2], bv[3]), pack_bf16x2(bv[4], bv[5]),
+                             pack_bf16x2(bv[6], bv[7]));
+    }
+    stage_and_store<NBUF>(tmAB, ebuf + (nstore++ % NBUF) * P_EPI_BUF, va, lane, f0 + blk * 32, y);
+    stage_and_store<NBUF>(tmAB, ebuf + (nstore++ % NBUF) * P_EPI_BUF, vb, lane, (int)F + f0 + blk * 32, y);
+    const MxScale s = mx_scale_from_amax_bits(am);
+    uint32_t w[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      w[i] = s.bad ? 0x7f7f7f7fu
+                   : pack_e4m3x4(hv[4 * i] * s.inv, hv[4 * i + 1] * s.inv, hv[4 * i + 2] * s.inv,
+                                 hv[4 * i + 3] * s.inv);
+    hv4[blk * 2] = make_uint4(w[0], w[1], w[2], w[3]);
+    hv4[blk * 2 + 1] = make_uint4(w[4], w[5], w[6], w[7]);
+    p.hs[sf_swizzle_offset(orow, f0 / 32 + blk, round_up(F / 32, 4))] = (uint8_t)s.byte;
+  }
+  stage_and_store<NBUF>(tmH, ebuf + (nstore++ % NBUF) * P_EPI_BUF, hv4, lane, f0, y);
+}
+
 __global__ void __launch_bounds__(P_THREADS, 1)
     k_grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
-                        const __grid_constant__ CUtensorMap tmC, Params p) {
+                        const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmH,
+                        Params p) {
   using C = PairCfg;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -213,7 +261,8 @@ __global__ void __launch_bounds__(P_THREADS, 1)
     prefetch_tmap(&tmB);
     prefetch_tmap(&tmSFA);
     prefetch_tmap(&tmSFB);
-    if (p.epi != EPI_GLU) prefetch_tmap(&tmC);
+    prefetch_tmap(&tmC);
+    if (p.epi == EPI_GLU) prefetch_tmap(&tmH);
   }
   __syncthreads();
   if (!*s_flag) return;  // identical decision in both CTAs of the pair
@@ -363,12 +412,12 @@ __global__ void __launch_bounds__(P_THREADS, 1)
       if (lane == 0) mbar_arrive_cluster_relaxed(leader_tmem_empty);
       acc_phase ^= 1;
       if (!tl.store) continue;
+      const int y = (int)(tl.out_row + q * 32);
       if (p.epi == EPI_GLU) {
-        epi_store(p, orow, tl.out_col + h * 64, r);
+        glu_epilogue<C::EPI_BUFS>(p, &tmC, &tmH, ebuf, nstore, lane, orow, y, (int)(tl.out_col + h * 64), r);
         continue;
       }
       // 64-byte row segments: fp32 16 columns, bf16 32 columns per chunk
-      const int y = (int)(tl.out_row + q * 32);
       const int x0 = (int)(tl.out_col + h * EC);
       if (p.epi == EPI_F32) {
 #pragma unroll
@@ -453,7 +502,7 @@ mx_status launch_pair(const Params &p, const uint8_t *A, int64_t a_inner, int64_
     }
     clusters = g_pclusters[dev];
   }
-  CUtensorMap ma, mb, msa, msb, mc;
+  CUtensorMap ma, mb, msa, msb, mc, mh;
   mx_status st = make_map_u8_128x128(&ma, A, a_inner, a_outer);
   if (st == MX_OK) st = make_map_u8_128x128(&mb, B, b_inner, b_outer);
   if (st == MX_OK) st = make_map_sf_chunks(&msa, p.sA, sfa_bytes / 512);
@@ -462,14 +511,17 @@ mx_status launch_pair(const Params &p, const uint8_t *A, int64_t a_inner, int64_
     const int64_t rows = p.op == OP_ROWS ? p.M_cap : (int64_t)p.E * p.N;
     const int64_t ldc = p.op == OP_ROWS ? p.N : p.K;
     st = make_map_store_64b(&mc, p.C, p.epi == EPI_F32, ldc, rows);
-  } else {
-    mc = ma;  // unused by the SwiGLU epilogue
+    mh = mc;  // unused outside the SwiGLU epilogue
+  } else if (st == MX_OK) {
+    // SwiGLU: a|b bf16 [M_cap, 2F] and h E4M3 [M_cap, F]
+    st = make_map_store_64b(&mc, p.ab, false, 2 * p.N, p.M_cap);
+    if (st == MX_OK) st = make_map_store_64b_u8(&mh, p.hq, p.N, p.M_cap);
   }
   if (st != MX_OK) return st;
   cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attr;
   pair_config(&cfg, &attr, 2 * clusters, stream);
-  MX_CUDA_TRY(cudaLaunchKernelEx(&cfg, k_grouped_gemm_pair, ma, mb, msa, msb, mc, p));
+  MX_CUDA_TRY(cudaLaunchKernelEx(&cfg, k_grouped_gemm_pair, ma, mb, msa, msb, mc, mh, p));
   return launch_status();
 }
 

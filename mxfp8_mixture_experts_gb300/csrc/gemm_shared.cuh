@@ -138,6 +138,7 @@ mx_status make_map_u8_128x128(CUtensorMap *m, const void *base, int64_t inner, i
 mx_status make_map_u8_128x128_swz(CUtensorMap *m, const void *base, int64_t inner, int64_t outer, int swizzle);
 mx_status make_map_sf_chunks(CUtensorMap *m, const void *base, int64_t nchunks);
 mx_status make_map_store_64b(CUtensorMap *m, void *base, bool f32, int64_t cols, int64_t rows);
+mx_status make_map_store_64b_u8(CUtensorMap *m, void *base, int64_t cols, int64_t rows);
 mx_status launch_1cta(const Params &p, const uint8_t *A, int64_t a_inner, int64_t a_outer, const uint8_t *B,
                       int64_t b_inner, int64_t b_outer, int64_t max_tiles, mx_stream stream);
 mx_status launch_pair(const Params &p, const uint8_t *A, int64_t a_inner, int64_t a_outer, const uint8_t *B,
