@@ -98,6 +98,18 @@ int32_t mx_abi_version(void);
 /* MX_OK if the current CUDA device is an sm_103 part this library runs on. */
 mx_status mx_check_device(void);
 
+/*
+ * Self-test of the device-side failure path (no counterpart on the pages:
+ * it checks this library's own error handling).  Every pipeline wait in the
+ * kernels is bounded; when a wait expires, the kernel writes MX_ERR_TIMEOUT to
+ * dev_status, leaves its loops and exits with nothing in flight, so the CUDA
+ * context stays usable.  This call runs one warp that waits, through the same
+ * bounded wait, on an mbarrier that nothing ever arrives on, for timeout_ns
+ * nanoseconds (at most 100 ms), then records MX_ERR_TIMEOUT in dev_status
+ * (device int32, required).  Enqueued on `stream`; returns host errors only.
+ */
+mx_status mx_selftest_wait_timeout(int64_t timeout_ns, int32_t *dev_status, mx_stream stream);
+
 /* Bytes of a scale array for `rows` x `cols` elements (cols % 32 == 0) in the
  * given layout: rows*cols/32 (PLAIN) or the padded tile size (SWIZZLED). */
 int64_t mx_scale_bytes(int64_t rows, int64_t cols, int32_t layout);

@@ -37,6 +37,7 @@ SIGNATURES = {
     "mx_status_string": (C.c_char_p, [_i32]),
     "mx_abi_version": (_i32, []),
     "mx_check_device": (_i32, []),
+    "mx_selftest_wait_timeout": (_i32, [_i64, _p, _p]),
     "mx_scale_bytes": (_i64, [_i64, _i64, _i32]),
     "mx_quantize": (_i32, [_p, _i64, _i64, _i64, _i32, _i32, _p, _p, _p, _p, _p]),
     "moe_route": (_i32, [_p, _i64, _i32, _i32, _p, _p, _p]),

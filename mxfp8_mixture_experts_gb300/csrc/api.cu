@@ -28,7 +28,29 @@ mx_status launch_status() {
   return e == cudaSuccess ? MX_OK : MX_ERR_CUDA;
 }
 
+// One warp waits, with the kernels' own bounded warp-wide wait, on an mbarrier
+// that nothing ever arrives on; when the limit passes it records
+// MX_ERR_TIMEOUT and exits.  Nothing is in flight when it returns.
+__global__ void k_selftest_wait_timeout(uint64_t timeout_ns, int32_t *dev_status) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  if (!mbar_wait_warp(&bar, 0, timeout_ns) && threadIdx.x == 0) set_status(dev_status, MX_ERR_TIMEOUT);
+}
+
 }  // namespace mxmoe
+
+extern "C" mx_status mx_selftest_wait_timeout(int64_t timeout_ns, int32_t *dev_status, mx_stream stream) {
+  MX_HOST_CHECK(dev_status != nullptr, MX_ERR_INVALID_ARG);
+  MX_HOST_CHECK(timeout_ns > 0 && timeout_ns <= 100000000, MX_ERR_INVALID_ARG);  // at most 100 ms
+  mx_status st = mxmoe::check_device_cached();
+  if (st != MX_OK) return st;
+  mxmoe::k_selftest_wait_timeout<<<1, 32, 0, stream>>>((uint64_t)timeout_ns, dev_status);
+  return mxmoe::launch_status();
+}
 
 extern "C" const char *mx_status_string(mx_status s) {
   switch (s) {

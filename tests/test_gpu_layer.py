@@ -229,3 +229,50 @@ def test_layer_end_to_end_vs_independent_oracle(dev):
         print(f"{n}: rel err vs MXFP8 oracle {e:.2e}, SQNR vs unquantized layer {sqnr:.1f} dB")
         assert e < 1e-2, n
         assert sqnr > 20, n
+
+
+def test_bounded_wait_reports_timeout_and_context_survives():
+    """The device failure path: a bounded wait on an mbarrier that nothing
+    arrives on expires after 20 ms and reports MX_ERR_TIMEOUT; the context
+    stays usable (a quantize right after it is still bit-exact)."""
+    import mxfp8_mixture_experts_gb300 as m
+    from mxfp8_mixture_experts_gb300 import _lib
+    from oracle import mx as omx
+    dev = torch.device("cuda", 0)
+    L = m.lib()
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    s = torch.cuda.current_stream(dev).cuda_stream
+    assert L.mx_selftest_wait_timeout(20_000_000, st.data_ptr(), s) == 0
+    torch.cuda.synchronize()
+    assert int(st.item()) == _lib.MX_ERR_TIMEOUT
+    assert L.mx_selftest_wait_timeout(0, st.data_ptr(), s) == _lib.MX_ERR_INVALID_ARG
+    assert L.mx_selftest_wait_timeout(10**9, st.data_ptr(), s) == _lib.MX_ERR_INVALID_ARG
+    x = workloads.quantize_input(64, 128, seed=4, device=dev)
+    q, sc, _, _ = m.mx_quantize(x, m.MX_MODE_ROW, m.MX_SCALE_PLAIN)
+    torch.cuda.synchronize()
+    qr, sr = omx.quantize_rows(omx.bf16_to_f64(workloads.bf16_bits(x)))
+    assert np.array_equal(q.cpu().numpy(), qr) and np.array_equal(sc.cpu().numpy().reshape(sr.shape), sr)
+
+
+def test_layer_is_deterministic():
+    """Two runs of the layer forward and backward on the same inputs give
+    bit-identical outputs (no atomics and fixed reduction orders)."""
+    import mxfp8_mixture_experts_gb300 as m
+    dev = torch.device("cuda", 0)
+    d = m.MoELayerDims(T=512, H=256, F=512, E=4, k=2)
+    inp = workloads.layer_inputs(workloads.LayerDims(T=d.T, H=d.H, E=d.E, F=d.F, k=d.k), seed=9, device=dev,
+                                 router="logits")
+    W13 = torch.cat([inp["W1"], inp["W3"]], dim=2).contiguous()
+
+    def run():
+        wq = m.moe_layer_prep_weights(W13, inp["W2"])
+        ws = torch.empty(m.moe_layer_workspace_size(d), dtype=torch.uint8, device=dev)
+        out, ids, gate = m.moe_layer_fwd(inp["x"], wq, d, ws, logits=inp["logits"])
+        dX, dW13, dW2, dg = m.moe_layer_bwd(inp["x"], inp["dOut"], gate, wq, d, ws)
+        torch.cuda.synchronize()
+        return [t.clone() for t in (out, ids, gate, dX, dW13, dW2, dg)]
+
+    a, b = run(), run()
+    for u, v in zip(a, b):
+        assert torch.equal(u.view(torch.uint8) if u.dtype != torch.int32 else u,
+                           v.view(torch.uint8) if v.dtype != torch.int32 else v)
