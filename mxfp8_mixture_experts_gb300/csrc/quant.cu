@@ -60,7 +60,9 @@ __device__ __forceinline__ uint32_t quant32_store(const float *v, uint8_t *dst) 
 }
 
 template <bool ROW, bool COL, bool GATHER>
-__global__ void __launch_bounds__(QT_THREADS) k_quantize_bf16(QuantArgs a) {
+// 6 resident CTAs per SM (registers capped at 42): 1.5-2% faster than the
+// register-limited 5, measured side by side in one process.
+__global__ void __launch_bounds__(QT_THREADS, 6) k_quantize_bf16(QuantArgs a) {
   __shared__ __align__(16) uint16_t tile[QT_ROWS][QT_COLS];
   // COL output staged as [64 columns][128 rows] bytes (+16 pad per row: the
   // 16-byte writes of 8 consecutive columns then fall in distinct banks)

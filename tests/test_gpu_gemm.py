@@ -246,3 +246,19 @@ def test_full_size_grouped_gemm_sampled(dev):
         X = deq_rows(c_cq, c_cs, n_s, M)[:, lo:hi]
         Y = deq_rows(a_cq, a_cs, k_s, M)[:, lo:hi]
         assert rel_frob(dWh[e][np.ix_(n_s, k_s)], X @ Y.T) <= TOL
+
+
+def test_one_cta_kernel_variant():
+    """The one-CTA kernel (128 x 256 tiles, selected by MXMOE_GEMM_CTAS=1 at
+    process start) passes the same GEMM tests in a child process."""
+    import os
+    import subprocess
+    import sys
+    if os.environ.get("MXMOE_GEMM_CTAS") == "1":
+        pytest.skip("already running the one-CTA variant")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, MXMOE_GEMM_CTAS="1")
+    r = subprocess.run([sys.executable, "-m", "pytest", os.path.join(root, "tests", "test_gpu_gemm.py"), "-q", "-x",
+                        "-m", "gpu", "-k", "not one_cta and not full_size", "-p", "no:cacheprovider"],
+                       cwd=root, env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-2000:]
