@@ -276,3 +276,173 @@ def test_layer_is_deterministic():
     for u, v in zip(a, b):
         assert torch.equal(u.view(torch.uint8) if u.dtype != torch.int32 else u,
                            v.view(torch.uint8) if v.dtype != torch.int32 else v)
+
+
+# ---------------------------------------------------------------------------
+# full-size layer (T=16384, H=5120, E=16, F=8192, top-1 softmax router): every
+# stage checked on sampled outputs that the oracle computes one at a time, on
+# the GPU's own inputs to that stage
+# ---------------------------------------------------------------------------
+def _rows_u8(t, rows):
+    return t[torch.as_tensor(np.asarray(rows), device=t.device)].cpu().numpy().astype(np.uint8)
+
+
+def _deq_sampled(q_rows, s_flat, rows, ncols):
+    """Dequantize sampled rows of an MXFP8 matrix with ncols columns whose
+    scales are in the swizzled layout (flat numpy array)."""
+    cb = ncols // 32
+    rr, cc = np.meshgrid(np.asarray(rows), np.arange(cb), indexing="ij")
+    sc = s_flat[mx.swizzled_offset(rr, cc, cb)]
+    return mx.dequantize_rows(q_rows, sc)
+
+
+def _sampled_scales(s_flat, rows, ncols):
+    cb = ncols // 32
+    rr, cc = np.meshgrid(np.asarray(rows), np.arange(cb), indexing="ij")
+    return s_flat[mx.swizzled_offset(rr, cc, cb)]
+
+
+def _dot_check(got, terms, what, rel=1e-4):
+    """fp32-accumulated dot products against the fp64 sum of the same terms:
+    |got - ref| <= rel * sum |terms| (a bound that holds without cancellation
+    assumptions)."""
+    ref = terms.sum(axis=-1)
+    bound = rel * np.abs(terms).sum(axis=-1) + 1e-30
+    bad = np.abs(np.asarray(got, np.float64) - ref) > bound
+    assert not bad.any(), f"{what}: {int(bad.sum())} sampled entries off; first {np.argwhere(bad)[:3].tolist()}"
+
+
+def test_layer_full_size_sampled(dev):
+    import mxfp8_mixture_experts_gb300 as m
+    dims = workloads.FULL_LAYER
+    d = m.MoELayerDims(T=dims.T, H=dims.H, F=dims.F, E=dims.E, k=dims.k)
+    T, H, F, E, k = d.T, d.H, d.F, d.E, d.k
+    inp = workloads.layer_inputs(dims, seed=0, device=dev, router="logits")
+    s = _staged(dev, inp, d, inp["logits"])
+    R = s["R"]
+    g = np.random.default_rng(123)
+
+    # router and grouping map: exact over all tokens
+    ids_ref, gate_ref = moe.route(inp["logits"].cpu().numpy(), k)
+    assert np.array_equal(s["ids"].cpu().numpy(), ids_ref)
+    gate = s["gate"].cpu().numpy()
+    np.testing.assert_allclose(gate, gate_ref, rtol=2e-6, atol=1e-9)
+    counts, off, dst, src = moe.permute_map(ids_ref, E)
+    assert np.array_equal(s["off"].cpu().numpy(), off)
+    assert np.array_equal(s["dst"].cpu().numpy(), dst)
+    P = int(off[E])
+    assert np.array_equal(s["src"].cpu().numpy()[:P], src[:P])
+    e_of = np.searchsorted(off, np.arange(P), side="right") - 1       # expert of each padded row
+    real = np.flatnonzero(src[:P] >= 0)
+
+    x_bits = workloads.bf16_bits(inp["x"])
+    W1b, W3b, W2b = (inp[n] for n in ("W1", "W3", "W2"))
+
+    # permuted, quantized x: sampled rows bit-exact
+    rows = np.sort(g.choice(real, 48, replace=False))
+    xr = mx.bf16_to_f64(x_bits[src[rows] // k])
+    q_ref, s_ref = mx.quantize_rows(xr)
+    assert_bytes_equal(_rows_u8(s["xq"], rows), q_ref, "xq rows")
+    xs_flat = u8(s["xs"])
+    assert_bytes_equal(_sampled_scales(xs_flat, rows, H), s_ref, "xs rows")
+
+    # GEMM1: a|b entries on the GPU's quantized x and the column-quantized W13 row
+    xhat = _deq_sampled(_rows_u8(s["xq"], rows), xs_flat, rows, H)                 # [48, H]
+    cols = g.choice(2 * F, 16, replace=False)
+    ab_rows = bits(s["ab"][torch.as_tensor(rows, device=dev)])                      # [48, 2F]
+    for c in cols:
+        ex = e_of[rows]
+        wcol = np.stack([mx.bf16_to_f64(workloads.bf16_bits(
+            (W1b if c < F else W3b)[e, :, c % F].contiguous())) for e in ex])         # [48, H]
+        wq, ws_ = mx.quantize_rows(wcol)                                               # blocks along H
+        terms = xhat * mx.dequantize_rows(wq, ws_)
+        assert_bf16_within_one_ulp(ab_rows[:, c], terms.sum(axis=1), f"a|b col {c}")
+
+    # fused SwiGLU -> h, quantized (teacher forced on the GPU's a, b)
+    abv = mx.bf16_to_f64(ab_rows)
+    h = moe.swiglu(abv[:, :F], abv[:, F:])
+    hs_flat = u8(s["hs"])
+    quant_mismatches_outside_margin(_rows_u8(s["hq"], rows), _sampled_scales(hs_flat, rows, F), h, "hq rows")
+
+    # GEMM2: y entries on the GPU's h and the column-quantized W2 row
+    hhat = _deq_sampled(_rows_u8(s["hq"], rows), hs_flat, rows, F)
+    y_rows = bits(s["y"][torch.as_tensor(rows, device=dev)])
+    for c in g.choice(H, 8, replace=False):
+        wcol = np.stack([mx.bf16_to_f64(workloads.bf16_bits(W2b[e, :, c].contiguous())) for e in e_of[rows]])
+        wq, ws_ = mx.quantize_rows(wcol)
+        assert_bf16_within_one_ulp(y_rows[:, c], (hhat * mx.dequantize_rows(wq, ws_)).sum(axis=1), f"y col {c}")
+
+    # combine (top-1): out[t] = bf16(fp32(gate * y[dst[t]])), exact
+    toks = g.choice(T, 64, replace=False)
+    yv = mx.bf16_to_f64(bits(s["y"][torch.as_tensor(dst[toks], device=dev)])).astype(np.float32)
+    want = mx.f32_to_bf16_bits((gate[toks, 0:1] * yv).astype(np.float32))
+    assert_bytes_equal(bits(s["out"][torch.as_tensor(toks, device=dev)]).view(np.uint8),
+                       want.view(np.uint8), "out")
+
+    # gradient shuffle: dY rows = bf16(fp32(gate * dOut)), quantized both ways, exact
+    dO_bits = workloads.bf16_bits(inp["dOut"])
+    tok = src[rows] // k
+    dY = mx.bf16_to_f64(mx.f32_to_bf16_bits((gate[tok, 0:1] * mx.bf16_to_f64(dO_bits[tok]).astype(np.float32))
+                                            .astype(np.float32)))
+    q_ref, s_ref = mx.quantize_rows(dY)
+    assert_bytes_equal(_rows_u8(s["dy_rq"], rows), q_ref, "dY row q")
+    dys_flat = u8(s["dy_rs"])
+    assert_bytes_equal(_sampled_scales(dys_flat, rows, H), s_ref, "dY row s")
+    # a column block of dY: 32 routed rows x one column
+    blk = int(g.choice(P // 32)) * 32
+    col = int(g.integers(H))
+    brows = np.arange(blk, blk + 32)
+    btok = src[brows]
+    colvals = np.zeros(32)
+    live = btok >= 0
+    colvals[live] = mx.bf16_to_f64(mx.f32_to_bf16_bits(
+        (gate[btok[live] // k, 0] * mx.bf16_to_f64(dO_bits[btok[live] // k, col]).astype(np.float32)).astype(np.float32)))
+    q_ref, s_ref = mx.quantize_blocks(colvals)
+    assert_bytes_equal(u8(s["dy_cq"][col, blk:blk + 32]), q_ref, "dY col block")
+    assert int(u8(s["dy_cs"])[mx.swizzled_offset(col, blk // 32, R // 32)]) == int(s_ref)
+
+    # dgrad2: dh entries on the GPU's dY and the row-quantized W2 row
+    dyhat = _deq_sampled(_rows_u8(s["dy_rq"], rows), dys_flat, rows, H)
+    dh_rows = s["dh"][torch.as_tensor(rows, device=dev)].cpu().numpy()
+    for f in g.choice(F, 8, replace=False):
+        wrow = np.stack([mx.bf16_to_f64(workloads.bf16_bits(W2b[e, f, :].contiguous())) for e in e_of[rows]])
+        wq, ws_ = mx.quantize_rows(wrow)
+        _dot_check(dh_rows[:, f], dyhat * mx.dequantize_rows(wq, ws_), f"dh col {f}")
+
+    # SwiGLU backward on the GPU's dh, a, b: row-quantized [da|db] (teacher forced)
+    da, db = moe.swiglu_bwd(dh_rows.astype(np.float64), abv[:, :F], abv[:, F:])
+    dab = np.concatenate([da, db], axis=1)
+    quant_mismatches_outside_margin(_rows_u8(s["dab_rq"], rows), _sampled_scales(u8(s["dab_rs"]), rows, 2 * F),
+                                    dab, "dab rows")
+
+    # wgrad2 / wgrad1 on the GPU's column-quantized operands, one expert:
+    # dW2[e, f, c] = sum over its tokens of h[t, f] dY[t, c];
+    # dW13[e, c, j] = sum over its tokens of xp[t, c] [da|db][t, j]
+    e = int(np.argmax(np.diff(off)))
+    lo, hi = int(off[e]), int(off[e + 1])
+    fs, cs, js = g.choice(F, 4, replace=False), g.choice(H, 4, replace=False), g.choice(2 * F, 4, replace=False)
+
+    def col_rows(qname, sname, which):
+        q = _rows_u8(s[qname], which)                                  # [n, R] transposed rows
+        return _deq_sampled(q, u8(s[sname]), which, R)[:, lo:hi]
+
+    hT, dyT = col_rows("h_cq", "h_cs", fs), col_rows("dy_cq", "dy_cs", cs)
+    got = s["dW2"][e][torch.as_tensor(fs, device=dev)][:, torch.as_tensor(cs, device=dev)].cpu().numpy()
+    _dot_check(got, hT[:, None, :] * dyT[None, :, :], f"dW2[{e}]")
+    xT, dabT = col_rows("xp_cq", "xp_cs", cs), col_rows("dab_cq", "dab_cs", js)
+    got = s["dW13"][e][torch.as_tensor(cs, device=dev)][:, torch.as_tensor(js, device=dev)].cpu().numpy()
+    _dot_check(got, xT[:, None, :] * dabT[None, :, :], f"dW13[{e}]")
+
+    # dgrad1: dxp entries on the GPU's row-quantized [da|db] and the row-quantized W13 row
+    dabhat = _deq_sampled(_rows_u8(s["dab_rq"], rows), u8(s["dab_rs"]), rows, 2 * F)
+    dxp_rows = bits(s["dxp"][torch.as_tensor(rows, device=dev)])
+    for c in g.choice(H, 4, replace=False):
+        wrow = np.stack([np.concatenate([mx.bf16_to_f64(workloads.bf16_bits(W1b[e_, c, :].contiguous())),
+                                         mx.bf16_to_f64(workloads.bf16_bits(W3b[e_, c, :].contiguous()))])
+                         for e_ in e_of[rows]])
+        wq, ws_ = mx.quantize_rows(wrow)
+        assert_bf16_within_one_ulp(dxp_rows[:, c], (dabhat * mx.dequantize_rows(wq, ws_)).sum(axis=1), f"dxp col {c}")
+
+    # combine of dX (unit gates, top-1): dX[t] = dxp[dst[t]] exactly
+    assert_bytes_equal(bits(s["dX"][torch.as_tensor(toks, device=dev)]).view(np.uint8),
+                       bits(s["dxp"][torch.as_tensor(dst[toks], device=dev)]).view(np.uint8), "dX")
