@@ -420,6 +420,17 @@ def _cpu_baseline(d_full, seconds_hint=20.0):
             "seconds": t}
 
 
+def _reduce_max(value: float, device) -> float:
+    """The slowest rank's value (replicas: the job's time is the max over
+    ranks); the value itself without an initialised process group."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def _dist():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -523,11 +534,7 @@ def main():
     barrier()
     clk = clocks.stop()
     elapsed = t0.elapsed_time(t1) * 1e-3
-    if world > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([elapsed], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        elapsed = float(tt.item())
+    elapsed = _reduce_max(elapsed, dev)
     assert int(step.b["status"].item()) == 0, "device status set during the timed steps"
 
     per = {n: [] for n in LayerStep.NAMES}
