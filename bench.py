@@ -567,7 +567,8 @@ def main():
 
     line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "fp8xfp8->f32 (MXFP8 E4M3, E8M0 scales)",
+            "vs_baseline": None, "dtype": "fp8",
+            "dtype_detail": "E4M3 x E4M3 block-scaled (E8M0, 32-element blocks) MMAs accumulating in fp32",
             "data": "synthetic (seeded, random-init weights)", "config": config,
             "gpu_launches": args.steps * sum(LayerStep.KERNELS) * 1,
             "clocks": clk,
