@@ -81,7 +81,19 @@ __global__ void __launch_bounds__(QT_THREADS, 6) k_quantize_bf16(QuantArgs a) {
   const int64_t cblocks = a.cols / 32, rblocks = a.rows / 32;
 
   // ---- phase 0: every load of this thread in flight at once ----
+  // (gather mode: all source indices first, then the rows and their gates,
+  // so phase 1 never waits on a dependent load)
   uint4 v[ITERS];
+  int32_t sidx[ITERS];
+  float gv[ITERS];
+  if (GATHER) {
+#pragma unroll
+    for (int it = 0; it < ITERS; ++it) {
+      const int c = it * QT_THREADS + tid;
+      const int64_t gr = row0 + (c >> 3), gc = col0 + (c & 7) * 8;
+      sidx[it] = (gr < a.rows && gc < a.cols) ? a.src[gr] : -1;
+    }
+  }
 #pragma unroll
   for (int it = 0; it < ITERS; ++it) {
     const int c = it * QT_THREADS + tid;
@@ -90,8 +102,11 @@ __global__ void __launch_bounds__(QT_THREADS, 6) k_quantize_bf16(QuantArgs a) {
     const bool valid = gr < a.rows && gc < a.cols;
     v[it] = make_uint4(0, 0, 0, 0);
     if (GATHER) {
-      const int32_t sidx = valid ? a.src[gr] : -1;
-      if (sidx >= 0) v[it] = __ldg(reinterpret_cast<const uint4 *>(a.x + (int64_t)(sidx / a.k) * a.cols + gc));
+      gv[it] = 1.0f;
+      if (sidx[it] >= 0) {
+        v[it] = __ldg(reinterpret_cast<const uint4 *>(a.x + (int64_t)(sidx[it] / a.k) * a.cols + gc));
+        if (a.gate) gv[it] = __ldg(a.gate + sidx[it]);
+      }
     } else if (valid) {
       v[it] = __ldg(reinterpret_cast<const uint4 *>(x + gr * a.cols + gc));
     }
@@ -106,9 +121,8 @@ __global__ void __launch_bounds__(QT_THREADS, 6) k_quantize_bf16(QuantArgs a) {
     const bool valid = gr < a.rows && gc < a.cols;
     uint4 w = v[it];
     if (GATHER && a.gate) {
-      const int32_t sidx = valid ? a.src[gr] : -1;
-      if (sidx >= 0) {
-        const float g = a.gate[sidx];
+      if (sidx[it] >= 0) {
+        const float g = gv[it];
         w.x = pack_bf16x2(g * bf16_lo(w.x), g * bf16_hi(w.x));
         w.y = pack_bf16x2(g * bf16_lo(w.y), g * bf16_hi(w.y));
         w.z = pack_bf16x2(g * bf16_lo(w.z), g * bf16_hi(w.z));
