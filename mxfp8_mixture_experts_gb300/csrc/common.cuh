@@ -80,6 +80,30 @@ __device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float
 
 __device__ __forceinline__ uint32_t abs_bits(float v) { return __float_as_uint(v) & 0x7fffffffu; }
 
+// Two-lane 16-bit integer max.  On bf16 pairs with the sign bits cleared
+// (& 0x7fff7fff) it is the per-half |x| maximum, NaN and Inf patterns above
+// every finite value, exactly as abs_bits on fp32.
+__device__ __forceinline__ uint32_t vmax_u16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// Four fp32 scaled by `inv` (an exact power of two: every product is exact
+// or an IEEE round-to-nearest result, as with scalar multiplies) in two packed
+// fp32x2 multiplies, then cast to E4M3 and packed, first element lowest.
+__device__ __forceinline__ uint32_t scale_pack_e4m3x4(float a, float b, float c, float d, float inv) {
+  uint64_t x, y, s2, r1, r2;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(a), "f"(b));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(y) : "f"(c), "f"(d));
+  asm("mov.b64 %0, {%1, %1};" : "=l"(s2) : "f"(inv));
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r1) : "l"(x), "l"(s2));
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r2) : "l"(y), "l"(s2));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r1));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(c), "=f"(d) : "l"(r2));
+  return pack_e4m3x4(a, b, c, d);
+}
+
 // bf16 helpers (storage as uint16)
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }

@@ -200,9 +200,12 @@ __global__ void __launch_bounds__(256) k_permute(PermuteArgs a) {
       const uint4 *xs = reinterpret_cast<const uint4 *>(a.x + t * a.H * 2);
       for (int64_t b = lane; b < nb; b += 32) {
         float f[32];
+        uint32_t am2 = 0;  // packed |bf16| maximum of the block
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           const uint4 v = __ldg(xs + b * 4 + q);
+          am2 = vmax_u16x2(am2, vmax_u16x2(vmax_u16x2(v.x & 0x7fff7fffu, v.y & 0x7fff7fffu),
+                                           vmax_u16x2(v.z & 0x7fff7fffu, v.w & 0x7fff7fffu)));
           f[8 * q + 0] = bf16_lo(v.x);
           f[8 * q + 1] = bf16_hi(v.x);
           f[8 * q + 2] = bf16_lo(v.y);
@@ -212,16 +215,11 @@ __global__ void __launch_bounds__(256) k_permute(PermuteArgs a) {
           f[8 * q + 6] = bf16_lo(v.w);
           f[8 * q + 7] = bf16_hi(v.w);
         }
-        uint32_t am = 0;
-#pragma unroll
-        for (int i = 0; i < 32; ++i) am = max(am, abs_bits(f[i]));
-        const MxScale s = mx_scale_from_amax_bits(am);
+        const MxScale s = mx_scale_from_amax_bits(max(am2 << 16, am2 & 0xffff0000u));
         uint32_t wd[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i)
-          wd[i] = s.bad ? 0x7f7f7f7fu
-                        : pack_e4m3x4(f[4 * i] * s.inv, f[4 * i + 1] * s.inv, f[4 * i + 2] * s.inv,
-                                      f[4 * i + 3] * s.inv);
+          wd[i] = s.bad ? 0x7f7f7f7fu : scale_pack_e4m3x4(f[4 * i], f[4 * i + 1], f[4 * i + 2], f[4 * i + 3], s.inv);
         for (int j = 0; j < a.k; ++j) {
           if (rows[j] < 0) continue;
           uint4 *o = reinterpret_cast<uint4 *>(a.out + (int64_t)rows[j] * a.H + b * 32);
