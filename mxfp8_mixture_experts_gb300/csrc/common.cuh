@@ -80,6 +80,22 @@ __device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float
 
 __device__ __forceinline__ uint32_t abs_bits(float v) { return __float_as_uint(v) & 0x7fffffffu; }
 
+// e^-a as 2^(-a log2 e) on the hardware's approximate base-2 exponential
+// (ex2.approx, a few ulp); rounding -a log2 e to fp32 adds about |a| 2^-24
+// relative.  +inf for a below about -88.7; 0 (flushed) for a above about 87.
+__device__ __forceinline__ float exp_neg_approx(float a) {
+  float e;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(a * -1.4426950408889634f));
+  return e;
+}
+
+// 1/x on the hardware's approximate reciprocal (rcp.approx, within 1 ulp).
+__device__ __forceinline__ float rcp_approx(float x) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+
 // Two-lane 16-bit integer max.  On bf16 pairs with the sign bits cleared
 // (& 0x7fff7fff) it is the per-half |x| maximum, NaN and Inf patterns above
 // every finite value, exactly as abs_bits on fp32.

@@ -212,7 +212,6 @@ constexpr int SB_VAL_STRIDE = SB_COLS + 1;            // fp32 staging row (padde
 constexpr int SB_Q_STRIDE = SB_ROWS + 16;             // transposed byte row (padded)
 constexpr int SB_SMEM = 3 * SB_ROWS * SB_VAL_STRIDE * 4 + 3 * SB_COLS * SB_Q_STRIDE + 3 * SB_COLS * 4;
 
-__device__ __forceinline__ float sigmoidf_(float a) { return 1.0f / (1.0f + expf(-a)); }
 
 __global__ void __launch_bounds__(SB_THREADS) k_swiglu_bwd(const float *__restrict__ dh, const uint16_t *__restrict__ ab,
                                                            int64_t rows, int64_t F, uint8_t *dab_rq, uint8_t *dab_rs,
@@ -253,9 +252,12 @@ __global__ void __launch_bounds__(SB_THREADS) k_swiglu_bwd(const float *__restri
     uint32_t ama = 0, amb = 0;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      const float s = sigmoidf_(A[i]);
+      // s = sigmoid(a) = 1 / (1 + e^-a) and 1 - s = e^-a s (no cancellation
+      // for large a); a is clamped at -87 so that e^-a stays finite
+      const float e = exp_neg_approx(fmaxf(A[i], -87.0f));
+      const float s = rcp_approx(1.0f + e);
       const float silu = A[i] * s;
-      da[i] = d[i] * B[i] * s * (1.0f + A[i] * (1.0f - s));
+      da[i] = d[i] * B[i] * s * (1.0f + A[i] * (e * s));
       db[i] = d[i] * silu;
       vals[(0 * SB_ROWS + r) * SB_VAL_STRIDE + ch * 8 + i] = da[i];
       vals[(1 * SB_ROWS + r) * SB_VAL_STRIDE + ch * 8 + i] = db[i];
