@@ -37,12 +37,6 @@ struct QuantArgs {
   int32_t swizzled;
 };
 
-__device__ __forceinline__ void store_scale(uint8_t *s, int64_t r, int64_t c, int64_t ncols_blocks, bool swz,
-                                            uint32_t v) {
-  int64_t off = swz ? sf_swizzle_offset(r, c, round_up(ncols_blocks, 4)) : r * ncols_blocks + c;
-  s[off] = (uint8_t)v;
-}
-
 // Quantize 32 values that one thread holds; writes 32 bytes to dst (16-B aligned).
 __device__ __forceinline__ uint32_t quant32_store(const float *v, uint8_t *dst) {
   uint32_t am = 0;
@@ -78,8 +72,15 @@ __global__ void __launch_bounds__(QT_THREADS, 6) k_quantize_bf16(QuantArgs a) {
   // keep the row-major reads and writes contiguous instead.
   const int64_t row0 = (int64_t)(ROW ? blockIdx.y : blockIdx.x) * QT_ROWS;
   const int64_t col0 = (int64_t)(ROW ? blockIdx.x : blockIdx.y) * QT_COLS;
-  const uint16_t *x = a.x + b * a.rows * a.cols;
-  const int64_t cblocks = a.cols / 32, rblocks = a.rows / 32;
+  // This thread's chunks: tile rows it * 32 + tr (it < ITERS), columns
+  // tc .. tc + 7.  64-bit bases once per CTA, 32-bit offsets inside the tile
+  // (the host bounds rows and cols so that they fit).
+  const int tr = tid >> 3, tc = (tid & 7) * 8;
+  const int64_t gc = col0 + tc;
+  const bool col_ok = gc < a.cols;
+  const uint32_t ucols = (uint32_t)a.cols;
+  const int64_t tile_off = (b * a.rows + row0) * a.cols + gc;  // element (row0 + tr, gc) minus tr rows
+  const uint32_t t_off = (uint32_t)tr * ucols;
 
   // ---- phase 0: every load of this thread in flight at once ----
   // (gather mode: all source indices first, then the rows and their gates,
@@ -90,36 +91,50 @@ __global__ void __launch_bounds__(QT_THREADS, 6) k_quantize_bf16(QuantArgs a) {
   if (GATHER) {
 #pragma unroll
     for (int it = 0; it < ITERS; ++it) {
-      const int c = it * QT_THREADS + tid;
-      const int64_t gr = row0 + (c >> 3), gc = col0 + (c & 7) * 8;
-      sidx[it] = (gr < a.rows && gc < a.cols) ? a.src[gr] : -1;
+      const int64_t gr = row0 + it * 32 + tr;
+      sidx[it] = (gr < a.rows && col_ok) ? a.src[gr] : -1;
     }
   }
 #pragma unroll
   for (int it = 0; it < ITERS; ++it) {
-    const int c = it * QT_THREADS + tid;
-    const int r = c >> 3, ch = c & 7;
-    const int64_t gr = row0 + r, gc = col0 + ch * 8;
-    const bool valid = gr < a.rows && gc < a.cols;
+    const bool valid = col_ok && row0 + it * 32 + tr < a.rows;
     v[it] = make_uint4(0, 0, 0, 0);
     if (GATHER) {
       gv[it] = 1.0f;
       if (sidx[it] >= 0) {
-        v[it] = __ldg(reinterpret_cast<const uint4 *>(a.x + (int64_t)(sidx[it] / a.k) * a.cols + gc));
+        const int32_t t = a.k == 1 ? sidx[it] : sidx[it] / a.k;
+        v[it] = __ldg(reinterpret_cast<const uint4 *>(a.x + (int64_t)t * a.cols + gc));
         if (a.gate) gv[it] = __ldg(a.gate + sidx[it]);
       }
     } else if (valid) {
-      v[it] = __ldg(reinterpret_cast<const uint4 *>(x + gr * a.cols + gc));
+      v[it] = __ldg(reinterpret_cast<const uint4 *>(a.x + tile_off + (t_off + (uint32_t)(it * 32) * ucols)));
+    }
+  }
+
+  // row-scale position of this thread's blocks: row r = row0 + it*32 + tr,
+  // block column c = gc / 32.  row0 is a multiple of 128 and col0 of 64, so
+  // in the swizzled layout r >> 7 = row0 >> 7, r & 31 = tr,
+  // (r & 127) >> 5 = it, c >> 2 = col0 >> 7 and c & 3 = ((col0 >> 5) & 3) +
+  // ((tid & 7) >> 2): the offset is a per-CTA base plus it * 4.
+  const int64_t cblocks = a.cols / 32;
+  int64_t rs_base = 0;
+  uint32_t rs_step = 0;
+  if (ROW) {
+    if (a.swizzled) {
+      rs_base = ((row0 >> 7) * (round_up(cblocks, 4) >> 2) + (col0 >> 7)) * 512 + tr * 16 + ((col0 >> 5) & 3) +
+                ((tid & 7) >> 2);
+      rs_step = 4;
+    } else {
+      rs_base = (row0 + tr) * cblocks + (gc >> 5);
+      rs_step = (uint32_t)(32 * cblocks);
     }
   }
 
   // ---- phase 1: ROW quant (a 32-element block = 4 consecutive lanes), stage ----
 #pragma unroll
   for (int it = 0; it < ITERS; ++it) {
-    const int c = it * QT_THREADS + tid;
-    const int r = c >> 3, ch = c & 7;
-    const int64_t gr = row0 + r, gc = col0 + ch * 8;
-    const bool valid = gr < a.rows && gc < a.cols;
+    const int r = it * 32 + tr;
+    const bool valid = col_ok && row0 + r < a.rows;
     uint4 w = v[it];
     if (GATHER && a.gate) {
       if (sidx[it] >= 0) {
@@ -130,7 +145,7 @@ __global__ void __launch_bounds__(QT_THREADS, 6) k_quantize_bf16(QuantArgs a) {
         w.w = pack_bf16x2(g * bf16_lo(w.w), g * bf16_hi(w.w));
       }
     }
-    if (COL) *reinterpret_cast<uint4 *>(&tile[r][ch * 8]) = w;
+    if (COL) *reinterpret_cast<uint4 *>(&tile[r][tc]) = w;
     if (ROW) {
       const float f[8] = {bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y),
                           bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w)};
@@ -145,8 +160,8 @@ __global__ void __launch_bounds__(QT_THREADS, 6) k_quantize_bf16(QuantArgs a) {
       o.x = s.bad ? 0x7f7f7f7fu : scale_pack_e4m3x4(f[0], f[1], f[2], f[3], s.inv);
       o.y = s.bad ? 0x7f7f7f7fu : scale_pack_e4m3x4(f[4], f[5], f[6], f[7], s.inv);
       if (valid) {
-        *reinterpret_cast<uint2 *>(a.q_row + b * a.rows * a.cols + gr * a.cols + gc) = o;
-        if ((ch & 3) == 0) store_scale(a.s_row + b * a.s_row_stride, gr, gc / 32, cblocks, a.swizzled, s.byte);
+        *reinterpret_cast<uint2 *>(a.q_row + tile_off + (t_off + (uint32_t)(it * 32) * ucols)) = o;
+        if ((tid & 3) == 0) a.s_row[b * a.s_row_stride + rs_base + it * rs_step] = (uint8_t)s.byte;
       }
     }
   }
@@ -176,21 +191,25 @@ __global__ void __launch_bounds__(QT_THREADS, 6) k_quantize_bf16(QuantArgs a) {
   __syncthreads();
 
   // ---- phase 3: full-line writes of the transposed output and its scales ----
-  const int64_t nrows_valid = min((int64_t)QT_ROWS, a.rows - row0);  // multiple of 32
-  uint8_t *qc = a.q_col + b * a.rows * a.cols;
+  const int nrows_valid = (int)min((int64_t)QT_ROWS, a.rows - row0);  // multiple of 32
+  uint8_t *qc = a.q_col + (b * a.cols + col0) * a.rows + row0;      // (col0, row0) of the COL output
+  const int part = tid & 7;                                         // 8 x 16 bytes per staged row
 #pragma unroll
   for (int it = 0; it < (QT_COLS * QT_ROWS / 16) / QT_THREADS; ++it) {
-    const int c = it * QT_THREADS + tid;
-    const int cc = c >> 3, part = c & 7;  // 8 x 16 bytes per staged row
-    const int64_t gc = col0 + cc;
-    if (gc < a.cols && part * 16 < nrows_valid)
-      *reinterpret_cast<uint4 *>(qc + gc * a.rows + row0 + part * 16) =
+    const int cc = it * (QT_THREADS / 8) + (tid >> 3);
+    if (col0 + cc < a.cols && part * 16 < nrows_valid)
+      *reinterpret_cast<uint4 *>(qc + (int64_t)cc * a.rows + part * 16) =
           *reinterpret_cast<const uint4 *>(&qcol[cc][part * 16]);
   }
   if (tid < QT_COLS && col0 + tid < a.cols) {
-    const int64_t gc = col0 + tid;
-    uint8_t *sc = a.s_col + b * a.s_col_stride;
-    for (int i = 0; i < (int)(nrows_valid / 32); ++i) store_scale(sc, gc, row0 / 32 + i, rblocks, a.swizzled, scol[tid][i]);
+    // column gc = col0 + tid, block rows row0/32 + i: row0 is a multiple of
+    // 128, so the (up to) four scale bytes are consecutive in both layouts
+    const int64_t gcs = col0 + tid, rblocks = a.rows / 32;
+    const int64_t off = a.swizzled ? ((gcs >> 7) * (round_up(rblocks, 4) >> 2) + (row0 >> 7)) * 512 +
+                                         (gcs & 31) * 16 + ((gcs & 127) >> 5) * 4
+                                   : gcs * rblocks + (row0 >> 5);
+    uint8_t *sc = a.s_col + b * a.s_col_stride + off;
+    for (int i = 0; i < nrows_valid / 32; ++i) sc[i] = scol[tid][i];
   }
 }
 
