@@ -246,22 +246,35 @@ __global__ void __launch_bounds__(SB_THREADS) k_swiglu_bwd(const float *__restri
   const int64_t twoF = 2 * F;
   const int64_t cb2 = twoF / 32;
 
+  // 512 chunks (128 rows x 4 chunks of 8): this thread's are tile rows
+  // it * 64 + rt, columns ch * 8 .. + 7.  64-bit bases once, 32-bit offsets
+  // inside the tile (the host bounds F).
+  const int rt = tid >> 2, ch = tid & 3;
+  const int64_t gf = f0 + ch * 8;
+  const uint32_t uF = (uint32_t)F, u2F = 2u * uF;
+  const float *dh_t = dh + row0 * F + gf;
+  const uint16_t *ab_t = ab + row0 * twoF + gf;
+  uint8_t *dab_t = dab_rq + row0 * twoF + gf;
   float4 d0[2], d1[2];
   uint4 av[2], bv[2];
 #pragma unroll
-  for (int it = 0; it < 2; ++it) {  // 512 chunks: 128 rows x 4 chunks of 8
-    const int c = it * SB_THREADS + tid;
-    const int64_t gr = row0 + (c >> 2), gf = f0 + (c & 3) * 8;
-    d0[it] = *reinterpret_cast<const float4 *>(dh + gr * F + gf);
-    d1[it] = *reinterpret_cast<const float4 *>(dh + gr * F + gf + 4);
-    av[it] = *reinterpret_cast<const uint4 *>(ab + gr * twoF + gf);
-    bv[it] = *reinterpret_cast<const uint4 *>(ab + gr * twoF + F + gf);
+  for (int it = 0; it < 2; ++it) {
+    const uint32_t r = (uint32_t)(it * 64 + rt);
+    d0[it] = *reinterpret_cast<const float4 *>(dh_t + r * uF);
+    d1[it] = *reinterpret_cast<const float4 *>(dh_t + r * uF + 4);
+    av[it] = *reinterpret_cast<const uint4 *>(ab_t + r * u2F);
+    bv[it] = *reinterpret_cast<const uint4 *>(ab_t + r * u2F + uF);
   }
+  // row-scale offsets (swizzled): r >> 7 = row0 >> 7, r & 31 = rt & 31,
+  // (r & 127) >> 5 = 2 * it + (rt >> 5); block column f0 / 32 for da and
+  // (F + f0) / 32 for db
+  const int64_t ca = f0 >> 5, cbk = (F + f0) >> 5, cp4 = round_up(cb2, 4);
+  const int64_t rs_row = (row0 >> 7) * (cp4 >> 2);
+  const int64_t rs_a = (rs_row + (ca >> 2)) * 512 + (rt & 31) * 16 + (rt >> 5) * 4 + (ca & 3);
+  const int64_t rs_b = (rs_row + (cbk >> 2)) * 512 + (rt & 31) * 16 + (rt >> 5) * 4 + (cbk & 3);
 #pragma unroll
   for (int it = 0; it < 2; ++it) {
-    const int c = it * SB_THREADS + tid;
-    const int r = c >> 2, ch = c & 3;
-    const int64_t gr = row0 + r, gf = f0 + ch * 8;
+    const int r = it * 64 + rt;
     const float d[8] = {d0[it].x, d0[it].y, d0[it].z, d0[it].w, d1[it].x, d1[it].y, d1[it].z, d1[it].w};
     const float A[8] = {bf16_lo(av[it].x), bf16_hi(av[it].x), bf16_lo(av[it].y), bf16_hi(av[it].y),
                         bf16_lo(av[it].z), bf16_hi(av[it].z), bf16_lo(av[it].w), bf16_hi(av[it].w)};
@@ -294,11 +307,11 @@ __global__ void __launch_bounds__(SB_THREADS) k_swiglu_bwd(const float *__restri
     oa.y = sa.bad ? 0x7f7f7f7fu : scale_pack_e4m3x4(da[4], da[5], da[6], da[7], sa.inv);
     ob.x = sbb.bad ? 0x7f7f7f7fu : scale_pack_e4m3x4(db[0], db[1], db[2], db[3], sbb.inv);
     ob.y = sbb.bad ? 0x7f7f7f7fu : scale_pack_e4m3x4(db[4], db[5], db[6], db[7], sbb.inv);
-    *reinterpret_cast<uint2 *>(dab_rq + gr * twoF + gf) = oa;
-    *reinterpret_cast<uint2 *>(dab_rq + gr * twoF + F + gf) = ob;
+    *reinterpret_cast<uint2 *>(dab_t + (uint32_t)r * u2F) = oa;
+    *reinterpret_cast<uint2 *>(dab_t + (uint32_t)r * u2F + uF) = ob;
     if (ch == 0) {
-      dab_rs[sf_swizzle_offset(gr, gf / 32, round_up(cb2, 4))] = (uint8_t)sa.byte;
-      dab_rs[sf_swizzle_offset(gr, (F + gf) / 32, round_up(cb2, 4))] = (uint8_t)sbb.byte;
+      dab_rs[rs_a + it * 8] = (uint8_t)sa.byte;
+      dab_rs[rs_b + it * 8] = (uint8_t)sbb.byte;
     }
   }
   __syncthreads();
