@@ -44,9 +44,9 @@ FP8_PER_BF16 = 2.0   # nominal dense fp8 / bf16 tensor rate (4.5 / 2.25 PFLOP/s)
 # the T=2048, E=2 step (1024 routed rows per expert, as in the full layer),
 # scaled by 8 to E=16 (profiles/layer_step_dram_T2048_E2.md).  Valid only for
 # the GEMM sources it was taken on; reported as null once they change.
-GEMM_TRAFFIC_BYTES_PER_STEP = 8 * 1734.179584e6
+GEMM_TRAFFIC_BYTES_PER_STEP = 8 * 1730.593e6
 GEMM_TRAFFIC_SOURCES = ("gemm_pair.cu", "gemm_shared.cuh", "common.cuh")
-GEMM_TRAFFIC_SHA256 = "3e3f5b513a4cb21c2a1ab5f487ac561d59b7af5b47bd1d328e311cbf9254f6d2"
+GEMM_TRAFFIC_SHA256 = "988050576863d72ef6d8b3f54656260085fd8f9c301bc87a4f10adc3b0ef0ced"
 
 
 def _gemm_sources_sha256():
