@@ -287,6 +287,34 @@ def _quant_bench(dev, iters=20):
     return {"GB/s": nbytes / t / 1e9, "us": t * 1e6, "bytes": nbytes, "l2": "flushed (256 MiB write) before each launch"}
 
 
+def _dequant_bench(dev, iters=20):
+    """MXFP8 dequantize of the quantize workload's ROW output (E4M3 [16384,
+    7168] + swizzled scales) to bf16, each launch timed after an L2 flush."""
+    import mxfp8_mixture_experts_gb300 as m
+    R, C = workloads.QUANTIZE_SHAPE
+    x = workloads.quantize_input(R, C, seed=0, device=dev)
+    q, sc, _, _ = m.mx_quantize(x, m.MX_MODE_ROW, m.MX_SCALE_SWIZZLED)
+    out = torch.empty((R, C), dtype=torch.bfloat16, device=dev)
+    L = m.lib()
+    s = torch.cuda.current_stream(dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    times = []
+    for i in range(iters + 3):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        code = L.mx_dequantize(q.data_ptr(), sc.data_ptr(), 1, R, C, 1, 0, out.data_ptr(), s.cuda_stream)
+        e1.record(s)
+        assert code == 0
+        torch.cuda.synchronize()
+        if i >= 3:
+            times.append(e0.elapsed_time(e1) * 1e-3)
+    t = statistics.median(times)
+    nbytes = R * C + R * C // 32 + 2 * R * C
+    return {"GB/s": nbytes / t / 1e9, "us": t * 1e6, "bytes": nbytes, "out": "bf16",
+            "l2": "flushed (256 MiB write) before each launch"}
+
+
 def _permute_bench(dev, iters=10):
     """Token permute / unpermute workload: T=32768 tokens, H=5120, E=16
     experts, top-4 Zipf(1.1) expert choice over 14 live experts (two empty).
@@ -449,9 +477,9 @@ def main():
     ap.add_argument("--no-quant", action="store_true", help="skip the quantize-kernel line of the layer run")
     ap.add_argument("--T", type=int, default=None, help="override the token count (profiling of small cases)")
     ap.add_argument("--E", type=int, default=None, help="override the expert count (profiling of small cases)")
-    ap.add_argument("--workload", default="layer", choices=["layer", "gemm", "quantize", "permute"],
-                    help="layer: the full training step (the bench line); gemm / quantize: one kernel family "
-                         "on its own workload, for profiling")
+    ap.add_argument("--workload", default="layer", choices=["layer", "gemm", "quantize", "dequantize", "permute"],
+                    help="layer: the full training step (the bench line); gemm / quantize / dequantize / "
+                         "permute: one kernel family on its own workload, for profiling")
     args = ap.parse_args()
     rank, world, local = _dist()
     if args.workload != "layer":
@@ -461,6 +489,8 @@ def main():
             r = _gemm_bench(dev, args)
         elif args.workload == "permute":
             r = _permute_bench(dev, max(args.steps, 1))
+        elif args.workload == "dequantize":
+            r = _dequant_bench(dev, max(args.steps, 1))
         else:
             r = _quant_bench(dev, max(args.steps, 1))
         print(json.dumps({"workload": args.workload, **r}))
@@ -555,7 +585,7 @@ def main():
     gemm_tflops = total_flops / gemm_time / 1e12
     hbm = _peak_val(peaks, "hbm_gbs") or FALLBACK["hbm_gbs"]
 
-    quant = perm = None
+    quant = perm = deq = None
     if not args.no_quant:
         quant = _quant_bench(dev)
         quant["frac"] = quant["GB/s"] / hbm
@@ -564,6 +594,8 @@ def main():
         perm = _permute_bench(dev)
         for key in ("permute", "unpermute"):
             perm[key]["frac"] = perm[key]["GB/s"] / hbm
+        deq = _dequant_bench(dev)
+        deq["frac"] = deq["GB/s"] / hbm
 
     line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
@@ -585,6 +617,7 @@ def main():
             "gemm_tflops": {n: round(gf[n] / avg[n] / 1e12, 1) for n in gf},
             "quantize": quant,
             "permute": perm,
+            "dequantize": deq,
             "routed_rows": routed}
 
     if not args.no_e2e:

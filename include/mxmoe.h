@@ -140,6 +140,26 @@ mx_status mx_quantize(const void *x, int64_t batch, int64_t rows, int64_t cols,
                       mx_stream stream);
 
 /* ------------------------------------------------------------------------ */
+/* MXFP8 dequantize  ([B] Stacked PRs: the mxfp8 dequantization kernel and   */
+/* the e8m0 -> fp32 scale decode; [C] section 6.3)                           */
+/* ------------------------------------------------------------------------ */
+/*
+ * q: E4M3 [batch, rows, cols] with scales s in `scale_layout` (per batch
+ * entry one scale array(rows, cols), as mx_quantize writes its ROW output; a
+ * COL output dequantizes the same way into the transposed matrix).  Every
+ * element becomes E4M3(q) * 2^(s - 127), the E8M0 decode of its block's
+ * scale byte:
+ *   MX_OUT_F32:  out fp32, exact (fp32 subnormals kept; overflow to +-Inf);
+ *   MX_OUT_BF16: out bf16, that exact value rounded to nearest even once.
+ * Scale byte 0xFF and the E4M3 NaN codes (0x7F, 0xFF) give NaN.
+ * out [batch, rows, cols].  cols % 32 == 0 (cols % 128 == 0 is not needed:
+ * the swizzled array's padding is not read); q and out 16-byte aligned.
+ */
+mx_status mx_dequantize(const uint8_t *q, const uint8_t *s, int64_t batch, int64_t rows,
+                        int64_t cols, int32_t scale_layout, int32_t out_dtype, void *out,
+                        mx_stream stream);
+
+/* ------------------------------------------------------------------------ */
 /* R: router (helper; the pages name no router -- top-k with softmax gate)   */
 /* ------------------------------------------------------------------------ */
 /*

@@ -20,7 +20,7 @@ from ._lib import (MX_GEMM_DGRAD, MX_GEMM_FWD, MX_GEMM_WGRAD, MX_MODE_BOTH, MX_M
                    MX_PERMUTE_FP8, MX_SCALE_PLAIN, MX_SCALE_SWIZZLED, MxError)
 
 __all__ = [
-    "lib", "MxError", "mx_quantize", "mx_scale_bytes", "moe_route", "moe_rows_cap", "moe_permute_map",
+    "lib", "MxError", "mx_quantize", "mx_dequantize", "mx_scale_bytes", "moe_route", "moe_rows_cap", "moe_permute_map",
     "moe_permute", "moe_unpermute", "mx_grouped_gemm", "moe_gemm1_swiglu", "moe_swiglu_bwd",
     "moe_gather_quant", "moe_gate_grad", "MoELayerDims", "moe_layer_prep_weights", "moe_layer_fwd",
     "moe_layer_bwd", "moe_layer_workspace_size", "moe_layer_weights_size",
@@ -74,6 +74,19 @@ def mx_quantize(x: torch.Tensor, mode: int = MX_MODE_ROW, scale_layout: int = MX
     _lib.check(lib().mx_quantize(_ptr(x), b, r, c, mode, scale_layout, _ptr(q_row), _ptr(s_row), _ptr(q_col),
                                  _ptr(s_col), _stream(dev)), "mx_quantize")
     return q_row, s_row, q_col, s_col
+
+
+def mx_dequantize(q: torch.Tensor, s: torch.Tensor, scale_layout: int = MX_SCALE_PLAIN,
+                  out_dtype: int = MX_OUT_F32):
+    """q uint8 [rows, cols] or [batch, rows, cols] with its scales -> fp32 or
+    bf16 of the same shape."""
+    _req(q, torch.uint8, "q")
+    batched = q.dim() == 3
+    b, r, c = (q.shape if batched else (1, *q.shape))
+    out = torch.empty(q.shape, dtype=torch.float32 if out_dtype == MX_OUT_F32 else torch.bfloat16, device=q.device)
+    _lib.check(lib().mx_dequantize(_ptr(q), _ptr(s), b, r, c, scale_layout, out_dtype, _ptr(out),
+                                   _stream(q.device)), "mx_dequantize")
+    return out
 
 
 def moe_route(logits: torch.Tensor, k: int):

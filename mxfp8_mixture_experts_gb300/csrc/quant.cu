@@ -367,6 +367,65 @@ __global__ void __launch_bounds__(SB_THREADS) k_swiglu_bwd(const float *__restri
   }
 }
 
+// ---------------------------------------------------------------------------
+// MXFP8 dequantize (see mx_dequantize in mxmoe.h).  HBM-bound: a CTA of
+// DQ_THREADS threads covers DQ_COLS columns of one row; a thread takes 16
+// consecutive E4M3 bytes (one 16-byte load; a warp reads 512 contiguous
+// bytes) and the scale byte of their 32-element block.  E4M3 -> f16 pairs
+// (exact: every E4M3 value is an f16 value), -> fp32, times 2^(s - 127) built
+// from the scale byte's bits: all exact in fp32.
+// ---------------------------------------------------------------------------
+constexpr int DQ_THREADS = 128;
+constexpr int DQ_COLS = DQ_THREADS * 16;
+
+__device__ __forceinline__ float2 e4m3x2_to_f32x2(uint32_t two_bytes) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((uint16_t)two_bytes));
+  return __half22float2(*reinterpret_cast<const __half2 *>(&h2));
+}
+
+// 2^(b - 127) for an E8M0 byte: fp32 exponent field b for b >= 1; 2^-127 is
+// the fp32 subnormal 0x00400000; 0xFF is NaN.
+__device__ __forceinline__ float e8m0_to_f32(uint32_t b) {
+  return __uint_as_float(b == 0xffu ? 0x7fc00000u : b == 0u ? 0x00400000u : b << 23);
+}
+
+template <bool F32>
+__global__ void __launch_bounds__(DQ_THREADS) k_dequantize(const uint8_t *__restrict__ q, const uint8_t *__restrict__ s,
+                                                           int64_t rows, int64_t cols, int64_t s_stride, int swizzled,
+                                                           void *out) {
+  const int64_t grow = blockIdx.x;  // row over all batch entries
+  const int64_t c0 = (int64_t)blockIdx.y * DQ_COLS + threadIdx.x * 16;
+  if (c0 >= cols) return;
+  const int64_t b = grow / rows, r = grow - b * rows;
+  const int64_t cblocks = cols / 32;
+  const int64_t c = c0 >> 5;
+  const int64_t soff = swizzled ? sf_swizzle_offset(r, c, round_up(cblocks, 4)) : r * cblocks + c;
+  const float sc = e8m0_to_f32(__ldg(s + b * s_stride + soff));
+  const uint4 w = __ldg(reinterpret_cast<const uint4 *>(q + grow * cols + c0));
+  const uint32_t wd[4] = {w.x, w.y, w.z, w.w};
+  float v[16];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 lo = e4m3x2_to_f32x2(wd[i] & 0xffffu), hi = e4m3x2_to_f32x2(wd[i] >> 16);
+    v[4 * i] = lo.x * sc;
+    v[4 * i + 1] = lo.y * sc;
+    v[4 * i + 2] = hi.x * sc;
+    v[4 * i + 3] = hi.y * sc;
+  }
+  if (F32) {
+    float4 *o = reinterpret_cast<float4 *>(static_cast<float *>(out) + grow * cols + c0);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) o[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+  } else {
+    uint4 *o = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(out) + grow * cols + c0);
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+      o[i] = make_uint4(pack_bf16x2(v[8 * i], v[8 * i + 1]), pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
+                        pack_bf16x2(v[8 * i + 4], v[8 * i + 5]), pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
+  }
+}
+
 }  // namespace mxmoe
 
 using namespace mxmoe;
@@ -421,6 +480,27 @@ extern "C" mx_status mx_quantize(const void *x, int64_t batch, int64_t rows, int
     k_quantize_bf16<true, false, false><<<grid, QT_THREADS, 0, stream>>>(a);
   else
     k_quantize_bf16<false, true, false><<<grid, QT_THREADS, 0, stream>>>(a);
+  return launch_status();
+}
+
+extern "C" mx_status mx_dequantize(const uint8_t *q, const uint8_t *s, int64_t batch, int64_t rows, int64_t cols,
+                                   int32_t scale_layout, int32_t out_dtype, void *out, mx_stream stream) {
+  MX_HOST_CHECK(q && s && out, MX_ERR_INVALID_ARG);
+  MX_HOST_CHECK(scale_layout == MX_SCALE_PLAIN || scale_layout == MX_SCALE_SWIZZLED, MX_ERR_INVALID_ARG);
+  MX_HOST_CHECK(out_dtype == MX_OUT_BF16 || out_dtype == MX_OUT_F32, MX_ERR_INVALID_ARG);
+  MX_HOST_CHECK(batch >= 1 && rows > 0 && cols > 0, MX_ERR_INVALID_ARG);
+  MX_HOST_CHECK(cols % 32 == 0, MX_ERR_SHAPE);
+  MX_HOST_CHECK(batch * rows < (int64_t)1 << 31 && (cols + DQ_COLS - 1) / DQ_COLS < 65535, MX_ERR_SHAPE);
+  MX_HOST_CHECK(aligned16(q) && aligned16(out), MX_ERR_ALIGNMENT);
+  mx_status st = check_device_cached();
+  if (st != MX_OK) return st;
+  const dim3 grid((unsigned)(batch * rows), (unsigned)((cols + DQ_COLS - 1) / DQ_COLS));
+  const int64_t s_stride = mx_scale_bytes(rows, cols, scale_layout);
+  const int swz = scale_layout == MX_SCALE_SWIZZLED;
+  if (out_dtype == MX_OUT_F32)
+    k_dequantize<true><<<grid, DQ_THREADS, 0, stream>>>(q, s, rows, cols, s_stride, swz, out);
+  else
+    k_dequantize<false><<<grid, DQ_THREADS, 0, stream>>>(q, s, rows, cols, s_stride, swz, out);
   return launch_status();
 }
 

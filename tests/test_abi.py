@@ -61,6 +61,11 @@ def test_host_side_argument_errors(lib):
     odd = C.c_void_p((1 << 20) + 4)
     # null input
     assert lib.mx_quantize(None, 1, 64, 64, 1, 0, fake, fake, None, None, None) == _lib.MX_ERR_INVALID_ARG
+    assert lib.mx_dequantize(None, fake, 1, 64, 64, 0, 1, fake, None) == _lib.MX_ERR_INVALID_ARG
+    assert lib.mx_dequantize(fake, fake, 1, 64, 64, 2, 1, fake, None) == _lib.MX_ERR_INVALID_ARG
+    assert lib.mx_dequantize(fake, fake, 1, 64, 64, 0, 5, fake, None) == _lib.MX_ERR_INVALID_ARG
+    assert lib.mx_dequantize(fake, fake, 1, 64, 48, 0, 1, fake, None) == _lib.MX_ERR_SHAPE
+    assert lib.mx_dequantize(C.c_void_p((1 << 20) + 8), fake, 1, 64, 64, 0, 1, fake, None) == _lib.MX_ERR_ALIGNMENT
     # unknown mode / layout
     assert lib.mx_quantize(fake, 1, 64, 64, 7, 0, fake, fake, None, None, None) == _lib.MX_ERR_INVALID_ARG
     assert lib.mx_quantize(fake, 1, 64, 64, 1, 5, fake, fake, None, None, None) == _lib.MX_ERR_INVALID_ARG
