@@ -369,14 +369,18 @@ __global__ void __launch_bounds__(SB_THREADS) k_swiglu_bwd(const float *__restri
 
 // ---------------------------------------------------------------------------
 // MXFP8 dequantize (see mx_dequantize in mxmoe.h).  HBM-bound: a CTA of
-// DQ_THREADS threads covers DQ_COLS columns of one row; a thread takes 16
-// consecutive E4M3 bytes (one 16-byte load; a warp reads 512 contiguous
-// bytes) and the scale byte of their 32-element block.  E4M3 -> f16 pairs
-// (exact: every E4M3 value is an f16 value), -> fp32, times 2^(s - 127) built
-// from the scale byte's bits: all exact in fp32.
+// DQ_THREADS threads covers DQ_COLS columns of one row; a thread takes
+// DQ_CHUNKS runs of 16 consecutive E4M3 bytes (16-byte loads, all issued
+// before any math; a warp's load reads 512 contiguous bytes) and the scale
+// byte of each run's 32-element block.  E4M3 -> f16 pairs (exact: every E4M3
+// value is an f16 value) -> fp32, times 2^(s - 127) built from the scale
+// byte's bits: all exact in fp32.  Each lane writes whole 32-byte sectors.
+// Four runs per thread and the 32-byte stores measured 18% (bf16) and 34%
+// (fp32) faster than one run with 16-byte stores.
 // ---------------------------------------------------------------------------
 constexpr int DQ_THREADS = 128;
-constexpr int DQ_COLS = DQ_THREADS * 16;
+constexpr int DQ_CHUNKS = 4;
+constexpr int DQ_COLS = DQ_THREADS * 16 * DQ_CHUNKS;
 
 __device__ __forceinline__ float2 e4m3x2_to_f32x2(uint32_t two_bytes) {
   uint32_t h2;
@@ -391,38 +395,76 @@ __device__ __forceinline__ float e8m0_to_f32(uint32_t b) {
 }
 
 template <bool F32>
+__device__ __forceinline__ void dq_store16(void *out, int64_t idx, const float (&v)[16]) {
+  // whole 32-byte sectors per lane when the output allows it
+  if (F32) {
+    float *o = static_cast<float *>(out) + idx;
+    if (((uintptr_t)o & 31) == 0) {
+#pragma unroll
+      for (int i = 0; i < 2; ++i)
+        asm volatile("st.global.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(o + 8 * i), "f"(v[8 * i]),
+                     "f"(v[8 * i + 1]), "f"(v[8 * i + 2]), "f"(v[8 * i + 3]), "f"(v[8 * i + 4]), "f"(v[8 * i + 5]),
+                     "f"(v[8 * i + 6]), "f"(v[8 * i + 7])
+                     : "memory");
+    } else {
+      float4 *o4 = reinterpret_cast<float4 *>(o);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) o4[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+    }
+  } else {
+    uint16_t *o = static_cast<uint16_t *>(out) + idx;
+    uint32_t w8[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) w8[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+    if (((uintptr_t)o & 31) == 0) {
+      asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(o), "r"(w8[0]), "r"(w8[1]),
+                   "r"(w8[2]), "r"(w8[3]), "r"(w8[4]), "r"(w8[5]), "r"(w8[6]), "r"(w8[7])
+                   : "memory");
+    } else {
+      uint4 *o4 = reinterpret_cast<uint4 *>(o);
+      o4[0] = make_uint4(w8[0], w8[1], w8[2], w8[3]);
+      o4[1] = make_uint4(w8[4], w8[5], w8[6], w8[7]);
+    }
+  }
+}
+
+template <bool F32>
 __global__ void __launch_bounds__(DQ_THREADS) k_dequantize(const uint8_t *__restrict__ q, const uint8_t *__restrict__ s,
                                                            int64_t rows, int64_t cols, int64_t s_stride, int swizzled,
                                                            void *out) {
   const int64_t grow = blockIdx.x;  // row over all batch entries
-  const int64_t c0 = (int64_t)blockIdx.y * DQ_COLS + threadIdx.x * 16;
-  if (c0 >= cols) return;
   const int64_t b = grow / rows, r = grow - b * rows;
   const int64_t cblocks = cols / 32;
-  const int64_t c = c0 >> 5;
-  const int64_t soff = swizzled ? sf_swizzle_offset(r, c, round_up(cblocks, 4)) : r * cblocks + c;
-  const float sc = e8m0_to_f32(__ldg(s + b * s_stride + soff));
-  const uint4 w = __ldg(reinterpret_cast<const uint4 *>(q + grow * cols + c0));
-  const uint32_t wd[4] = {w.x, w.y, w.z, w.w};
-  float v[16];
+  const uint8_t *sb = s + b * s_stride;
+  // DQ_CHUNKS chunks of 16 per thread, DQ_THREADS * 16 elements apart (each
+  // load instruction of a warp stays 512 contiguous bytes); loads first
+  uint4 w[DQ_CHUNKS];
+  uint32_t sbyte[DQ_CHUNKS];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float2 lo = e4m3x2_to_f32x2(wd[i] & 0xffffu), hi = e4m3x2_to_f32x2(wd[i] >> 16);
-    v[4 * i] = lo.x * sc;
-    v[4 * i + 1] = lo.y * sc;
-    v[4 * i + 2] = hi.x * sc;
-    v[4 * i + 3] = hi.y * sc;
+  for (int j = 0; j < DQ_CHUNKS; ++j) {
+    const int64_t c0 = (int64_t)blockIdx.y * DQ_COLS + j * (DQ_THREADS * 16) + threadIdx.x * 16;
+    if (c0 < cols) {
+      const int64_t c = c0 >> 5;
+      sbyte[j] = __ldg(sb + (swizzled ? sf_swizzle_offset(r, c, round_up(cblocks, 4)) : r * cblocks + c));
+      w[j] = __ldg(reinterpret_cast<const uint4 *>(q + grow * cols + c0));
+    }
   }
-  if (F32) {
-    float4 *o = reinterpret_cast<float4 *>(static_cast<float *>(out) + grow * cols + c0);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) o[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
-  } else {
-    uint4 *o = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(out) + grow * cols + c0);
+  for (int j = 0; j < DQ_CHUNKS; ++j) {
+    const int64_t c0 = (int64_t)blockIdx.y * DQ_COLS + j * (DQ_THREADS * 16) + threadIdx.x * 16;
+    if (c0 >= cols) continue;
+    const float sc = e8m0_to_f32(sbyte[j]);
+    const uint32_t wd[4] = {w[j].x, w[j].y, w[j].z, w[j].w};
+    float v[16];
 #pragma unroll
-    for (int i = 0; i < 2; ++i)
-      o[i] = make_uint4(pack_bf16x2(v[8 * i], v[8 * i + 1]), pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
-                        pack_bf16x2(v[8 * i + 4], v[8 * i + 5]), pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
+    for (int i = 0; i < 4; ++i) {
+      const float2 lo = e4m3x2_to_f32x2(wd[i] & 0xffffu), hi = e4m3x2_to_f32x2(wd[i] >> 16);
+      v[4 * i] = lo.x * sc;
+      v[4 * i + 1] = lo.y * sc;
+      v[4 * i + 2] = hi.x * sc;
+      v[4 * i + 3] = hi.y * sc;
+    }
+    dq_store16<F32>(out, grow * cols + c0, v);
   }
 }
 
