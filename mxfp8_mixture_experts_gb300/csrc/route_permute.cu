@@ -179,10 +179,17 @@ __global__ void __launch_bounds__(256) k_permute(PermuteArgs a) {
     for (int j = 0; j < a.k; ++j) rows[j] = a.dst[t * a.k + j];
     if (a.kind == MX_PERMUTE_FP8) {
       const uint4 *xs = reinterpret_cast<const uint4 *>(a.x + t * a.H);
-      for (int64_t c = lane; c < a.H / 16; c += 32) {
-        const uint4 v = __ldg(xs + c);
-        for (int j = 0; j < a.k; ++j)
-          if (rows[j] >= 0) reinterpret_cast<uint4 *>(a.out + (int64_t)rows[j] * a.H)[c] = v;
+      const int64_t nc = a.H / 16;
+      for (int64_t c0 = lane; c0 < nc; c0 += 32 * 4) {  // four 16-byte loads in flight per lane
+        uint4 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          if (c0 + 32 * u < nc) v[u] = __ldg(xs + c0 + 32 * u);
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          if (c0 + 32 * u < nc)
+            for (int j = 0; j < a.k; ++j)
+              if (rows[j] >= 0) reinterpret_cast<uint4 *>(a.out + (int64_t)rows[j] * a.H)[c0 + 32 * u] = v[u];
       }
       for (int64_t c = lane; c < nb; c += 32) {
         const uint8_t s = a.x_scales[t * nb + c];
@@ -222,9 +229,13 @@ __global__ void __launch_bounds__(256) k_permute(PermuteArgs a) {
           wd[i] = s.bad ? 0x7f7f7f7fu : scale_pack_e4m3x4(f[4 * i], f[4 * i + 1], f[4 * i + 2], f[4 * i + 3], s.inv);
         for (int j = 0; j < a.k; ++j) {
           if (rows[j] < 0) continue;
-          uint4 *o = reinterpret_cast<uint4 *>(a.out + (int64_t)rows[j] * a.H + b * 32);
-          o[0] = make_uint4(wd[0], wd[1], wd[2], wd[3]);
-          o[1] = make_uint4(wd[4], wd[5], wd[6], wd[7]);
+          uint8_t *o = a.out + (int64_t)rows[j] * a.H + b * 32;
+          if (((uintptr_t)o & 31) == 0) {  // a whole sector per lane
+            st_global_32B(o, wd[0], wd[1], wd[2], wd[3], wd[4], wd[5], wd[6], wd[7]);
+          } else {
+            reinterpret_cast<uint4 *>(o)[0] = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+            reinterpret_cast<uint4 *>(o)[1] = make_uint4(wd[4], wd[5], wd[6], wd[7]);
+          }
           a.out_scales[scale_off(a, rows[j], b)] = (uint8_t)s.byte;
         }
       }
@@ -243,37 +254,57 @@ __global__ void __launch_bounds__(256) k_permute(PermuteArgs a) {
 // ---------------------------------------------------------------------------
 // unpermute / combine: one warp per token, 8 bf16 per lane-step
 // ---------------------------------------------------------------------------
+// U chunks of 8 per lane with all their K row loads issued first (8 loads
+// in flight per lane for every k); the per-element arithmetic and its order
+// are the plain definition's.
+template <int K>
 __global__ void __launch_bounds__(256) k_unpermute(const uint16_t *__restrict__ y, const int32_t *__restrict__ dst,
-                                                   const float *__restrict__ gate, int64_t T, int64_t H, int k,
+                                                   const float *__restrict__ gate, int64_t T, int64_t H,
                                                    uint16_t *out) {
+  constexpr int U = K >= 8 ? 1 : 8 / K;
   const int lane = threadIdx.x & 31;
   const int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   if (t >= T) return;
-  int32_t rows[8];
-  float g[8];
-  for (int j = 0; j < k; ++j) {
-    rows[j] = dst[t * k + j];
-    g[j] = gate ? gate[t * k + j] : 1.0f;
-  }
-  for (int64_t c = lane; c < H / 8; c += 32) {
-    float acc[8];
-    for (int j = 0; j < k; ++j) {
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (rows[j] >= 0) v = __ldg(reinterpret_cast<const uint4 *>(y + (int64_t)rows[j] * H) + c);
-      const float f[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
-                          bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
+  int32_t rows[K];
+  float g[K];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float p = gate ? __fmul_rn(g[j], f[i]) : f[i];
-        acc[i] = (j == 0) ? p : __fadd_rn(acc[i], p);
+  for (int j = 0; j < K; ++j) {
+    rows[j] = dst[t * K + j];
+    g[j] = gate ? gate[t * K + j] : 1.0f;
+  }
+  const int64_t nc = H / 8;
+  for (int64_t c0 = lane; c0 < nc; c0 += 32 * U) {
+    uint4 v[U][K];
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+#pragma unroll
+      for (int j = 0; j < K; ++j) {
+        v[u][j] = make_uint4(0, 0, 0, 0);
+        if (c0 + 32 * u < nc && rows[j] >= 0)
+          v[u][j] = __ldg(reinterpret_cast<const uint4 *>(y + (int64_t)rows[j] * H) + c0 + 32 * u);
       }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      if (c0 + 32 * u >= nc) break;
+      float acc[8];
+#pragma unroll
+      for (int j = 0; j < K; ++j) {
+        const uint4 w = v[u][j];
+        const float f[8] = {bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y),
+                            bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w)};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float p = gate ? __fmul_rn(g[j], f[i]) : f[i];
+          acc[i] = (j == 0) ? p : __fadd_rn(acc[i], p);
+        }
+      }
+      uint4 o;
+      o.x = pack_bf16x2(acc[0], acc[1]);
+      o.y = pack_bf16x2(acc[2], acc[3]);
+      o.z = pack_bf16x2(acc[4], acc[5]);
+      o.w = pack_bf16x2(acc[6], acc[7]);
+      reinterpret_cast<uint4 *>(out + t * H)[c0 + 32 * u] = o;
     }
-    uint4 o;
-    o.x = pack_bf16x2(acc[0], acc[1]);
-    o.y = pack_bf16x2(acc[2], acc[3]);
-    o.z = pack_bf16x2(acc[4], acc[5]);
-    o.w = pack_bf16x2(acc[6], acc[7]);
-    reinterpret_cast<uint4 *>(out + t * H)[c] = o;
   }
 }
 
@@ -292,16 +323,27 @@ __global__ void __launch_bounds__(256) k_gate_grad(const uint16_t *__restrict__ 
   if (row >= 0) {
     const uint4 *a = reinterpret_cast<const uint4 *>(dOut + t * H);
     const uint4 *b = reinterpret_cast<const uint4 *>(y + (int64_t)row * H);
-    for (int64_t c = lane; c < H / 8; c += 32) {
-      const uint4 u = __ldg(a + c), v = __ldg(b + c);
-      acc = fmaf(bf16_lo(u.x), bf16_lo(v.x), acc);
-      acc = fmaf(bf16_hi(u.x), bf16_hi(v.x), acc);
-      acc = fmaf(bf16_lo(u.y), bf16_lo(v.y), acc);
-      acc = fmaf(bf16_hi(u.y), bf16_hi(v.y), acc);
-      acc = fmaf(bf16_lo(u.z), bf16_lo(v.z), acc);
-      acc = fmaf(bf16_hi(u.z), bf16_hi(v.z), acc);
-      acc = fmaf(bf16_lo(u.w), bf16_lo(v.w), acc);
-      acc = fmaf(bf16_hi(u.w), bf16_hi(v.w), acc);
+    const int64_t nc = H / 8;
+    for (int64_t c0 = lane; c0 < nc; c0 += 32 * 4) {  // four chunk pairs in flight per lane
+      uint4 u[4], v[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        if (c0 + 32 * q < nc) {
+          u[q] = __ldg(a + c0 + 32 * q);
+          v[q] = __ldg(b + c0 + 32 * q);
+        }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        if (c0 + 32 * q >= nc) break;
+        acc = fmaf(bf16_lo(u[q].x), bf16_lo(v[q].x), acc);
+        acc = fmaf(bf16_hi(u[q].x), bf16_hi(v[q].x), acc);
+        acc = fmaf(bf16_lo(u[q].y), bf16_lo(v[q].y), acc);
+        acc = fmaf(bf16_hi(u[q].y), bf16_hi(v[q].y), acc);
+        acc = fmaf(bf16_lo(u[q].z), bf16_lo(v[q].z), acc);
+        acc = fmaf(bf16_hi(u[q].z), bf16_hi(v[q].z), acc);
+        acc = fmaf(bf16_lo(u[q].w), bf16_lo(v[q].w), acc);
+        acc = fmaf(bf16_hi(u[q].w), bf16_hi(v[q].w), acc);
+      }
     }
   }
 #pragma unroll
@@ -450,8 +492,19 @@ extern "C" mx_status moe_unpermute(const void *y, const int32_t *dst, const floa
   mx_status st = check_device_cached();
   if (st != MX_OK) return st;
   if (T == 0) return MX_OK;
-  k_unpermute<<<(unsigned)((T + 7) / 8), 256, 0, stream>>>(static_cast<const uint16_t *>(y), dst, gate, T, H, k,
-                                                           static_cast<uint16_t *>(out));
+  const unsigned grid = (unsigned)((T + 7) / 8);
+  const uint16_t *yy = static_cast<const uint16_t *>(y);
+  uint16_t *oo = static_cast<uint16_t *>(out);
+  switch (k) {
+    case 1: k_unpermute<1><<<grid, 256, 0, stream>>>(yy, dst, gate, T, H, oo); break;
+    case 2: k_unpermute<2><<<grid, 256, 0, stream>>>(yy, dst, gate, T, H, oo); break;
+    case 3: k_unpermute<3><<<grid, 256, 0, stream>>>(yy, dst, gate, T, H, oo); break;
+    case 4: k_unpermute<4><<<grid, 256, 0, stream>>>(yy, dst, gate, T, H, oo); break;
+    case 5: k_unpermute<5><<<grid, 256, 0, stream>>>(yy, dst, gate, T, H, oo); break;
+    case 6: k_unpermute<6><<<grid, 256, 0, stream>>>(yy, dst, gate, T, H, oo); break;
+    case 7: k_unpermute<7><<<grid, 256, 0, stream>>>(yy, dst, gate, T, H, oo); break;
+    default: k_unpermute<8><<<grid, 256, 0, stream>>>(yy, dst, gate, T, H, oo); break;
+  }
   return launch_status();
 }
 
