@@ -191,10 +191,22 @@ __global__ void __launch_bounds__(256) k_permute(PermuteArgs a) {
             for (int j = 0; j < a.k; ++j)
               if (rows[j] >= 0) reinterpret_cast<uint4 *>(a.out + (int64_t)rows[j] * a.H)[c0 + 32 * u] = v[u];
       }
-      for (int64_t c = lane; c < nb; c += 32) {
-        const uint8_t s = a.x_scales[t * nb + c];
-        for (int j = 0; j < a.k; ++j)
-          if (rows[j] >= 0) a.out_scales[scale_off(a, rows[j], c)] = s;
+      // Scales: the blocks 4i .. 4i+3 of a row are 4 contiguous bytes in both
+      // layouts (plain: r * nb + c; swizzled: c & 3 is the lowest field), so
+      // a lane moves one 32-bit word when the arrays allow 4-byte access.
+      const uint8_t *xsc = a.x_scales + t * nb;
+      if (nb % 4 == 0 && ((uintptr_t)xsc & 3) == 0 && ((uintptr_t)a.out_scales & 3) == 0) {
+        for (int64_t c4 = lane; c4 < nb / 4; c4 += 32) {
+          const uint32_t w = *reinterpret_cast<const uint32_t *>(xsc + 4 * c4);
+          for (int j = 0; j < a.k; ++j)
+            if (rows[j] >= 0) *reinterpret_cast<uint32_t *>(a.out_scales + scale_off(a, rows[j], 4 * c4)) = w;
+        }
+      } else {
+        for (int64_t c = lane; c < nb; c += 32) {
+          const uint8_t sc = xsc[c];
+          for (int j = 0; j < a.k; ++j)
+            if (rows[j] >= 0) a.out_scales[scale_off(a, rows[j], c)] = sc;
+        }
       }
     } else if (a.kind == MX_PERMUTE_BF16) {
       const uint4 *xs = reinterpret_cast<const uint4 *>(a.x + t * a.H * 2);
@@ -205,6 +217,7 @@ __global__ void __launch_bounds__(256) k_permute(PermuteArgs a) {
       }
     } else {  // BF16_QUANT: quantize 32-element blocks while moving them
       const uint4 *xs = reinterpret_cast<const uint4 *>(a.x + t * a.H * 2);
+      const bool words = nb % 4 == 0 && ((uintptr_t)a.out_scales & 3) == 0;  // scales as 32-bit words
       for (int64_t b = lane; b < nb; b += 32) {
         float f[32];
         uint32_t am2 = 0;  // packed |bf16| maximum of the block
@@ -236,7 +249,19 @@ __global__ void __launch_bounds__(256) k_permute(PermuteArgs a) {
             reinterpret_cast<uint4 *>(o)[0] = make_uint4(wd[0], wd[1], wd[2], wd[3]);
             reinterpret_cast<uint4 *>(o)[1] = make_uint4(wd[4], wd[5], wd[6], wd[7]);
           }
-          a.out_scales[scale_off(a, rows[j], b)] = (uint8_t)s.byte;
+          if (!words) a.out_scales[scale_off(a, rows[j], b)] = (uint8_t)s.byte;
+        }
+        if (words) {
+          // lanes 4i .. 4i+3 hold blocks b .. b+3 (b % 4 == 0 for lane 4i):
+          // their scale bytes leave as one 32-bit word from lane 4i.  The
+          // four lanes of a group are active together (nb % 4 == 0).
+          const unsigned m = __activemask();
+          const uint32_t s1 = __shfl_down_sync(m, s.byte, 1, 4), s2 = __shfl_down_sync(m, s.byte, 2, 4),
+                         s3 = __shfl_down_sync(m, s.byte, 3, 4);
+          const uint32_t w = s.byte | (s1 << 8) | (s2 << 16) | (s3 << 24);
+          if ((lane & 3) == 0)
+            for (int j = 0; j < a.k; ++j)
+              if (rows[j] >= 0) *reinterpret_cast<uint32_t *>(a.out_scales + scale_off(a, rows[j], b)) = w;
         }
       }
     }
@@ -250,7 +275,6 @@ __global__ void __launch_bounds__(256) k_permute(PermuteArgs a) {
   if (a.kind != MX_PERMUTE_BF16)
     for (int64_t c = lane; c < nb; c += 32) a.out_scales[scale_off(a, r, c)] = 0;
 }
-
 // ---------------------------------------------------------------------------
 // unpermute / combine: one warp per token, 8 bf16 per lane-step
 // ---------------------------------------------------------------------------
