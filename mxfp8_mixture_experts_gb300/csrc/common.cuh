@@ -96,14 +96,6 @@ __device__ __forceinline__ float rcp_approx(float x) {
   return r;
 }
 
-// One 32-byte store (a whole sector per lane); p must be 32-byte aligned.
-__device__ __forceinline__ void st_global_32B(void *p, uint32_t w0, uint32_t w1, uint32_t w2, uint32_t w3,
-                                              uint32_t w4, uint32_t w5, uint32_t w6, uint32_t w7) {
-  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w0), "r"(w1), "r"(w2),
-               "r"(w3), "r"(w4), "r"(w5), "r"(w6), "r"(w7)
-               : "memory");
-}
-
 // Two-lane 16-bit integer max.  On bf16 pairs with the sign bits cleared
 // (& 0x7fff7fff) it is the per-half |x| maximum, NaN and Inf patterns above
 // every finite value, exactly as abs_bits on fp32.

@@ -152,6 +152,14 @@ __global__ void __launch_bounds__(MAP_CHUNK) k_map_assign(const int32_t *__restr
 // permute (scatter): one warp per token row, plus one warp per row of the
 // output that might be padding (it zeroes the row if src says so)
 // ---------------------------------------------------------------------------
+// One 32-byte store (a whole sector per lane); p must be 32-byte aligned.
+__device__ __forceinline__ void st_global_32B(void *p, uint32_t w0, uint32_t w1, uint32_t w2, uint32_t w3,
+                                              uint32_t w4, uint32_t w5, uint32_t w6, uint32_t w7) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w0), "r"(w1), "r"(w2),
+               "r"(w3), "r"(w4), "r"(w5), "r"(w6), "r"(w7)
+               : "memory");
+}
+
 struct PermuteArgs {
   int kind;
   const uint8_t *x;        // fp8 [T,H] or bf16 [T,H]
