@@ -80,7 +80,7 @@ class ClockSampler:
     """nvidia-smi clocks and throttle reasons sampled during the timed region."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,enforced.power.limit")
 
     def __init__(self, index: int):
         self.index = index
@@ -114,7 +114,7 @@ class ClockSampler:
             self.proc.wait(timeout=5)
         except Exception:
             self.proc.kill()
-        sm, smax, power, reasons = [], [], [], set()
+        sm, smax, power, limit, reasons = [], [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         timed = self.lines[self.first:] or self.lines
         for ln in timed:
@@ -130,11 +130,17 @@ class ClockSampler:
                 power.append(float(parts[3]))
             except ValueError:
                 pass
+            if len(parts) > 9:
+                try:
+                    limit.append(float(parts[9]))
+                except ValueError:
+                    pass
             for n, v in zip(names, parts[5:9]):
                 if v.lower() == "active":
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
-                "power_w": statistics.median(power) if power else None, "reasons": sorted(reasons),
+                "power_w": statistics.median(power) if power else None,
+                "power_limit_w": max(limit) if limit else None, "reasons": sorted(reasons),
                 "samples": len(sm), "interval_ms": 50}
 
 
