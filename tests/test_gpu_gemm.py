@@ -139,6 +139,35 @@ def test_wgrad_with_empty_group(dev, N, K):
         assert rel_frob(Ch[e], ref[e]) <= TOL
 
 
+def test_all_groups_empty(dev):
+    """offsets all zero: the row-grouped GEMM touches no output row (rows past
+    offsets[E] are never written) and wgrad writes exact zeros for every
+    expert; no device error either way."""
+    import mxfp8_mixture_experts_gb300 as m
+    g = np.random.default_rng(11)
+    E, M_cap, N, K = 3, 256, 256, 256
+    A = g.integers(0, 126, (M_cap, K), dtype=np.uint8)
+    B = g.integers(0, 126, (E, N, K), dtype=np.uint8)
+    As = mx.swizzle_scales(np.full((M_cap, K // 32), 127, np.uint8))
+    Bs = mx.swizzle_scales(np.full((E * N, K // 32), 127, np.uint8))
+    off = torch.zeros(E + 1, dtype=torch.int32, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    C = torch.full((M_cap, N), 7.0, device=dev)
+    m.mx_grouped_gemm(m.MX_GEMM_FWD, to_dev_u8(A, dev), to_dev_u8(As, dev), to_dev_u8(B, dev), to_dev_u8(Bs, dev),
+                      off, E, M_cap, N, K, m.MX_OUT_F32, out=C, dev_status=st)
+    X = g.integers(0, 126, (N, M_cap), dtype=np.uint8)
+    Y = g.integers(0, 126, (K, M_cap), dtype=np.uint8)
+    Xs = mx.swizzle_scales(np.full((N, M_cap // 32), 127, np.uint8))
+    Ys = mx.swizzle_scales(np.full((K, M_cap // 32), 127, np.uint8))
+    W = torch.full((E, N, K), 7.0, device=dev)
+    m.mx_grouped_gemm(m.MX_GEMM_WGRAD, to_dev_u8(X, dev), to_dev_u8(Xs, dev), to_dev_u8(Y, dev), to_dev_u8(Ys, dev),
+                      off, E, M_cap, N, K, m.MX_OUT_F32, out=W, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert torch.all(C == 7.0)
+    assert torch.all(W == 0.0)
+
+
 def test_bad_offsets_set_device_status(dev):
     import mxfp8_mixture_experts_gb300 as m
     A = torch.zeros((256, 128), dtype=torch.uint8, device=dev)
