@@ -231,6 +231,38 @@ def test_layer_end_to_end_vs_independent_oracle(dev):
         assert sqnr > 20, n
 
 
+def test_layer_with_empty_experts(dev):
+    """Experts 1, 4 and 5 of 6 receive no token (ids drawn from {0, 2, 3}),
+    gates U(0.5, 1): their weight gradients are exactly zero, and the layer
+    matches the independent MXFP8 oracle chain as in the end-to-end test."""
+    import mxfp8_mixture_experts_gb300 as m
+    dims = workloads.LayerDims(T=256, H=256, E=6, F=256, k=1)
+    d = m.MoELayerDims(T=dims.T, H=dims.H, F=dims.F, E=dims.E, k=dims.k)
+    inp = workloads.layer_inputs(dims, seed=4, device=dev)
+    g = np.random.default_rng(4)
+    ids_np = np.array([0, 2, 3], np.int32)[g.integers(0, 3, (dims.T, 1))]
+    gate_np = g.uniform(0.5, 1.0, (dims.T, 1)).astype(np.float32)
+    ids = torch.from_numpy(ids_np).to(dev)
+    gate = torch.from_numpy(gate_np).to(dev)
+    W13t = torch.cat([inp["W1"], inp["W3"]], dim=2).contiguous()
+    wq = m.moe_layer_prep_weights(W13t, inp["W2"])
+    ws = torch.empty(m.moe_layer_workspace_size(d), dtype=torch.uint8, device=dev)
+    out, _, _ = m.moe_layer_fwd(inp["x"], wq, d, ws, ids=ids, gate=gate)
+    dX, dW13, dW2, dg = m.moe_layer_bwd(inp["x"], inp["dOut"], gate, wq, d, ws)
+    torch.cuda.synchronize()
+    for e in (1, 4, 5):
+        assert torch.all(dW13[e] == 0) and torch.all(dW2[e] == 0), e
+    b = {n: bits(inp[n]) for n in ("x", "W1", "W3", "W2", "dOut")}
+    fq = moe.layer_forward(b["x"], b["W1"], b["W3"], b["W2"], ids_np, gate_np, quant=True)
+    bq = moe.layer_backward(fq, b["x"], b["W1"], b["W3"], b["W2"], b["dOut"])
+    got = {"out": out.float().cpu().numpy(), "dX": dX.float().cpu().numpy(),
+           "dW13": dW13.cpu().numpy()[[0, 2, 3]], "dW2": dW2.cpu().numpy()[[0, 2, 3]]}
+    ref = {"out": fq["out"], "dX": bq["dX"], "dW13": np.concatenate([bq["dW1"], bq["dW3"]], 2)[[0, 2, 3]],
+           "dW2": bq["dW2"][[0, 2, 3]]}
+    for n in got:
+        assert rel_frob(got[n], ref[n]) < 1e-2, n
+
+
 def test_bounded_wait_reports_timeout_and_context_survives():
     """The device failure path: a bounded wait on an mbarrier that nothing
     arrives on expires after 20 ms and reports MX_ERR_TIMEOUT; the context
