@@ -358,7 +358,9 @@ mx_status moe_gate_grad(const void *dOut, const void *y, const int32_t *dst,
 /* ------------------------------------------------------------------------ */
 /*
  * Dimensions: T tokens, H hidden, E experts, F FFN width, k experts per token.
- * H % 256 == 0, F % 256 == 0, T >= 1, 1 <= k <= min(E, 8), E <= 256.
+ * H % 256 == 0, F % 256 == 0, T >= 0, 1 <= k <= min(E, 8), E <= 256.  T = 0 (an
+ * empty batch) is valid: nothing is routed, the weight gradients are zero,
+ * and the token arrays may be NULL.
  *
  * Weights (bf16, device): W13 [E, H, 2F] = [W1 | W3] stacked along the last
  * dim; W2 [E, F, H].  moe_layer_prep_weights quantizes them into the four

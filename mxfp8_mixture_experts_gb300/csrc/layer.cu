@@ -106,7 +106,7 @@ static int64_t carve_ws(void *base, int64_t T, int64_t H, int64_t F, int32_t E, 
 }
 
 static mx_status check_dims(int64_t T, int64_t H, int64_t F, int32_t E, int32_t k) {
-  if (T < 1 || H < 1 || F < 1 || E < 1 || E > 256 || k < 1 || k > E || k > 8) return MX_ERR_INVALID_ARG;
+  if (T < 0 || H < 1 || F < 1 || E < 1 || E > 256 || k < 1 || k > E || k > 8) return MX_ERR_INVALID_ARG;
   if (H % 256 || F % 256) return MX_ERR_SHAPE;
   return MX_OK;
 }
@@ -151,7 +151,7 @@ extern "C" mx_status moe_layer_prep_weights(const void *W13, const void *W2, int
 extern "C" mx_status moe_layer_fwd(const void *x, const float *logits, int32_t *ids, float *gate, const void *wq,
                                    int64_t T, int64_t H, int64_t F, int32_t E, int32_t k, void *ws,
                                    int64_t ws_bytes, void *out, int32_t *dev_status, mx_stream stream) {
-  MX_HOST_CHECK(x && ids && wq && ws && out, MX_ERR_INVALID_ARG);
+  MX_HOST_CHECK(wq && ws && (T == 0 || (x && ids && out)), MX_ERR_INVALID_ARG);
   MX_HOST_CHECK(!logits || gate, MX_ERR_INVALID_ARG);
   MX_TRY(check_dims(T, H, F, E, k));
   MX_HOST_CHECK(ws_bytes >= moe_layer_workspace_size(T, H, F, E, k), MX_ERR_WORKSPACE);
@@ -176,7 +176,7 @@ extern "C" mx_status moe_layer_fwd(const void *x, const float *logits, int32_t *
 extern "C" mx_status moe_layer_bwd(const void *x, const void *dOut, const float *gate, const void *wq, int64_t T,
                                    int64_t H, int64_t F, int32_t E, int32_t k, void *ws, int64_t ws_bytes, void *dX,
                                    float *dW13, float *dW2, float *d_gate, int32_t *dev_status, mx_stream stream) {
-  MX_HOST_CHECK(x && dOut && wq && ws && dX && dW13 && dW2, MX_ERR_INVALID_ARG);
+  MX_HOST_CHECK(wq && ws && dW13 && dW2 && (T == 0 || (x && dOut && dX)), MX_ERR_INVALID_ARG);
   MX_TRY(check_dims(T, H, F, E, k));
   MX_HOST_CHECK(ws_bytes >= moe_layer_workspace_size(T, H, F, E, k), MX_ERR_WORKSPACE);
   WeightsView v;

@@ -549,7 +549,7 @@ extern "C" mx_status mx_dequantize(const uint8_t *q, const uint8_t *s, int64_t b
 extern "C" mx_status moe_gather_quant(const void *x, const float *gate, const int32_t *src, int64_t T, int64_t H,
                                       int32_t k, int64_t rows_cap, int32_t mode, uint8_t *q_row, uint8_t *s_row,
                                       uint8_t *q_col, uint8_t *s_col, mx_stream stream) {
-  MX_HOST_CHECK(x && src, MX_ERR_INVALID_ARG);
+  MX_HOST_CHECK(src && (T == 0 || x), MX_ERR_INVALID_ARG);  // T = 0: every row is a zero pad row
   MX_HOST_CHECK(mode == MX_MODE_ROW || mode == MX_MODE_COL || mode == MX_MODE_BOTH, MX_ERR_INVALID_ARG);
   MX_HOST_CHECK(T >= 0 && H > 0 && k >= 1 && rows_cap >= 0, MX_ERR_INVALID_ARG);
   const bool row = mode & MX_MODE_ROW, col = mode & MX_MODE_COL;

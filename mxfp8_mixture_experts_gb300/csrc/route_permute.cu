@@ -389,7 +389,7 @@ using namespace mxmoe;
 
 extern "C" mx_status moe_route(const float *logits, int64_t T, int32_t E, int32_t k, int32_t *ids, float *gate,
                                mx_stream stream) {
-  MX_HOST_CHECK(logits && ids && gate, MX_ERR_INVALID_ARG);
+  MX_HOST_CHECK(T == 0 || (logits && ids && gate), MX_ERR_INVALID_ARG);  // T = 0: nothing to read or write
   MX_HOST_CHECK(T >= 0 && E >= 1 && E <= MAP_MAX_E && k >= 1 && k <= E && k <= 8, MX_ERR_INVALID_ARG);
   mx_status st = check_device_cached();
   if (st != MX_OK) return st;
@@ -412,7 +412,7 @@ extern "C" int64_t moe_permute_map_workspace_size(int64_t T, int32_t k, int32_t 
 extern "C" mx_status moe_permute_map(const int32_t *ids, int64_t T, int32_t k, int32_t E, int64_t rows_cap,
                                      int32_t *counts, int32_t *offsets, int32_t *dst, int32_t *src, void *workspace,
                                      int64_t workspace_bytes, int32_t *dev_status, mx_stream stream) {
-  MX_HOST_CHECK(ids && counts && offsets && dst && src, MX_ERR_INVALID_ARG);
+  MX_HOST_CHECK(counts && offsets && src && (T == 0 || (ids && dst)), MX_ERR_INVALID_ARG);
   MX_HOST_CHECK(T >= 0 && k >= 1 && k <= 8 && E >= 1 && E <= MAP_MAX_E, MX_ERR_INVALID_ARG);
   MX_HOST_CHECK(rows_cap >= moe_rows_cap(T, k, E), MX_ERR_SHAPE);
   const int64_t need = moe_permute_map_workspace_size(T, k, E);
@@ -461,7 +461,7 @@ mx_status noalloc_scratch(int32_t **out) {
 extern "C" mx_status moe_permute_map_noalloc(const int32_t *ids, int64_t T, int32_t k, int32_t E, int64_t rows_cap,
                                              int32_t *counts, int32_t *offsets, int32_t *dst, int32_t *src,
                                              int32_t *dev_status, mx_stream stream) {
-  MX_HOST_CHECK(ids && counts && offsets && dst && src, MX_ERR_INVALID_ARG);
+  MX_HOST_CHECK(counts && offsets && src && (T == 0 || (ids && dst)), MX_ERR_INVALID_ARG);
   MX_HOST_CHECK(T >= 0 && k >= 1 && k <= 8 && E >= 1 && E <= MAP_MAX_E, MX_ERR_INVALID_ARG);
   MX_HOST_CHECK(rows_cap >= moe_rows_cap(T, k, E), MX_ERR_SHAPE);
   MX_HOST_CHECK(moe_permute_map_workspace_size(T, k, E) <= (int64_t)MOE_NOALLOC_SCRATCH_BYTES, MX_ERR_SCRATCH_LIMIT);
@@ -485,9 +485,10 @@ extern "C" mx_status moe_permute(int32_t kind, const void *x, const uint8_t *x_s
                                  uint8_t *out_scales, int32_t scale_layout, mx_stream stream) {
   MX_HOST_CHECK(kind == MX_PERMUTE_FP8 || kind == MX_PERMUTE_BF16 || kind == MX_PERMUTE_BF16_QUANT,
                 MX_ERR_INVALID_ARG);
-  MX_HOST_CHECK(x && dst && src && out, MX_ERR_INVALID_ARG);
+  // T = 0: no token rows (x, x_scales, dst may be NULL); the pad rows are still zeroed
+  MX_HOST_CHECK(src && out && (T == 0 || (x && dst)), MX_ERR_INVALID_ARG);
   MX_HOST_CHECK(kind == MX_PERMUTE_BF16 || (out_scales != nullptr), MX_ERR_INVALID_ARG);
-  MX_HOST_CHECK(kind != MX_PERMUTE_FP8 || x_scales != nullptr, MX_ERR_INVALID_ARG);
+  MX_HOST_CHECK(kind != MX_PERMUTE_FP8 || T == 0 || x_scales != nullptr, MX_ERR_INVALID_ARG);
   MX_HOST_CHECK(scale_layout == MX_SCALE_PLAIN || scale_layout == MX_SCALE_SWIZZLED, MX_ERR_INVALID_ARG);
   MX_HOST_CHECK(T >= 0 && H > 0 && k >= 1 && k <= 8 && rows_cap >= 0, MX_ERR_INVALID_ARG);
   MX_HOST_CHECK(H % 32 == 0, MX_ERR_SHAPE);
@@ -517,7 +518,7 @@ extern "C" mx_status moe_permute(int32_t kind, const void *x, const uint8_t *x_s
 
 extern "C" mx_status moe_unpermute(const void *y, const int32_t *dst, const float *gate, int64_t T, int64_t H,
                                    int32_t k, void *out, mx_stream stream) {
-  MX_HOST_CHECK(y && dst && out, MX_ERR_INVALID_ARG);
+  MX_HOST_CHECK(T == 0 || (y && dst && out), MX_ERR_INVALID_ARG);
   MX_HOST_CHECK(T >= 0 && H > 0 && k >= 1 && k <= 8, MX_ERR_INVALID_ARG);
   MX_HOST_CHECK(H % 8 == 0, MX_ERR_SHAPE);
   MX_HOST_CHECK(aligned16(y) && aligned16(out), MX_ERR_ALIGNMENT);
@@ -542,7 +543,7 @@ extern "C" mx_status moe_unpermute(const void *y, const int32_t *dst, const floa
 
 extern "C" mx_status moe_gate_grad(const void *dOut, const void *y, const int32_t *dst, int64_t T, int64_t H,
                                    int32_t k, float *d_gate, mx_stream stream) {
-  MX_HOST_CHECK(dOut && y && dst && d_gate, MX_ERR_INVALID_ARG);
+  MX_HOST_CHECK(T == 0 || (dOut && y && dst && d_gate), MX_ERR_INVALID_ARG);
   MX_HOST_CHECK(T >= 0 && H > 0 && k >= 1 && k <= 8, MX_ERR_INVALID_ARG);
   MX_HOST_CHECK(H % 8 == 0, MX_ERR_SHAPE);
   MX_HOST_CHECK(aligned16(dOut) && aligned16(y), MX_ERR_ALIGNMENT);

@@ -62,6 +62,11 @@ def test_host_side_argument_errors(lib):
     # null input
     assert lib.mx_quantize(None, 1, 64, 64, 1, 0, fake, fake, None, None, None) == _lib.MX_ERR_INVALID_ARG
     assert lib.mx_dequantize(None, fake, 1, 64, 64, 0, 1, fake, None) == _lib.MX_ERR_INVALID_ARG
+    # T = 0: the token arrays may be NULL (the argument checks pass; without a
+    # GPU the device check then fails)
+    assert lib.moe_route(None, 0, 4, 1, None, None, None) != _lib.MX_ERR_INVALID_ARG
+    assert lib.moe_route(None, 5, 4, 1, None, None, None) == _lib.MX_ERR_INVALID_ARG
+    assert lib.moe_unpermute(None, None, None, 0, 64, 1, None, None) != _lib.MX_ERR_INVALID_ARG
     assert lib.mx_dequantize(fake, fake, 1, 64, 64, 2, 1, fake, None) == _lib.MX_ERR_INVALID_ARG
     assert lib.mx_dequantize(fake, fake, 1, 64, 64, 0, 5, fake, None) == _lib.MX_ERR_INVALID_ARG
     assert lib.mx_dequantize(fake, fake, 1, 64, 48, 0, 1, fake, None) == _lib.MX_ERR_SHAPE

@@ -263,6 +263,26 @@ def test_layer_with_empty_experts(dev):
         assert rel_frob(got[n], ref[n]) < 1e-2, n
 
 
+def test_layer_empty_batch(dev):
+    """T = 0 through moe_layer_fwd/bwd: no error, zero weight gradients."""
+    import mxfp8_mixture_experts_gb300 as m
+    dims = workloads.LayerDims(T=0, H=256, E=4, F=256, k=1)
+    d = m.MoELayerDims(T=0, H=dims.H, F=dims.F, E=dims.E, k=dims.k)
+    g = workloads.generator(2, dev)
+    W13 = workloads.randn_bf16((dims.E, dims.H, 2 * dims.F), 0.02, g, dev)
+    W2 = workloads.randn_bf16((dims.E, dims.F, dims.H), 0.02, g, dev)
+    wq = m.moe_layer_prep_weights(W13, W2)
+    ws = torch.empty(m.moe_layer_workspace_size(d), dtype=torch.uint8, device=dev)
+    x = torch.empty((0, dims.H), dtype=torch.bfloat16, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    out, ids, gate = m.moe_layer_fwd(x, wq, d, ws, logits=torch.empty((0, dims.E), device=dev), dev_status=st)
+    dX, dW13, dW2, dg = m.moe_layer_bwd(x, x, gate, wq, d, ws, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert out.shape == (0, dims.H) and dX.shape == (0, dims.H)
+    assert bool(torch.all(dW13 == 0)) and bool(torch.all(dW2 == 0))
+
+
 def test_bounded_wait_reports_timeout_and_context_survives():
     """The device failure path: a bounded wait on an mbarrier that nothing
     arrives on expires after 20 ms and reports MX_ERR_TIMEOUT; the context

@@ -195,3 +195,26 @@ def test_gate_grad(dev):
     # fp32 accumulation of H = 1024 products: |err| <= ~H * 2^-24 * sum|terms|
     bound = 1024 * 2.0 ** -24 * np.stack([np.sum(np.abs(dv * yv[rows[:, j]]), axis=1) for j in range(k)], axis=1)
     assert np.all(np.abs(dg.cpu().numpy() - ref) <= bound)
+
+
+def test_empty_batch(dev):
+    """T = 0 through the token-indexed entry points: no error; the map marks
+    every row a pad row, the permute and gather outputs are zero rows with
+    zero scales, and the combine and gate gradient have nothing to do."""
+    import mxfp8_mixture_experts_gb300 as m
+    E, k, H = 4, 2, 256
+    ids, gate = m.moe_route(torch.empty((0, E), device=dev), k)
+    assert ids.shape == (0, k) and gate.shape == (0, k)
+    counts, off, dst, src = m.moe_permute_map(ids, E)
+    x = torch.empty((0, H), dtype=torch.bfloat16, device=dev)
+    out, out_s = m.moe_permute(m.MX_PERMUTE_BF16_QUANT, x, dst, src, k, scale_layout=m.MX_SCALE_SWIZZLED)
+    qr, sr, qc, sc = m.moe_gather_quant(x, gate, src, k, m.MX_MODE_BOTH)
+    y = torch.zeros((src.numel(), H), dtype=torch.bfloat16, device=dev)
+    comb = m.moe_unpermute(y, dst, gate, 0, k)
+    dg = m.moe_gate_grad(x, y, dst, k)
+    torch.cuda.synchronize()
+    assert int(counts.sum()) == 0 and off.cpu().tolist() == [0] * (E + 1)
+    assert src.numel() == m.moe_rows_cap(0, k, E) and bool(torch.all(src == -1))
+    for t in (out, out_s, qr, sr, qc, sc):
+        assert bool(torch.all(t == 0))
+    assert comb.shape == (0, H) and dg.shape == (0, k)
