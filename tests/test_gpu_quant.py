@@ -51,6 +51,15 @@ def test_quantize_matches_oracle(dev, shape, mode, layout):
     _check(x, mode, layout)
 
 
+@pytest.mark.parametrize("shape", [(1, 64), (100, 96), (257, 160), (130, 7168)])
+@pytest.mark.parametrize("layout", [0, 1])
+def test_quantize_rows_ragged(dev, shape, layout):
+    """ROW mode needs cols % 32 == 0 only: row counts off every tile and
+    block boundary (the swizzled array's padding stays zero)."""
+    x = workloads.quantize_input(*shape, seed=sum(shape), device=dev)
+    _check(x, 1, layout)
+
+
 @pytest.mark.parametrize("layout", [0, 1])
 def test_quantize_batched(dev, layout):
     g = workloads.generator(3, dev)
