@@ -263,6 +263,28 @@ def test_layer_with_empty_experts(dev):
         assert rel_frob(got[n], ref[n]) < 1e-2, n
 
 
+@pytest.mark.parametrize("rows,F", [(128, 96), (384, 32), (256, 160)])
+def test_swiglu_bwd_standalone(dev, rows, F):
+    """moe_swiglu_bwd on widths the layer never uses (F a multiple of 32 but
+    not of 256) with N(0,1) a, b and dh: [da|db] and h quantized both ways
+    against the fp64 SwiGLU backward of the same bf16 a, b and fp32 dh
+    (margin rule at E4M3 rounding boundaries)."""
+    import mxfp8_mixture_experts_gb300 as m
+    g = workloads.generator(rows + F, dev)
+    ab = workloads.randn_bf16((rows, 2 * F), 1.0, g, dev)
+    dh = torch.randn((rows, F), generator=g, device=dev)
+    dab_rq, dab_rs, dab_cq, dab_cs, h_cq, h_cs = m.moe_swiglu_bwd(dh, ab)
+    torch.cuda.synchronize()
+    abv = mx.bf16_to_f64(bits(ab))
+    da, db = moe.swiglu_bwd(dh.cpu().numpy().astype(np.float64), abv[:, :F], abv[:, F:])
+    dab = np.concatenate([da, db], axis=1)
+    h = moe.swiglu(abv[:, :F], abv[:, F:])
+    quant_mismatches_outside_margin(u8(dab_rq), mx.unswizzle_scales(u8(dab_rs), rows, 2 * F // 32), dab, "dab rows")
+    quant_mismatches_outside_margin(u8(dab_cq), mx.unswizzle_scales(u8(dab_cs), 2 * F, rows // 32), dab.T.copy(),
+                                    "dab cols")
+    quant_mismatches_outside_margin(u8(h_cq), mx.unswizzle_scales(u8(h_cs), F, rows // 32), h.T.copy(), "h cols")
+
+
 def test_layer_empty_batch(dev):
     """T = 0 through moe_layer_fwd/bwd: no error, zero weight gradients."""
     import mxfp8_mixture_experts_gb300 as m
