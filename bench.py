@@ -494,6 +494,7 @@ def main():
     ap.add_argument("--no-quant", action="store_true", help="skip the quantize-kernel line of the layer run")
     ap.add_argument("--T", type=int, default=None, help="override the token count (profiling of small cases)")
     ap.add_argument("--E", type=int, default=None, help="override the expert count (profiling of small cases)")
+    ap.add_argument("--k", type=int, default=None, help="override top-k (a variant; the bench line is top-1)")
     ap.add_argument("--workload", default="layer", choices=["layer", "gemm", "quantize", "dequantize", "permute"],
                     help="layer: the full training step (the bench line); gemm / quantize / dequantize / "
                          "permute: one kernel family on its own workload, for profiling")
@@ -514,8 +515,8 @@ def main():
         return
 
     dims = workloads.FULL_LAYER
-    if args.T or args.E:
-        dims = workloads.LayerDims(T=args.T or dims.T, H=dims.H, E=args.E or dims.E, F=dims.F, k=dims.k)
+    if args.T or args.E or args.k:
+        dims = workloads.LayerDims(T=args.T or dims.T, H=dims.H, E=args.E or dims.E, F=dims.F, k=args.k or dims.k)
     config = {"workload": f"full MoE SwiGLU layer fwd+bwd: T={dims.T} tokens, H={dims.H}, E={dims.E} experts, "
                           f"F={dims.F}, top-{dims.k} softmax router on N(0,1) logits, MXFP8 on all expert GEMMs",
               "T": dims.T, "H": dims.H, "E": dims.E, "F": dims.F, "k": dims.k,
