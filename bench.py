@@ -39,14 +39,14 @@ FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1
 FP8_PER_BF16 = 2.0   # nominal dense fp8 / bf16 tensor rate (4.5 / 2.25 PFLOP/s)
 
 
-# DRAM traffic of the six grouped-GEMM launches of one full-layer step: the
-# per-launch dram__bytes_read.sum + dram__bytes_write.sum of an ncu capture of
-# the T=2048, E=2 step (1024 routed rows per expert, as in the full layer),
-# scaled by 8 to E=16 (profiles/layer_step_dram_T2048_E2.md).  Valid only for
-# the GEMM sources it was taken on; reported as null once they change.
-GEMM_TRAFFIC_BYTES_PER_STEP = 8 * 1730.593e6
+# DRAM traffic of the six grouped-GEMM launches of one full-layer step
+# (dram__bytes_read.sum + dram__bytes_write.sum per launch, summed), from an
+# ncu capture of those launches alone.  Valid only for the GEMM sources it was
+# taken on (checked by hash); reported as null otherwise.
+GEMM_TRAFFIC_BYTES_PER_STEP = None
+GEMM_TRAFFIC_HOW = None
 GEMM_TRAFFIC_SOURCES = ("gemm_pair.cu", "gemm_shared.cuh", "common.cuh")
-GEMM_TRAFFIC_SHA256 = "988050576863d72ef6d8b3f54656260085fd8f9c301bc87a4f10adc3b0ef0ced"
+GEMM_TRAFFIC_SHA256 = None
 
 
 def _gemm_sources_sha256():
@@ -168,8 +168,13 @@ class LayerStep:
         b["w13_cq"], b["w13_cs"] = u8(E * 2 * F * H), u8(sb(E * 2 * F, H))
         b["w2_rq"], b["w2_rs"] = u8(E * F * H), u8(sb(E * F, H))
         b["w2_cq"], b["w2_cs"] = u8(E * H * F), u8(sb(E * H, F))
-        b["ids"] = torch.empty((T, k), dtype=torch.int32, device=dev)
-        b["gate"] = torch.empty((T, k), dtype=torch.float32, device=dev)
+        self.routed = inp.get("logits") is not None
+        if self.routed:
+            b["ids"] = torch.empty((T, k), dtype=torch.int32, device=dev)
+            b["gate"] = torch.empty((T, k), dtype=torch.float32, device=dev)
+        else:  # ids and gates given (no router launch)
+            b["ids"] = inp["ids"].to(dev, torch.int32).contiguous()
+            b["gate"] = inp["gate"].to(dev, torch.float32).contiguous()
         b["counts"] = torch.empty(E, dtype=torch.int32, device=dev)
         b["off"] = torch.empty(E + 1, dtype=torch.int32, device=dev)
         b["dst"] = torch.empty(T * k, dtype=torch.int32, device=dev)
@@ -207,7 +212,7 @@ class LayerStep:
         s = stream.cuda_stream
         x = self.inp["x"].data_ptr()
         dOut = self.inp["dOut"].data_ptr()
-        logits = self.inp["logits"].data_ptr()
+        logits = self.inp["logits"].data_ptr() if self.routed else None
         st = p["status"]
         ev = events
 
@@ -224,7 +229,9 @@ class LayerStep:
         mark()
         chk(L.mx_quantize(self.W13.data_ptr(), E, H, 2 * F, 3, 1, p["w13_rq"], p["w13_rs"], p["w13_cq"], p["w13_cs"], s), "q W13"); mark()
         chk(L.mx_quantize(self.W2.data_ptr(), E, F, H, 3, 1, p["w2_rq"], p["w2_rs"], p["w2_cq"], p["w2_cs"], s), "q W2"); mark()
-        chk(L.moe_route(logits, T, E, k, p["ids"], p["gate"], s), "route"); mark()
+        if self.routed:
+            chk(L.moe_route(logits, T, E, k, p["ids"], p["gate"], s), "route")
+        mark()
         chk(L.moe_permute_map(p["ids"], T, k, E, R, p["counts"], p["off"], p["dst"], p["src"], p["map_ws"],
                               self.map_ws_bytes, st, s), "map"); mark()
         chk(L.moe_permute(2, x, None, T, H, k, p["dst"], p["src"], R, p["xq"], p["xs"], 1, s), "permute"); mark()
@@ -234,17 +241,19 @@ class LayerStep:
             "gemm2"); mark()
         chk(L.moe_unpermute(p["y"], p["dst"], p["gate"], T, H, k, p["out"], s), "combine"); mark()
         chk(L.moe_gate_grad(dOut, p["y"], p["dst"], T, H, k, p["d_gate"], s), "gate grad"); mark()
+        lim = p["off"] + 4 * E  # offsets[E]: the routed rows end there
         chk(L.moe_gather_quant(dOut, p["gate"], p["src"], T, H, k, R, 3, p["dy_rq"], p["dy_rs"], p["dy_cq"],
-                               p["dy_cs"], s), "dY quant"); mark()
+                               p["dy_cs"], lim, s), "dY quant"); mark()
         chk(L.mx_grouped_gemm(1, p["dy_rq"], p["dy_rs"], p["w2_rq"], p["w2_rs"], p["off"], E, R, F, H, p["dh"], 1, st,
                               s), "dgrad2"); mark()
         chk(L.moe_swiglu_bwd(p["dh"], p["ab"], R, F, p["dab_rq"], p["dab_rs"], p["dab_cq"], p["dab_cs"], p["h_cq"],
-                             p["h_cs"], s), "swiglu bwd"); mark()
+                             p["h_cs"], lim, s), "swiglu bwd"); mark()
         chk(L.mx_grouped_gemm(2, p["h_cq"], p["h_cs"], p["dy_cq"], p["dy_cs"], p["off"], E, R, F, H, p["dW2"], 1, st,
                               s), "wgrad2"); mark()
         chk(L.mx_grouped_gemm(1, p["dab_rq"], p["dab_rs"], p["w13_rq"], p["w13_rs"], p["off"], E, R, H, 2 * F,
                               p["dxp"], 0, st, s), "dgrad1"); mark()
-        chk(L.moe_gather_quant(x, None, p["src"], T, H, k, R, 2, None, None, p["xp_cq"], p["xp_cs"], s), "x col quant"); mark()
+        chk(L.moe_gather_quant(x, None, p["src"], T, H, k, R, 2, None, None, p["xp_cq"], p["xp_cs"], lim, s),
+            "x col quant"); mark()
         chk(L.mx_grouped_gemm(2, p["xp_cq"], p["xp_cs"], p["dab_cq"], p["dab_cs"], p["off"], E, R, H, 2 * F,
                               p["dW13"], 1, st, s), "wgrad1"); mark()
         chk(L.moe_unpermute(p["dxp"], p["dst"], None, T, H, k, p["dX"], s), "combine dX"); mark()
@@ -432,7 +441,114 @@ def _gemm_bench(dev, args):
         res[name] = {"TFLOP/s": flops / t / 1e12, "us": t * 1e6}
     res["sizes"] = sizes
     res["flops_per_op"] = flops
+    res["workload"] = (f"grouped GEMM: E={E}, {M} routed rows in Zipf(1.1) groups {sizes}, K={K}, N={N}; fwd and "
+                       f"dgrad bf16 out, wgrad fp32 out")
+    res["l2"] = "flushed (256 MiB write) before each launch"
     return res
+
+
+def _tiny_layer_bench(dev, iters=20):
+    """Tiny MoE layer workload (T=512, H=256, E=4, F=512, top-1 ids uniform
+    over experts, gate 1): one fwd+bwd step of the same launches as the full
+    layer (no router: the ids are given), each step timed with CUDA events
+    after an L2 flush.  Launch- and latency-bound at this size."""
+    import mxfp8_mixture_experts_gb300 as m
+    dims = workloads.TINY_LAYER
+    d = m.MoELayerDims(T=dims.T, H=dims.H, F=dims.F, E=dims.E, k=dims.k)
+    inp = workloads.layer_inputs(dims, seed=0, device=dev, router="uniform")
+    step = LayerStep(d, inp, dev)
+    s = torch.cuda.current_stream(dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    times = []
+    for i in range(iters + 3):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        step.run(s)
+        e1.record(s)
+        torch.cuda.synchronize()
+        if i >= 3:
+            times.append(e0.elapsed_time(e1) * 1e-3)
+    assert int(step.b["status"].item()) == 0
+    t = statistics.median(times)
+    flops = sum(_gemm_flops(d, dims.T * dims.k).values())
+    return {"us_per_step": t * 1e6, "TFLOP/s": flops / t / 1e12, "flops": flops,
+            "workload": f"tiny MoE layer fwd+bwd: T={dims.T}, H={dims.H}, E={dims.E}, F={dims.F}, top-1 ids "
+                        f"uniform, gate 1", "launches": sum(LayerStep.KERNELS) - 1,
+            "l2": "flushed (256 MiB write) before each step"}
+
+
+def _bf16_layer_bench(dev, d, inp, steps, warmup):
+    """Context for the pages' MoE-layer speedup claim: the same layer step
+    (T, H, E, F, top-k from the same logits and inputs) in bf16 with plain
+    PyTorch eager ops -- torch.mm per expert (cuBLAS bf16 GEMMs, fp32
+    accumulation, bf16 outputs including the weight gradients), torch
+    elementwise SwiGLU, index-based permute and combine.  Not part of the
+    library; timed with CUDA events over the same number of steps."""
+    T, H, F, E, k = d.T, d.H, d.F, d.E, d.k
+    W13 = torch.cat([inp["W1"], inp["W3"]], dim=2).contiguous()       # [E, H, 2F]
+    W2 = inp["W2"]                                                      # [E, F, H]
+    x, dOut, logits = inp["x"], inp["dOut"], inp["logits"]
+    dW13 = torch.empty_like(W13)
+    dW2 = torch.empty_like(W2)
+
+    def step():
+        top = logits.topk(k, dim=1)
+        ids = top.indices
+        gate = torch.softmax(logits, dim=1).gather(1, ids)
+        flat = ids.reshape(-1)
+        order = torch.argsort(flat, stable=True)
+        counts = torch.bincount(flat, minlength=E).tolist()
+        tok = order // k
+        xp = x.index_select(0, tok)
+        g = gate.reshape(-1).index_select(0, order).to(torch.bfloat16).unsqueeze(1)
+        dY = dOut.index_select(0, tok) * g
+        out = torch.zeros_like(x)
+        dX = torch.zeros_like(x)
+        start = 0
+        ys, dxps = [], []
+        for e in range(E):
+            n = counts[e]
+            if n == 0:
+                dW13[e].zero_()
+                dW2[e].zero_()
+                continue
+            sl = slice(start, start + n)
+            start += n
+            ab = xp[sl] @ W13[e]
+            a, b = ab[:, :F], ab[:, F:]
+            sa = torch.sigmoid(a.float())
+            h = (a.float() * sa * b.float()).to(torch.bfloat16)
+            y = h @ W2[e]
+            ys.append(y)
+            dh = (dY[sl] @ W2[e].t()).float()
+            dW2[e] = h.t() @ dY[sl]
+            da = dh * b.float() * sa * (1 + a.float() * (1 - sa))
+            db = dh * a.float() * sa
+            dab = torch.cat([da, db], dim=1).to(torch.bfloat16)
+            dxps.append(dab @ W13[e].t())
+            dW13[e] = xp[sl].t() @ dab
+        y = torch.cat(ys)
+        out.index_add_(0, tok, y * g)
+        dX.index_add_(0, tok, torch.cat(dxps))
+        return out, dX
+
+    s = torch.cuda.current_stream(dev)
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    for _ in range(steps):
+        step()
+    e1.record(s)
+    torch.cuda.synchronize()
+    t = e0.elapsed_time(e1) * 1e-3 / steps
+    flops = sum(_gemm_flops(d, T * k).values())
+    return {"ms_per_step": t * 1e3, "TFLOP/s": flops / t / 1e12,
+            "what": "bf16 layer in plain PyTorch eager: torch.mm per expert (cuBLAS bf16, fp32 accumulation, bf16 "
+                    "outputs incl. weight gradients), elementwise SwiGLU in fp32, index-based permute/combine; "
+                    "context only, not part of the library"}
 
 
 def _cpu_baseline(d_full, seconds_hint=20.0):
@@ -465,6 +581,23 @@ def _cpu_baseline(d_full, seconds_hint=20.0):
             "seconds": t}
 
 
+def _fp8_peaks(peaks, clk):
+    """Dense fp8 tensor peaks (2 x the measured cuBLAS bf16 rates, the nominal
+    fp8/bf16 ratio) and the one this run is held to: the burst figure when
+    the clock record of the timed region shows the SM clock at its maximum
+    with no power cap, the sustained (power-capped) figure otherwise."""
+    burst = (_peak_val(peaks, "bf16_tflops") or FALLBACK["bf16_tflops"]) * FP8_PER_BF16
+    sust = (_peak_val(peaks, "bf16_tflops_sustained") or FALLBACK["bf16_tflops_sustained"]) * FP8_PER_BF16
+    sm, smax = clk.get("sm_mhz"), clk.get("sm_max_mhz")
+    capped = "sw_power_cap" in clk.get("reasons", [])
+    at_max = sm is not None and smax and sm >= 0.97 * smax
+    kind = "burst" if at_max and not capped else "sustained"
+    return {"burst": burst, "sustained": sust, "kind": kind,
+            "chosen": burst if kind == "burst" else sust, "other": sust if kind == "burst" else burst,
+            "rule": "burst when the timed region's median SM clock is >= 97% of max and no sw_power_cap sample; "
+                    "sustained otherwise"}
+
+
 def _reduce_max(value: float, device) -> float:
     """The slowest rank's value (replicas: the job's time is the max over
     ranks); the value itself without an initialised process group."""
@@ -491,7 +624,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--no-quant", action="store_true", help="skip the quantize-kernel line of the layer run")
+    ap.add_argument("--no-quant", action="store_true",
+                    help="skip the per-workload kernel lines (quantize, permute, dequantize, grouped GEMM, tiny layer)")
+    ap.add_argument("--no-bf16", action="store_true", help="skip the bf16 PyTorch layer timing (context)")
     ap.add_argument("--T", type=int, default=None, help="override the token count (profiling of small cases)")
     ap.add_argument("--E", type=int, default=None, help="override the expert count (profiling of small cases)")
     ap.add_argument("--k", type=int, default=None, help="override top-k (a variant; the bench line is top-1)")
@@ -598,13 +733,12 @@ def main():
     value = world * total_flops * args.steps / elapsed / 1e12
 
     peaks, src = _peaks()
-    bf16 = _peak_val(peaks, "bf16_tflops_sustained", "bf16_tflops") or FALLBACK["bf16_tflops_sustained"]
-    fp8_peak = bf16 * FP8_PER_BF16
+    hbm = _peak_val(peaks, "hbm_gbs") or FALLBACK["hbm_gbs"]
+    pk = _fp8_peaks(peaks, clk)
     gemm_time = sum(avg[n] for n in gf)
     gemm_tflops = total_flops / gemm_time / 1e12
-    hbm = _peak_val(peaks, "hbm_gbs") or FALLBACK["hbm_gbs"]
 
-    quant = perm = deq = None
+    quant = perm = deq = gemm = tiny = bf16 = None
     if not args.no_quant:
         quant = _quant_bench(dev)
         quant["frac"] = quant["GB/s"] / hbm
@@ -615,28 +749,46 @@ def main():
             perm[key]["frac"] = perm[key]["GB/s"] / hbm
         deq = _dequant_bench(dev)
         deq["frac"] = deq["GB/s"] / hbm
+        gemm = _gemm_bench(dev, args)
+        for op in ("fwd", "dgrad", "wgrad"):
+            gemm[op]["frac_burst"] = gemm[op]["TFLOP/s"] / pk["burst"]
+        gemm["peak"] = pk["burst"]
+        gemm["peak_source"] = f"{src} bf16_tflops (burst: each launch timed alone) x {FP8_PER_BF16}"
+        tiny = _tiny_layer_bench(dev)
+    if not args.no_bf16:
+        bf16 = _bf16_layer_bench(dev, d, inp, steps=min(args.steps, 10), warmup=2)
+        bf16["mxfp8_speedup"] = bf16["ms_per_step"] / ms
 
+    traffic = GEMM_TRAFFIC_BYTES_PER_STEP if GEMM_TRAFFIC_SHA256 == _gemm_sources_sha256() else None
     line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "fp8",
             "dtype_detail": "E4M3 x E4M3 block-scaled (E8M0, 32-element blocks) MMAs accumulating in fp32",
             "data": "synthetic (seeded, random-init weights)", "config": config,
-            "gpu_launches": args.steps * sum(LayerStep.KERNELS) * 1,
+            "gpu_launches": args.steps * (sum(LayerStep.KERNELS) - (0 if step.routed else 1)),
             "clocks": clk,
             "roofline": {"bound": "tensor", "kernel": "k_grouped_gemm_pair (6 launches per step)",
-                         "achieved": gemm_tflops, "peak": fp8_peak, "unit": "TFLOP/s", "frac": gemm_tflops / fp8_peak,
-                         "traffic": GEMM_TRAFFIC_BYTES_PER_STEP if _gemm_sources_sha256() == GEMM_TRAFFIC_SHA256
-                         else None,
-                         "traffic_unit": "DRAM bytes per step of the 6 GEMM launches (ncu, scaled from T=2048, E=2)",
+                         "achieved": gemm_tflops, "peak": pk["chosen"], "unit": "TFLOP/s",
+                         "frac": gemm_tflops / pk["chosen"], "peak_kind": pk["kind"],
+                         "peak_other": pk["other"], "frac_vs_other": gemm_tflops / pk["other"],
+                         "peak_rule": pk["rule"],
+                         "traffic": traffic,
+                         "traffic_unit": "DRAM bytes per step of the 6 GEMM launches",
+                         "traffic_how": GEMM_TRAFFIC_HOW if traffic is not None else
+                         "null: no ncu capture of the current GEMM sources",
                          "algorithmic_bytes": _gemm_alg_bytes(d, R=routed),
-                         "peak_source": f"{src} bf16_tflops_sustained {bf16} x {FP8_PER_BF16} (nominal dense "
-                                        f"fp8/bf16 ratio)"},
+                         "peak_source": f"{src} bf16_tflops / bf16_tflops_sustained x {FP8_PER_BF16} (nominal "
+                                        f"dense fp8/bf16 ratio)"},
             "value_excl_weight_prep": total_flops / (ms * 1e-3 - avg['quantize W13'] - avg['quantize W2']) / 1e12,
             "kernels_ms": {n: round(v * 1e3, 4) for n, v in avg.items()},
             "gemm_tflops": {n: round(gf[n] / avg[n] / 1e12, 1) for n in gf},
+            "gemm_frac": {n: round(gf[n] / avg[n] / 1e12 / pk["chosen"], 3) for n in gf},
             "quantize": quant,
             "permute": perm,
             "dequantize": deq,
+            "grouped_gemm": gemm,
+            "tiny_layer": tiny,
+            "bf16_layer_context": bf16,
             "routed_rows": routed}
 
     if not args.no_e2e:
@@ -654,10 +806,12 @@ def _e2e(m, d, dims, inp, dev, args, world):
     """The same step through the layer entry points (moe_layer_prep_weights,
     moe_layer_fwd, moe_layer_bwd), with every step's inputs (x, logits, dOut)
     copied in from pinned host memory and its results (out, dX, d_gate) read
-    back to pinned host memory inside the timed region.  The copies run on a
-    second stream into double-buffered device tensors, so step i+1's inputs
-    and step i-1's results move while step i computes; the timed region ends
-    when the last result has reached the host."""
+    back to pinned host memory inside the timed region.  Host-to-device and
+    device-to-host copies run on two streams of their own (the two directions
+    overlap each other and the compute) into double-buffered device tensors:
+    step i+1's inputs and step i-1's results move while step i computes.  The
+    timed region ends when the last result has reached the host.  The weight
+    gradients stay on the device (an optimizer would consume them there)."""
     W13 = torch.cat([inp["W1"], inp["W3"]], dim=2).contiguous()
     W2 = inp["W2"]
     wq = torch.empty(m.moe_layer_weights_size(d.H, d.F, d.E), dtype=torch.uint8, device=dev)
@@ -675,68 +829,89 @@ def _e2e(m, d, dims, inp, dev, args, world):
         b["dX"] = torch.empty_like(b["out"])
         b["dg"] = torch.empty((d.T, d.k), dtype=torch.float32, device=dev)
         bufs.append(b)
-    h_out = {n: torch.empty(bufs[0][n].shape, dtype=bufs[0][n].dtype).pin_memory() for n in ("out", "dX", "dg")}
+    h_out = [{n: torch.empty(bufs[0][n].shape, dtype=bufs[0][n].dtype).pin_memory() for n in ("out", "dX", "dg")}
+             for _ in range(2)]
     s = torch.cuda.current_stream(dev)
-    cs = torch.cuda.Stream(dev)
-    ev = lambda: torch.cuda.Event()
-    in_ready = [ev(), ev()]
-    done = [ev(), ev()]
+    hs, ds = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    tev = lambda: torch.cuda.Event(enable_timing=True)
+    in_ready = [tev(), tev()]      # inputs of the buffer copied in
+    done = [tev(), tev()]          # compute on the buffer finished
+    out_read = [tev(), tev()]      # results of the buffer copied out
+    marks = []                     # (h2d start, h2d end, d2h start, d2h end) per step
 
-    def h2d(i):
+    def h2d(i, mk):
         b = bufs[i % 2]
         if i >= 2:
-            cs.wait_event(done[i % 2])  # step i-2 no longer reads this buffer
-        with torch.cuda.stream(cs):
+            hs.wait_event(done[i % 2])         # step i-2 no longer reads this buffer
+        mk[0].record(hs)
+        with torch.cuda.stream(hs):
             for n, t in h_in.items():
                 b[n].copy_(t, non_blocking=True)
-        in_ready[i % 2].record(cs)
+        in_ready[i % 2].record(hs)
+        mk[1].record(hs)
 
     def compute(i):
         b = bufs[i % 2]
         s.wait_event(in_ready[i % 2])
+        if i >= 2:
+            s.wait_event(out_read[i % 2])      # step i-2's results have left this buffer
         m.moe_layer_prep_weights(W13, W2, wq)
         m.moe_layer_fwd(b["x"], wq, d, ws, logits=b["lg"], ids=ids, gate=gate, out=b["out"])
         m.moe_layer_bwd(b["x"], b["dO"], gate, wq, d, ws, dX=b["dX"], dW13=dW13, dW2=dW2, d_gate=b["dg"])
         done[i % 2].record(s)
 
-    def d2h(i):
+    def d2h(i, mk):
         b = bufs[i % 2]
-        cs.wait_event(done[i % 2])
-        with torch.cuda.stream(cs):
-            for n, t in h_out.items():
+        ds.wait_event(done[i % 2])
+        mk[2].record(ds)
+        with torch.cuda.stream(ds):
+            for n, t in h_out[i % 2].items():
                 t.copy_(b[n], non_blocking=True)
+        out_read[i % 2].record(ds)
+        mk[3].record(ds)
 
-    def run(k, start):
-        cs.wait_event(start)
-        h2d(0)
+    def run(k, start, record):
+        hs.wait_event(start)
+        ds.wait_event(start)
+        mks = [[tev() for _ in range(4)] for _ in range(k)]
+        h2d(0, mks[0])
         if k > 1:
-            h2d(1)
+            h2d(1, mks[1])
         for i in range(k):
             compute(i)
-            d2h(i)
+            d2h(i, mks[i])
             if i + 2 < k:
-                h2d(i + 2)
-        fin = ev()
-        fin.record(cs)
-        s.wait_event(fin)
+                h2d(i + 2, mks[i + 2])
+        fin_h, fin_d = tev(), tev()
+        fin_h.record(hs)
+        fin_d.record(ds)
+        s.wait_event(fin_h)
+        s.wait_event(fin_d)
+        if record:
+            marks.extend(mks)
 
-    st = ev()
+    st = tev()
     st.record(s)
-    run(max(args.warmup, 1), st)
+    run(max(args.warmup, 1), st, False)
     torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0, e1 = tev(), tev()
     e0.record(s)
-    run(args.steps, e0)
+    run(args.steps, e0, True)
     e1.record(s)
     torch.cuda.synchronize()
     el = e0.elapsed_time(e1) * 1e-3
     routed = d.T * d.k
     flops = sum(_gemm_flops(d, routed).values())
     h2d_b = sum(t.numel() * t.element_size() for t in h_in.values())
-    d2h_b = sum(t.numel() * t.element_size() for t in h_out.values())
+    d2h_b = sum(t.numel() * t.element_size() for t in h_out[0].values())
+    h2d_ms = statistics.mean(a.elapsed_time(b) for a, b, _, _ in marks)
+    d2h_ms = statistics.mean(c.elapsed_time(e) for _, _, c, e in marks)
     return {"value": world * flops * args.steps / el / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d_b,
             "d2h_bytes_per_step": d2h_b, "ms_per_step": el / args.steps * 1e3,
-            "copies": "pinned host <-> device on a second stream, double-buffered, inside the timed region"}
+            "h2d_ms_per_step": h2d_ms, "d2h_ms_per_step": d2h_ms,
+            "h2d_GBps": h2d_b / h2d_ms / 1e6, "d2h_GBps": d2h_b / d2h_ms / 1e6,
+            "copies": "pinned host <-> device, H2D and D2H on two streams of their own, double-buffered, inside "
+                      "the timed region; weight gradients stay on the device"}
 
 
 if __name__ == "__main__":

@@ -32,7 +32,9 @@
  *   - Matrices are row-major.  bf16 is IEEE bfloat16 (uint16 storage); fp8 is
  *     OCP E4M3FN (uint8); scales are E8M0 bytes (2^(b-127), 0xFF = NaN).
  *   - Sizes are int64_t; ids, counts and offsets are int32.
- *   - Device pointers must be 16-byte aligned (MX_ERR_ALIGNMENT otherwise).
+ *   - Device pointers must be 16-byte aligned (MX_ERR_ALIGNMENT otherwise),
+ *     except scale arrays, which may start at any byte unless an entry point
+ *     states otherwise.
  *   - Requires an sm_103 device (GB300); MX_ERR_UNSUPPORTED_DEVICE otherwise.
  */
 #ifndef MXMOE_H
@@ -51,7 +53,7 @@ typedef struct CUstream_st *mx_stream; /* same type as cudaStream_t */
 #define MX_OK 0
 #define MX_ERR_INVALID_ARG 1        /* null pointer, unknown enum, negative size */
 #define MX_ERR_SHAPE 2              /* a dimension breaks a multiple-of-32/128/256 rule */
-#define MX_ERR_ALIGNMENT 3          /* a pointer is not 16-byte aligned */
+#define MX_ERR_ALIGNMENT 3          /* a pointer breaks its alignment rule (16 bytes unless stated) */
 #define MX_ERR_UNSUPPORTED_DEVICE 4 /* current device is not sm_103 */
 #define MX_ERR_CUDA 5               /* a CUDA runtime/driver call failed */
 #define MX_ERR_DEVICE 6             /* device-detected: id out of range, bad offsets */
@@ -109,6 +111,20 @@ mx_status mx_check_device(void);
  * (device int32, required).  Enqueued on `stream`; returns host errors only.
  */
 mx_status mx_selftest_wait_timeout(int64_t timeout_ns, int32_t *dev_status, mx_stream stream);
+
+/*
+ * Self-test of the SwiGLU arithmetic (no counterpart on the pages: the pages
+ * fix no precision for the SwiGLU step; this exposes the fp32 sigmoid the
+ * fused SwiGLU forward and backward kernels use, so that its error can be
+ * measured against an exact evaluation).  For each of the n bf16 values a[i]
+ * (device, uint16 storage) writes three fp32 values to out[3i .. 3i+2]
+ * (device):
+ *   s = sigmoid(a) * 2^k,  1 - sigmoid(a),  2^-k,
+ * with k = 64 for a < -64 and 0 otherwise (the kernels carry the 2^64 factor
+ * until their last product, so that sigmoid(a) never leaves the fp32 normal
+ * range; s * 2^-k is sigmoid(a)).  n >= 0; a and out may be NULL when n = 0.
+ */
+mx_status mx_selftest_sigmoid(const void *a, int64_t n, float *out, mx_stream stream);
 
 /* Bytes of a scale array for `rows` x `cols` elements (cols % 32 == 0) in the
  * given layout: rows*cols/32 (PLAIN) or the padded tile size (SWIZZLED). */
@@ -282,6 +298,8 @@ mx_status moe_unpermute(const void *y, const int32_t *dst, const float *gate,
  *   C [E, N, K]; an empty group writes zeros.
  * Sizes: M_cap % 128 == 0, N % 256 == 0, K % 128 == 0, 1 <= E <= 1024.
  * c_dtype: MX_OUT_BF16 (round-to-nearest-even) or MX_OUT_F32.
+ * Alignment: A, B, sA, sB and C 16-byte aligned (the operands and their
+ * scales are read by TMA).
  */
 mx_status mx_grouped_gemm(int32_t op, const uint8_t *A, const uint8_t *sA,
                           const uint8_t *B, const uint8_t *sB,
@@ -298,9 +316,11 @@ mx_status mx_grouped_gemm(int32_t op, const uint8_t *A, const uint8_t *sA,
  * 0..F-1 of each expert from W1^T, F..2F-1 from W3^T), sB scales of (E*2F, H).
  * Per row: a = x W1, b = x W3 accumulated in fp32 and rounded to bf16, saved to
  * ab bf16 [M_cap, 2F] (a in columns 0..F-1, b in F..2F-1); h = silu(a) * b in
- * fp32 (silu(a) = a / (1 + e^-a)) is quantized (ROW mode, blocks along F)
- * into hq fp8 [M_cap, F] and hs (MX_SCALE_SWIZZLED scales of (M_cap, F)).
- * F % 128 == 0, H % 128 == 0, M_cap % 128 == 0.
+ * fp32 (silu(a) = a / (1 + e^-a), the sigmoid of mx_selftest_sigmoid) is
+ * quantized (ROW mode, blocks along F) into hq fp8 [M_cap, F] and hs
+ * (MX_SCALE_SWIZZLED scales of (M_cap, F)).
+ * F % 128 == 0, H % 128 == 0, M_cap % 128 == 0.  A, B, sA, sB, ab and hq
+ * 16-byte aligned; hs may sit at any byte.
  */
 mx_status moe_gemm1_swiglu(const uint8_t *A, const uint8_t *sA, const uint8_t *B,
                            const uint8_t *sB, const int32_t *offsets, int32_t E,
@@ -317,11 +337,20 @@ mx_status moe_gemm1_swiglu(const uint8_t *A, const uint8_t *sA, const uint8_t *B
  *   dab_cq / dab_cs; h = silu(a) * b is recomputed and quantized COL into
  *   h_cq [F, M_cap] / h_cs.  All scales MX_SCALE_SWIZZLED.
  * `rows` = rows to process (<= M_cap, multiple of 128).  F % 32 == 0.
+ * row_limit: optional device int32 (NULL = all `rows`): 128-row bands that
+ * start at or past *row_limit are skipped and their outputs left untouched
+ * (the layer passes offsets + E, the end of the routed rows).
+ * Arithmetic: fp32; sigmoid(a) from the hardware's approximate base-2
+ * exponential and reciprocal with an exactly rounded exponent (see
+ * mx_selftest_sigmoid): a few fp32 ulps over bf16 a in [-128, 128].
+ * Alignment: dab_cs and h_cs must be 4-byte aligned (each column's four
+ * row-block scales are written as one 32-bit word); dab_rs may sit at any byte.
  */
 mx_status moe_swiglu_bwd(const float *dh, const void *ab, int64_t rows,
                          int64_t F, uint8_t *dab_rq, uint8_t *dab_rs,
                          uint8_t *dab_cq, uint8_t *dab_cs, uint8_t *h_cq,
-                         uint8_t *h_cs, mx_stream stream);
+                         uint8_t *h_cs, const int32_t *row_limit,
+                         mx_stream stream);
 
 /* ------------------------------------------------------------------------ */
 /* Backward helpers (token shuffle of the gradients, gate gradient)          */
@@ -336,12 +365,15 @@ mx_status moe_swiglu_bwd(const float *dh, const void *ab, int64_t rows,
  * q_col [H, rows_cap] / s_col.  Scales are MX_SCALE_SWIZZLED.  Used for the
  * routed output gradient dY = gate * dOut (both layouts) and for the permuted
  * input x (COL, for wgrad).  x bf16 [T, H]; src from moe_permute_map.
- * H % 128 == 0, rows_cap % 128 == 0.
+ * H % 128 == 0, rows_cap % 128 == 0.  row_limit: optional device int32 (NULL
+ * = all rows_cap rows): 128-row bands that start at or past *row_limit are
+ * skipped and their outputs left untouched (the layer passes offsets + E).
  */
 mx_status moe_gather_quant(const void *x, const float *gate, const int32_t *src,
                            int64_t T, int64_t H, int32_t k, int64_t rows_cap,
                            int32_t mode, uint8_t *q_row, uint8_t *s_row,
-                           uint8_t *q_col, uint8_t *s_col, mx_stream stream);
+                           uint8_t *q_col, uint8_t *s_col,
+                           const int32_t *row_limit, mx_stream stream);
 
 /*
  * Gate gradient: d_gate[t,j] = sum_h dOut[t,h] * y[dst[t*k+j], h], fp32

@@ -22,7 +22,7 @@ from ._lib import (MX_GEMM_DGRAD, MX_GEMM_FWD, MX_GEMM_WGRAD, MX_MODE_BOTH, MX_M
 __all__ = [
     "lib", "MxError", "mx_quantize", "mx_dequantize", "mx_scale_bytes", "moe_route", "moe_rows_cap", "moe_permute_map",
     "moe_permute", "moe_unpermute", "mx_grouped_gemm", "moe_gemm1_swiglu", "moe_swiglu_bwd",
-    "moe_gather_quant", "moe_gate_grad", "MoELayerDims", "moe_layer_prep_weights", "moe_layer_fwd",
+    "moe_gather_quant", "moe_gate_grad", "mx_selftest_sigmoid", "MoELayerDims", "moe_layer_prep_weights", "moe_layer_fwd",
     "moe_layer_bwd", "moe_layer_workspace_size", "moe_layer_weights_size",
 ]
 
@@ -172,8 +172,10 @@ def moe_gemm1_swiglu(A, sA, B, sB, offsets, E: int, M_cap: int, F: int, H: int,
     return ab, hq, hs
 
 
-def moe_swiglu_bwd(dh: torch.Tensor, ab: torch.Tensor):
-    """-> (dab_rq, dab_rs, dab_cq, dab_cs, h_cq, h_cs), scales swizzled."""
+def moe_swiglu_bwd(dh: torch.Tensor, ab: torch.Tensor, row_limit: torch.Tensor | None = None):
+    """-> (dab_rq, dab_rs, dab_cq, dab_cs, h_cq, h_cs), scales swizzled.
+    row_limit: optional device int32 tensor whose first element bounds the
+    rows processed (128-row bands at or past it are left unwritten)."""
     _req(dh, torch.float32, "dh")
     _req(ab, torch.bfloat16, "ab")
     rows, F = dh.shape
@@ -185,12 +187,15 @@ def moe_swiglu_bwd(dh: torch.Tensor, ab: torch.Tensor):
     h_cq = torch.empty((F, rows), dtype=torch.uint8, device=dev)
     h_cs = _u8(mx_scale_bytes(F, rows, MX_SCALE_SWIZZLED), dev)
     _lib.check(lib().moe_swiglu_bwd(_ptr(dh), _ptr(ab), rows, F, _ptr(dab_rq), _ptr(dab_rs), _ptr(dab_cq),
-                                    _ptr(dab_cs), _ptr(h_cq), _ptr(h_cs), _stream(dev)), "moe_swiglu_bwd")
+                                    _ptr(dab_cs), _ptr(h_cq), _ptr(h_cs), _ptr(row_limit), _stream(dev)),
+               "moe_swiglu_bwd")
     return dab_rq, dab_rs, dab_cq, dab_cs, h_cq, h_cs
 
 
-def moe_gather_quant(x: torch.Tensor, gate, src: torch.Tensor, k: int, mode: int = MX_MODE_BOTH):
-    """-> (q_row, s_row, q_col, s_col) of the gathered [rows_cap, H] matrix."""
+def moe_gather_quant(x: torch.Tensor, gate, src: torch.Tensor, k: int, mode: int = MX_MODE_BOTH,
+                     row_limit: torch.Tensor | None = None):
+    """-> (q_row, s_row, q_col, s_col) of the gathered [rows_cap, H] matrix.
+    row_limit: as in moe_swiglu_bwd."""
     _req(x, torch.bfloat16, "x")
     T, H = x.shape
     R = src.numel()
@@ -203,8 +208,18 @@ def moe_gather_quant(x: torch.Tensor, gate, src: torch.Tensor, k: int, mode: int
         q_col = torch.empty((H, R), dtype=torch.uint8, device=dev)
         s_col = _u8(mx_scale_bytes(H, R, MX_SCALE_SWIZZLED), dev)
     _lib.check(lib().moe_gather_quant(_ptr(x), _ptr(gate), _ptr(src), T, H, k, R, mode, _ptr(q_row), _ptr(s_row),
-                                      _ptr(q_col), _ptr(s_col), _stream(dev)), "moe_gather_quant")
+                                      _ptr(q_col), _ptr(s_col), _ptr(row_limit), _stream(dev)), "moe_gather_quant")
     return q_row, s_row, q_col, s_col
+
+
+def mx_selftest_sigmoid(a: torch.Tensor):
+    """The SwiGLU kernels' fp32 sigmoid pieces on bf16 values a (any shape):
+    -> (s, one_minus_sigma, back) fp32 tensors of a's shape, sigma = s * back."""
+    _req(a, torch.bfloat16, "a")
+    a = a.contiguous()
+    out = torch.empty(a.shape + (3,), dtype=torch.float32, device=a.device)
+    _lib.check(lib().mx_selftest_sigmoid(_ptr(a), a.numel(), _ptr(out), _stream(a.device)), "mx_selftest_sigmoid")
+    return out[..., 0], out[..., 1], out[..., 2]
 
 
 def moe_gate_grad(dOut: torch.Tensor, y: torch.Tensor, dst: torch.Tensor, k: int):

@@ -38,6 +38,7 @@ SIGNATURES = {
     "mx_abi_version": (_i32, []),
     "mx_check_device": (_i32, []),
     "mx_selftest_wait_timeout": (_i32, [_i64, _p, _p]),
+    "mx_selftest_sigmoid": (_i32, [_p, _i64, _p, _p]),
     "mx_scale_bytes": (_i64, [_i64, _i64, _i32]),
     "mx_quantize": (_i32, [_p, _i64, _i64, _i64, _i32, _i32, _p, _p, _p, _p, _p]),
     "mx_dequantize": (_i32, [_p, _p, _i64, _i64, _i64, _i32, _i32, _p, _p]),
@@ -50,8 +51,8 @@ SIGNATURES = {
     "moe_unpermute": (_i32, [_p, _p, _p, _i64, _i64, _i32, _p, _p]),
     "mx_grouped_gemm": (_i32, [_i32, _p, _p, _p, _p, _p, _i32, _i64, _i64, _i64, _p, _i32, _p, _p]),
     "moe_gemm1_swiglu": (_i32, [_p, _p, _p, _p, _p, _i32, _i64, _i64, _i64, _p, _p, _p, _p, _p]),
-    "moe_swiglu_bwd": (_i32, [_p, _p, _i64, _i64, _p, _p, _p, _p, _p, _p, _p]),
-    "moe_gather_quant": (_i32, [_p, _p, _p, _i64, _i64, _i32, _i64, _i32, _p, _p, _p, _p, _p]),
+    "moe_swiglu_bwd": (_i32, [_p, _p, _i64, _i64, _p, _p, _p, _p, _p, _p, _p, _p]),
+    "moe_gather_quant": (_i32, [_p, _p, _p, _i64, _i64, _i32, _i64, _i32, _p, _p, _p, _p, _p, _p]),
     "moe_gate_grad": (_i32, [_p, _p, _p, _i64, _i64, _i32, _p, _p]),
     "moe_layer_weights_size": (_i64, [_i64, _i64, _i32]),
     "moe_layer_workspace_size": (_i64, [_i64, _i64, _i64, _i32, _i32]),

@@ -41,7 +41,29 @@ __global__ void k_selftest_wait_timeout(uint64_t timeout_ns, int32_t *dev_status
   if (!mbar_wait_warp(&bar, 0, timeout_ns) && threadIdx.x == 0) set_status(dev_status, MX_ERR_TIMEOUT);
 }
 
+// The SwiGLU kernels' sigmoid pieces (sigmoid_parts), evaluated on bf16 inputs:
+// out[3i] = s, out[3i+1] = 1 - sigma, out[3i+2] = back (sigma = s * back).
+__global__ void k_selftest_sigmoid(const uint16_t *__restrict__ a, int64_t n, float *__restrict__ out) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+    const SigParts p = sigmoid_parts(__uint_as_float((uint32_t)a[i] << 16));
+    out[3 * i] = p.s;
+    out[3 * i + 1] = p.oms;
+    out[3 * i + 2] = p.back;
+  }
+}
+
 }  // namespace mxmoe
+
+extern "C" mx_status mx_selftest_sigmoid(const void *a, int64_t n, float *out, mx_stream stream) {
+  MX_HOST_CHECK(n >= 0 && (n == 0 || (a && out)), MX_ERR_INVALID_ARG);
+  mx_status st = mxmoe::check_device_cached();
+  if (st != MX_OK) return st;
+  if (n == 0) return MX_OK;
+  const int64_t blocks = (n + 255) / 256;
+  mxmoe::k_selftest_sigmoid<<<(unsigned)(blocks < 4096 ? blocks : 4096), 256, 0, stream>>>(
+      static_cast<const uint16_t *>(a), n, out);
+  return mxmoe::launch_status();
+}
 
 extern "C" mx_status mx_selftest_wait_timeout(int64_t timeout_ns, int32_t *dev_status, mx_stream stream) {
   MX_HOST_CHECK(dev_status != nullptr, MX_ERR_INVALID_ARG);
@@ -57,7 +79,8 @@ extern "C" const char *mx_status_string(mx_status s) {
     case MX_OK: return "MX_OK";
     case MX_ERR_INVALID_ARG: return "MX_ERR_INVALID_ARG: null pointer, unknown enum or negative size";
     case MX_ERR_SHAPE: return "MX_ERR_SHAPE: a dimension breaks the multiple-of-32/128/256 rule";
-    case MX_ERR_ALIGNMENT: return "MX_ERR_ALIGNMENT: a device pointer is not 16-byte aligned";
+    case MX_ERR_ALIGNMENT:
+      return "MX_ERR_ALIGNMENT: a device pointer breaks its alignment rule (16 bytes; 4 for word-written scales)";
     case MX_ERR_UNSUPPORTED_DEVICE: return "MX_ERR_UNSUPPORTED_DEVICE: the current device is not sm_103";
     case MX_ERR_CUDA: return "MX_ERR_CUDA: a CUDA call failed";
     case MX_ERR_DEVICE: return "MX_ERR_DEVICE: the device found an expert id out of range or bad group offsets";
@@ -69,6 +92,6 @@ extern "C" const char *mx_status_string(mx_status s) {
   }
 }
 
-extern "C" int32_t mx_abi_version(void) { return 1; }
+extern "C" int32_t mx_abi_version(void) { return 2; }
 
 extern "C" mx_status mx_check_device(void) { return mxmoe::check_device_cached(); }

@@ -27,6 +27,7 @@ namespace mxmoe {
 // host-side validation helpers
 // ---------------------------------------------------------------------------
 static inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+static inline bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
 mx_status check_device_cached();  // defined in api.cu
 mx_status launch_status();        // cudaGetLastError -> mx_status
@@ -80,12 +81,10 @@ __device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float
 
 __device__ __forceinline__ uint32_t abs_bits(float v) { return __float_as_uint(v) & 0x7fffffffu; }
 
-// e^-a as 2^(-a log2 e) on the hardware's approximate base-2 exponential
-// (ex2.approx, a few ulp); rounding -a log2 e to fp32 adds about |a| 2^-24
-// relative.  +inf for a below about -88.7; 0 (flushed) for a above about 87.
-__device__ __forceinline__ float exp_neg_approx(float a) {
+// 2^x on the hardware's approximate base-2 exponential (ex2.approx).
+__device__ __forceinline__ float ex2_approx(float x) {
   float e;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(a * -1.4426950408889634f));
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(x));
   return e;
 }
 
@@ -94,6 +93,45 @@ __device__ __forceinline__ float rcp_approx(float x) {
   float r;
   asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
   return r;
+}
+
+// The sigmoid of a bf16 value a, in pieces that keep fp32 accuracy over the
+// whole range the SwiGLU kernels see:
+//   s    = sigma(a) * 2^k        (k = 64 when a < -64, else 0)
+//   oms  = 1 - sigma(a)
+//   back = 2^-k
+// so silu(a) * b = ((a * s) * b) * back, with the multiply by `back` the only
+// rounding that may enter the fp32 subnormal range.
+//
+// t = e^-|a| = 2^(-|a| log2 e).  log2 e is split as LOG2E_HI (16 significant
+// bits) plus a remainder: a has 8 significant bits, so |a| * LOG2E_HI is
+// exact in fp32 and the exponential's argument carries no rounding error (the
+// constant-splitting of Cody and Waite, 1980).  The remainder enters as the
+// factor e^-y with y = |a| (1 - LOG2E_HI ln 2), |y| < 1.3e-3, taken as
+// 1 - y + y^2/2 (error below 4e-10).  Then sigma(a) = 1/(1+t) for a >= 0 and
+// t/(1+t) for a < 0, and 1 - sigma(a) the other one: no cancellation on
+// either side.  For a < -64 the exponential is taken 2^64 higher, which keeps
+// t and s in the normal range down to a = -128 (1 + t is then 1 in fp32).
+// |a| is capped at 256 (t is 0 beyond); NaN propagates through the caller's
+// products with a.
+constexpr float LOG2E_HI = 0x1.7154p+0f;          // 23637 / 16384
+constexpr float LOG2E_REM_LN = 0x1.480fb6p-18f;   // 1 - LOG2E_HI * ln 2
+struct SigParts {
+  float s, oms, back;
+};
+__device__ __forceinline__ SigParts sigmoid_parts(float a) {
+  const float aa = fminf(fabsf(a), 256.0f);
+  const bool far = a < -64.0f;
+  const float t0 = ex2_approx(fmaf(aa, -LOG2E_HI, far ? 64.0f : 0.0f));  // exact argument
+  const float y = aa * LOG2E_REM_LN;
+  const float t = t0 * fmaf(y, fmaf(0.5f, y, -1.0f), 1.0f);               // e^-|a| (* 2^64 if far)
+  const float r = rcp_approx(far ? 1.0f : 1.0f + t);
+  const float tr = t * r;
+  SigParts p;
+  p.s = a >= 0.0f ? r : tr;
+  p.oms = a >= 0.0f ? tr : r;
+  p.back = far ? 0x1p-64f : 1.0f;
+  return p;
 }
 
 // Two-lane 16-bit integer max.  On bf16 pairs with the sign bits cleared

@@ -190,7 +190,7 @@ __device__ __forceinline__ void glu_epilogue(const Params &p, const CUtensorMap 
       for (int i = 0; i < 8; ++i) {
         av[i] = round_bf16(__uint_as_float(r[blk * 32 + j + i]));
         bv[i] = round_bf16(__uint_as_float(r[64 + blk * 32 + j + i]));
-        hv[j + i] = silu_f(av[i]) * bv[i];
+        hv[j + i] = swiglu_h(av[i], bv[i]);
         am = max(am, abs_bits(hv[j + i]));
       }
       va[j / 8] = make_uint4(pack_bf16x2(av[0], av[1]), pack_bf16x2(av[2], av[3]), pack_bf16x2(av[4], av[5]),

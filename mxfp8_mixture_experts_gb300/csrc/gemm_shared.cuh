@@ -38,11 +38,14 @@ __host__ __device__ constexpr uint32_t idesc_mxf8(int M, int N) {
   return (0u << 7) | (0u << 10) | ((uint32_t)(N >> 3) << 17) | (1u << 23) | ((uint32_t)(M >> 4) << 24);
 }
 
-// silu(a) = a / (1 + e^-a) from the approximate exponential and reciprocal:
-// within ~1e-6 relative for |a| < 16 (about 16% faster GEMM1 than IEEE expf
-// and division, whose instruction count the epilogue could not hide).  Very
-// negative a gives e^-a = inf and -0; NaN/inf inputs stay non-finite.
-__device__ __forceinline__ float silu_f(float a) { return a * rcp_approx(1.0f + exp_neg_approx(a)); }
+// h = silu(a) * b = a * sigma(a) * b in fp32 for bf16 a, b (sigma from
+// sigmoid_parts: within a few fp32 ulps of the exact value over the whole
+// bf16 range of a that matters, with one final rounding into the subnormal
+// range for very negative a).
+__device__ __forceinline__ float swiglu_h(float a, float b) {
+  const SigParts p = sigmoid_parts(a);
+  return ((a * p.s) * b) * p.back;
+}
 
 // Validate the group offsets (identically in every CTA): non-decreasing,
 // multiples of 128, last one within M_cap.
@@ -115,7 +118,7 @@ __device__ __forceinline__ void epi_store(const Params &p, int64_t orow, int64_t
         for (int i = 0; i < 8; ++i) {
           av[i] = round_bf16(__uint_as_float(r[blk * 32 + j + i]));
           bv[i] = round_bf16(__uint_as_float(r[64 + blk * 32 + j + i]));
-          hv[j + i] = silu_f(av[i]) * bv[i];
+          hv[j + i] = swiglu_h(av[i], bv[i]);
           am = max(am, abs_bits(hv[j + i]));
         }
         pa[(blk * 32 + j) / 8] = make_uint4(pack_bf16x2(av[0], av[1]), pack_bf16x2(av[2], av[3]),

@@ -15,7 +15,7 @@
 
 extern "C" mx_status moe_gather_quant(const void *x, const float *gate, const int32_t *src, int64_t T, int64_t H,
                                       int32_t k, int64_t rows_cap, int32_t mode, uint8_t *q_row, uint8_t *s_row,
-                                      uint8_t *q_col, uint8_t *s_col, mx_stream stream);
+                                      uint8_t *q_col, uint8_t *s_col, const int32_t *row_limit, mx_stream stream);
 extern "C" mx_status moe_gate_grad(const void *dOut, const void *y, const int32_t *dst, int64_t T, int64_t H,
                                    int32_t k, float *d_gate, mx_stream stream);
 
@@ -186,11 +186,15 @@ extern "C" mx_status moe_layer_bwd(const void *x, const void *dOut, const float 
   const int64_t R = w.R;
   if (d_gate) MX_TRY(moe_gate_grad(dOut, w.y, w.dst, T, H, k, d_gate, stream));
   // dY rows = gate * dOut, quantized along H (dgrad2) and along tokens (wgrad2)
-  MX_TRY(moe_gather_quant(dOut, gate, w.src, T, H, k, R, MX_MODE_BOTH, w.dy_rq, w.dy_rs, w.dy_cq, w.dy_cs, stream));
+  // (rows past offsets[E], the end of the routed rows, are skipped on the device)
+  const int32_t *row_limit = w.offsets + E;
+  MX_TRY(moe_gather_quant(dOut, gate, w.src, T, H, k, R, MX_MODE_BOTH, w.dy_rq, w.dy_rs, w.dy_cq, w.dy_cs, row_limit,
+                          stream));
   // dh = dY W2^T : B = W2[e] [F, H] quantized along H
   MX_TRY(mx_grouped_gemm(MX_GEMM_DGRAD, w.dy_rq, w.dy_rs, v.w2_rq, v.w2_rs, w.offsets, E, R, F, H, w.dh,
                          MX_OUT_F32, dev_status, stream));
-  MX_TRY(moe_swiglu_bwd(w.dh, w.ab, R, F, w.dab_rq, w.dab_rs, w.dab_cq, w.dab_cs, w.h_cq, w.h_cs, stream));
+  MX_TRY(moe_swiglu_bwd(w.dh, w.ab, R, F, w.dab_rq, w.dab_rs, w.dab_cq, w.dab_cs, w.h_cq, w.h_cs, row_limit,
+                        stream));
   // dW2[e] = h^T dY over the expert's tokens -> [F, H]
   MX_TRY(mx_grouped_gemm(MX_GEMM_WGRAD, w.h_cq, w.h_cs, w.dy_cq, w.dy_cs, w.offsets, E, R, F, H, dW2, MX_OUT_F32,
                          dev_status, stream));
@@ -198,7 +202,8 @@ extern "C" mx_status moe_layer_bwd(const void *x, const void *dOut, const float 
   MX_TRY(mx_grouped_gemm(MX_GEMM_DGRAD, w.dab_rq, w.dab_rs, v.w13_rq, v.w13_rs, w.offsets, E, R, H, 2 * F, w.dxp,
                          MX_OUT_BF16, dev_status, stream));
   // x permuted (bf16) and quantized along tokens for wgrad1
-  MX_TRY(moe_gather_quant(x, nullptr, w.src, T, H, k, R, MX_MODE_COL, nullptr, nullptr, w.xp_cq, w.xp_cs, stream));
+  MX_TRY(moe_gather_quant(x, nullptr, w.src, T, H, k, R, MX_MODE_COL, nullptr, nullptr, w.xp_cq, w.xp_cs, row_limit,
+                          stream));
   // dW13[e] = xp^T dab over the expert's tokens -> [H, 2F]
   MX_TRY(mx_grouped_gemm(MX_GEMM_WGRAD, w.xp_cq, w.xp_cs, w.dab_cq, w.dab_cs, w.offsets, E, R, H, 2 * F, dW13,
                          MX_OUT_F32, dev_status, stream));

@@ -32,6 +32,7 @@ struct QuantArgs {
   const int32_t *src;
   const float *gate;
   int k;
+  const int32_t *row_limit;  // gather mode, nullable: rows at or past *row_limit are skipped
   uint8_t *q_row, *s_row, *q_col, *s_col;
   int64_t s_row_stride, s_col_stride;  // bytes per batch entry
   int32_t swizzled;
@@ -81,6 +82,8 @@ __global__ void __launch_bounds__(QT_THREADS, 6) k_quantize_bf16(QuantArgs a) {
   const uint32_t ucols = (uint32_t)a.cols;
   const int64_t tile_off = (b * a.rows + row0) * a.cols + gc;  // element (row0 + tr, gc) minus tr rows
   const uint32_t t_off = (uint32_t)tr * ucols;
+
+  if (GATHER && a.row_limit && row0 >= __ldg(a.row_limit)) return;  // past the last routed row
 
   // ---- phase 0: every load of this thread in flight at once ----
   // (gather mode: all source indices first, then the rows and their gates,
@@ -235,7 +238,7 @@ constexpr int SB_SMEM = 3 * SB_ROWS * SB_VAL_STRIDE * 4 + 3 * SB_COLS * SB_Q_STR
 __global__ void __launch_bounds__(SB_THREADS) k_swiglu_bwd(const float *__restrict__ dh, const uint16_t *__restrict__ ab,
                                                            int64_t rows, int64_t F, uint8_t *dab_rq, uint8_t *dab_rs,
                                                            uint8_t *dab_cq, uint8_t *dab_cs, uint8_t *h_cq,
-                                                           uint8_t *h_cs) {
+                                                           uint8_t *h_cs, const int32_t *__restrict__ row_limit) {
   extern __shared__ __align__(16) uint8_t sb_smem[];
   float *vals = reinterpret_cast<float *>(sb_smem);                          // [3][128][33]
   uint8_t *qst = sb_smem + 3 * SB_ROWS * SB_VAL_STRIDE * 4;                    // [3][32][144]
@@ -243,6 +246,7 @@ __global__ void __launch_bounds__(SB_THREADS) k_swiglu_bwd(const float *__restri
   const int tid = threadIdx.x;
   const int64_t row0 = (int64_t)blockIdx.x * SB_ROWS;  // row bands fastest (see k_quantize_bf16)
   const int64_t f0 = (int64_t)blockIdx.y * SB_COLS;
+  if (row_limit && row0 >= __ldg(row_limit)) return;  // past the last routed row: nothing to do
   const int64_t twoF = 2 * F;
   const int64_t cb2 = twoF / 32;
 
@@ -284,16 +288,15 @@ __global__ void __launch_bounds__(SB_THREADS) k_swiglu_bwd(const float *__restri
     uint32_t ama = 0, amb = 0;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      // s = sigmoid(a) = 1 / (1 + e^-a) and 1 - s = e^-a s (no cancellation
-      // for large a); a is clamped at -87 so that e^-a stays finite
-      const float e = exp_neg_approx(fmaxf(A[i], -87.0f));
-      const float s = rcp_approx(1.0f + e);
-      const float silu = A[i] * s;
-      da[i] = d[i] * B[i] * s * (1.0f + A[i] * (e * s));
-      db[i] = d[i] * silu;
+      // sigma(a) (scaled by 2^64 for a < -64, undone by `back` in the last
+      // product) and 1 - sigma(a), each without cancellation
+      const SigParts p = sigmoid_parts(A[i]);
+      const float silu = A[i] * p.s;
+      da[i] = ((d[i] * B[i]) * p.s * (1.0f + A[i] * p.oms)) * p.back;
+      db[i] = (d[i] * silu) * p.back;
       vals[(0 * SB_ROWS + r) * SB_VAL_STRIDE + ch * 8 + i] = da[i];
       vals[(1 * SB_ROWS + r) * SB_VAL_STRIDE + ch * 8 + i] = db[i];
-      vals[(2 * SB_ROWS + r) * SB_VAL_STRIDE + ch * 8 + i] = silu * B[i];
+      vals[(2 * SB_ROWS + r) * SB_VAL_STRIDE + ch * 8 + i] = (silu * B[i]) * p.back;
       ama = max(ama, abs_bits(da[i]));
       amb = max(amb, abs_bits(db[i]));
     }
@@ -497,6 +500,7 @@ extern "C" mx_status mx_quantize(const void *x, int64_t batch, int64_t rows, int
   a.src = nullptr;
   a.gate = nullptr;
   a.k = 1;
+  a.row_limit = nullptr;
   a.x = static_cast<const uint16_t *>(x);
   a.rows = rows;
   a.cols = cols;
@@ -548,7 +552,7 @@ extern "C" mx_status mx_dequantize(const uint8_t *q, const uint8_t *s, int64_t b
 
 extern "C" mx_status moe_gather_quant(const void *x, const float *gate, const int32_t *src, int64_t T, int64_t H,
                                       int32_t k, int64_t rows_cap, int32_t mode, uint8_t *q_row, uint8_t *s_row,
-                                      uint8_t *q_col, uint8_t *s_col, mx_stream stream) {
+                                      uint8_t *q_col, uint8_t *s_col, const int32_t *row_limit, mx_stream stream) {
   MX_HOST_CHECK(src && (T == 0 || x), MX_ERR_INVALID_ARG);  // T = 0: every row is a zero pad row
   MX_HOST_CHECK(mode == MX_MODE_ROW || mode == MX_MODE_COL || mode == MX_MODE_BOTH, MX_ERR_INVALID_ARG);
   MX_HOST_CHECK(T >= 0 && H > 0 && k >= 1 && rows_cap >= 0, MX_ERR_INVALID_ARG);
@@ -567,6 +571,7 @@ extern "C" mx_status moe_gather_quant(const void *x, const float *gate, const in
   a.src = src;
   a.gate = gate;
   a.k = k;
+  a.row_limit = row_limit;
   a.q_row = q_row;
   a.s_row = s_row;
   a.q_col = q_col;
@@ -588,12 +593,14 @@ extern "C" mx_status moe_gather_quant(const void *x, const float *gate, const in
 
 extern "C" mx_status moe_swiglu_bwd(const float *dh, const void *ab, int64_t rows, int64_t F, uint8_t *dab_rq,
                                     uint8_t *dab_rs, uint8_t *dab_cq, uint8_t *dab_cs, uint8_t *h_cq,
-                                    uint8_t *h_cs, mx_stream stream) {
+                                    uint8_t *h_cs, const int32_t *row_limit, mx_stream stream) {
   MX_HOST_CHECK(dh && ab && dab_rq && dab_rs && dab_cq && dab_cs && h_cq && h_cs, MX_ERR_INVALID_ARG);
   MX_HOST_CHECK(rows >= 0 && F > 0, MX_ERR_INVALID_ARG);
   MX_HOST_CHECK(rows % SB_ROWS == 0 && F % SB_COLS == 0 && F / SB_COLS < 65535, MX_ERR_SHAPE);
   MX_HOST_CHECK(aligned16(dh) && aligned16(ab) && aligned16(dab_rq) && aligned16(dab_cq) && aligned16(h_cq),
                 MX_ERR_ALIGNMENT);
+  // the column scales leave as 32-bit words (four row blocks of one column)
+  MX_HOST_CHECK(aligned4(dab_cs) && aligned4(h_cs), MX_ERR_ALIGNMENT);
   mx_status st = check_device_cached();
   if (st != MX_OK) return st;
   if (rows == 0) return MX_OK;
@@ -606,6 +613,6 @@ extern "C" mx_status moe_swiglu_bwd(const float *dh, const void *ab, int64_t row
   }
   dim3 grid((unsigned)(rows / SB_ROWS), (unsigned)(F / SB_COLS));
   k_swiglu_bwd<<<grid, SB_THREADS, SB_SMEM, stream>>>(dh, static_cast<const uint16_t *>(ab), rows, F, dab_rq, dab_rs,
-                                                      dab_cq, dab_cs, h_cq, h_cs);
+                                                      dab_cq, dab_cs, h_cq, h_cs, row_limit);
   return launch_status();
 }

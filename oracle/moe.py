@@ -22,7 +22,7 @@ Sources
   a * sigmoid(a)).  The pages name no FFN; SwiGLU is the workload's stated
   expert type.
 
-Readings where the pages are silent (each is also listed in the design notes):
+Readings where the pages are silent:
 * Router: top-k of the fp32 logits, ties to the lower expert id; the gate of a
   chosen expert is the softmax over all E logits evaluated at it.
 * Each expert's group is padded to a multiple of 128 rows; pad rows hold zero

@@ -22,7 +22,7 @@ Sources
   specification, section 6.3 (conversion of a vector of scalars to MX).
   Element casts round to nearest, ties to even, and saturate to +-448.
 
-Readings where the sources are silent (each is also listed in the design notes):
+Readings where the sources are silent:
 * A block holding a NaN or an infinity gets scale byte 0xFF (NaN) and every
   element byte 0x7F (NaN).
 * An all-zero block (amax = 0) gets the smallest scale, byte 0x00 (2^-127);

@@ -43,7 +43,7 @@ def test_status_strings(lib):
     for code in range(0, 10):
         s = lib.mx_status_string(code).decode()
         assert s.startswith("MX_")
-    assert lib.mx_abi_version() == 1
+    assert lib.mx_abi_version() == 2
 
 
 def test_size_queries(lib):
@@ -97,6 +97,27 @@ def test_host_side_argument_errors(lib):
         _lib.MX_ERR_SHAPE
     # route: k > E
     assert lib.moe_route(fake, 16, 4, 5, fake, fake, None) == _lib.MX_ERR_INVALID_ARG
+    # sigmoid self-test: negative count, null buffers
+    assert lib.mx_selftest_sigmoid(fake, -1, fake, None) == _lib.MX_ERR_INVALID_ARG
+    assert lib.mx_selftest_sigmoid(None, 4, fake, None) == _lib.MX_ERR_INVALID_ARG
+
+
+def test_swiglu_bwd_word_written_scales_must_be_4_byte_aligned(lib):
+    """moe_swiglu_bwd writes each column's four row-block scales of dab_cs and
+    h_cs as one 32-bit word: a scale pointer off a 4-byte boundary is refused
+    on the host with MX_ERR_ALIGNMENT before anything is launched (the same
+    call with aligned pointers gets past every argument check and stops only
+    at the device check of this GPU-less machine).  dab_rs is written byte by
+    byte and may sit at any offset."""
+    from mxfp8_mixture_experts_gb300 import _lib
+    base = 1 << 20
+    f = C.c_void_p(base)
+    args = lambda dab_rs, dab_cs, h_cs: (f, f, 256, 64, f, dab_rs, f, dab_cs, f, h_cs, None, None)
+    for off in (1, 2, 3):
+        assert lib.moe_swiglu_bwd(*args(f, C.c_void_p(base + off), f)) == _lib.MX_ERR_ALIGNMENT
+        assert lib.moe_swiglu_bwd(*args(f, f, C.c_void_p(base + off))) == _lib.MX_ERR_ALIGNMENT
+    ok = {_lib.MX_ERR_UNSUPPORTED_DEVICE, _lib.MX_ERR_CUDA}
+    assert lib.moe_swiglu_bwd(*args(C.c_void_p(base + 1), C.c_void_p(base + 4), C.c_void_p(base + 8))) in ok
 
 
 def test_package_imports_and_fails_loudly_without_library(tmp_path):

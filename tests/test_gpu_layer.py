@@ -227,7 +227,7 @@ def test_layer_end_to_end_vs_independent_oracle(dev):
         e = rel_frob(got[n], refq[n])
         sqnr = 10 * np.log10(np.sum(refr[n] ** 2) / np.sum((refr[n] - got[n]) ** 2))
         print(f"{n}: rel err vs MXFP8 oracle {e:.2e}, SQNR vs unquantized layer {sqnr:.1f} dB")
-        assert e < 1e-2, n
+        assert e < 1e-3, n
         assert sqnr > 20, n
 
 
@@ -260,7 +260,7 @@ def test_layer_with_empty_experts(dev):
     ref = {"out": fq["out"], "dX": bq["dX"], "dW13": np.concatenate([bq["dW1"], bq["dW3"]], 2)[[0, 2, 3]],
            "dW2": bq["dW2"][[0, 2, 3]]}
     for n in got:
-        assert rel_frob(got[n], ref[n]) < 1e-2, n
+        assert rel_frob(got[n], ref[n]) < 1e-3, n
 
 
 @pytest.mark.parametrize("rows,F", [(128, 96), (384, 32), (256, 160)])
@@ -283,6 +283,71 @@ def test_swiglu_bwd_standalone(dev, rows, F):
     quant_mismatches_outside_margin(u8(dab_cq), mx.unswizzle_scales(u8(dab_cs), 2 * F, rows // 32), dab.T.copy(),
                                     "dab cols")
     quant_mismatches_outside_margin(u8(h_cq), mx.unswizzle_scales(u8(h_cs), F, rows // 32), h.T.copy(), "h cols")
+
+
+def test_row_limit_skips_rows_past_the_groups(dev):
+    """moe_swiglu_bwd and moe_gather_quant with a device row limit (the layer
+    passes offsets[E], where the routed rows end): every output of a row
+    below the limit is bit-identical to the unlimited call, and nothing at or
+    past it is written (buffers pre-filled with 0xAB keep that byte)."""
+    import mxfp8_mixture_experts_gb300 as m
+    L = m.lib()
+    s = torch.cuda.current_stream(dev).cuda_stream
+    R, F, P = 512, 256, 256
+    g = workloads.generator(21, dev)
+    ab = workloads.randn_bf16((R, 2 * F), 1.0, g, dev)
+    dh = torch.randn((R, F), generator=g, device=dev)
+    lim = torch.tensor([P], dtype=torch.int32, device=dev)
+    sb = lambda r, c: m.mx_scale_bytes(r, c, m.MX_SCALE_SWIZZLED)
+    shapes = {"dab_rq": R * 2 * F, "dab_rs": sb(R, 2 * F), "dab_cq": 2 * F * R, "dab_cs": sb(2 * F, R),
+              "h_cq": F * R, "h_cs": sb(F, R)}
+
+    def run(limit):
+        o = {n: torch.full((k,), 0xAB, dtype=torch.uint8, device=dev) for n, k in shapes.items()}
+        assert L.moe_swiglu_bwd(dh.data_ptr(), ab.data_ptr(), R, F, *(o[n].data_ptr() for n in shapes),
+                                None if limit is None else limit.data_ptr(), s) == 0
+        return o
+
+    full, part = run(None), run(lim)
+    torch.cuda.synchronize()
+
+    def col_scale_mask(rows, cols_blocks):
+        rr, cc = np.meshgrid(np.arange(rows), np.arange(cols_blocks), indexing="ij")
+        mask = np.zeros(sb(rows, cols_blocks * 32), bool)
+        mask[mx.swizzled_offset(rr, cc, cols_blocks)[cc < P // 32]] = True
+        return mask
+
+    f, p_ = {n: u8(t) for n, t in full.items()}, {n: u8(t) for n, t in part.items()}
+    below = {"dab_rq": np.arange(R * 2 * F) < P * 2 * F,
+             "dab_rs": np.arange(sb(R, 2 * F)) < sb(P, 2 * F),
+             "dab_cq": (np.arange(2 * F * R) % R) < P, "dab_cs": col_scale_mask(2 * F, R // 32),
+             "h_cq": (np.arange(F * R) % R) < P, "h_cs": col_scale_mask(F, R // 32)}
+    for n in shapes:
+        assert np.array_equal(p_[n][below[n]], f[n][below[n]]), n
+        assert np.all(p_[n][~below[n]] == 0xAB), n
+
+    # gather + quantize, both layouts
+    T, H, k = 300, 256, 1
+    x = workloads.randn_bf16((T, H), 1.0, g, dev)
+    src = torch.full((R,), -1, dtype=torch.int32, device=dev)
+    src[:T] = torch.arange(T, dtype=torch.int32, device=dev)
+    shapes = {"q_row": R * H, "s_row": sb(R, H), "q_col": H * R, "s_col": sb(H, R)}
+
+    def gq(limit):
+        o = {n: torch.full((k_,), 0xAB, dtype=torch.uint8, device=dev) for n, k_ in shapes.items()}
+        assert L.moe_gather_quant(x.data_ptr(), None, src.data_ptr(), T, H, k, R, m.MX_MODE_BOTH,
+                                  *(o[n].data_ptr() for n in shapes), None if limit is None else limit.data_ptr(),
+                                  s) == 0
+        return o
+
+    full, part = gq(None), gq(lim)
+    torch.cuda.synchronize()
+    f, p_ = {n: u8(t) for n, t in full.items()}, {n: u8(t) for n, t in part.items()}
+    below = {"q_row": np.arange(R * H) < P * H, "s_row": np.arange(sb(R, H)) < sb(P, H),
+             "q_col": (np.arange(H * R) % R) < P, "s_col": col_scale_mask(H, R // 32)}
+    for n in shapes:
+        assert np.array_equal(p_[n][below[n]], f[n][below[n]]), n
+        assert np.all(p_[n][~below[n]] == 0xAB), n
 
 
 def test_layer_empty_batch(dev):
@@ -376,14 +441,15 @@ def _sampled_scales(s_flat, rows, ncols):
     return s_flat[mx.swizzled_offset(rr, cc, cb)]
 
 
-def _dot_check(got, terms, what, rel=1e-4):
-    """fp32-accumulated dot products against the fp64 sum of the same terms:
-    |got - ref| <= rel * sum |terms| (a bound that holds without cancellation
-    assumptions)."""
-    ref = terms.sum(axis=-1)
-    bound = rel * np.abs(terms).sum(axis=-1) + 1e-30
-    bad = np.abs(np.asarray(got, np.float64) - ref) > bound
-    assert not bad.any(), f"{what}: {int(bad.sum())} sampled entries off; first {np.argwhere(bad)[:3].tolist()}"
+def _frob_check(got, ref, what, min_entries=64):
+    """fp32 GEMM outputs on sampled entries against the fp64 products of the
+    same dequantized operands: relative Frobenius error over the sample at
+    most TOL, the bound the full matrices are held to."""
+    got = np.asarray(got, np.float64)
+    assert got.shape == ref.shape and got.size >= min_entries, (what, got.shape, ref.shape)
+    e = rel_frob(got, ref)
+    print(f"{what}: rel Frobenius {e:.2e} over {got.size} sampled entries")
+    assert e <= TOL, f"{what}: rel Frobenius {e:.3e} > {TOL}"
 
 
 def test_layer_full_size_sampled(dev):
@@ -478,10 +544,13 @@ def test_layer_full_size_sampled(dev):
     # dgrad2: dh entries on the GPU's dY and the row-quantized W2 row
     dyhat = _deq_sampled(_rows_u8(s["dy_rq"], rows), dys_flat, rows, H)
     dh_rows = s["dh"][torch.as_tensor(rows, device=dev)].cpu().numpy()
-    for f in g.choice(F, 8, replace=False):
+    fsel = g.choice(F, 8, replace=False)
+    dh_ref = np.zeros((len(rows), len(fsel)))
+    for i, f in enumerate(fsel):
         wrow = np.stack([mx.bf16_to_f64(workloads.bf16_bits(W2b[e, f, :].contiguous())) for e in e_of[rows]])
         wq, ws_ = mx.quantize_rows(wrow)
-        _dot_check(dh_rows[:, f], dyhat * mx.dequantize_rows(wq, ws_), f"dh col {f}")
+        dh_ref[:, i] = (dyhat * mx.dequantize_rows(wq, ws_)).sum(axis=1)
+    _frob_check(dh_rows[:, fsel], dh_ref, "dh")
 
     # SwiGLU backward on the GPU's dh, a, b: row-quantized [da|db] (teacher forced)
     da, db = moe.swiglu_bwd(dh_rows.astype(np.float64), abv[:, :F], abv[:, F:])
@@ -489,23 +558,27 @@ def test_layer_full_size_sampled(dev):
     quant_mismatches_outside_margin(_rows_u8(s["dab_rq"], rows), _sampled_scales(u8(s["dab_rs"]), rows, 2 * F),
                                     dab, "dab rows")
 
-    # wgrad2 / wgrad1 on the GPU's column-quantized operands, one expert:
+    # wgrad2 / wgrad1 on the GPU's column-quantized operands, for the expert
+    # with the most routed rows and the one with the fewest (non-empty), 8 x 8
+    # sampled entries of each weight gradient per expert:
     # dW2[e, f, c] = sum over its tokens of h[t, f] dY[t, c];
     # dW13[e, c, j] = sum over its tokens of xp[t, c] [da|db][t, j]
-    e = int(np.argmax(np.diff(off)))
-    lo, hi = int(off[e]), int(off[e + 1])
-    fs, cs, js = g.choice(F, 4, replace=False), g.choice(H, 4, replace=False), g.choice(2 * F, 4, replace=False)
+    sizes = np.diff(off)
+    live = np.flatnonzero(sizes > 0)
+    for e in sorted({int(live[np.argmax(sizes[live])]), int(live[np.argmin(sizes[live])])}):
+        lo, hi = int(off[e]), int(off[e + 1])
+        fs, cs, js = g.choice(F, 8, replace=False), g.choice(H, 8, replace=False), g.choice(2 * F, 8, replace=False)
 
-    def col_rows(qname, sname, which):
-        q = _rows_u8(s[qname], which)                                  # [n, R] transposed rows
-        return _deq_sampled(q, u8(s[sname]), which, R)[:, lo:hi]
+        def col_rows(qname, sname, which):
+            q = _rows_u8(s[qname], which)                                  # [n, R] transposed rows
+            return _deq_sampled(q, u8(s[sname]), which, R)[:, lo:hi]
 
-    hT, dyT = col_rows("h_cq", "h_cs", fs), col_rows("dy_cq", "dy_cs", cs)
-    got = s["dW2"][e][torch.as_tensor(fs, device=dev)][:, torch.as_tensor(cs, device=dev)].cpu().numpy()
-    _dot_check(got, hT[:, None, :] * dyT[None, :, :], f"dW2[{e}]")
-    xT, dabT = col_rows("xp_cq", "xp_cs", cs), col_rows("dab_cq", "dab_cs", js)
-    got = s["dW13"][e][torch.as_tensor(cs, device=dev)][:, torch.as_tensor(js, device=dev)].cpu().numpy()
-    _dot_check(got, xT[:, None, :] * dabT[None, :, :], f"dW13[{e}]")
+        hT, dyT = col_rows("h_cq", "h_cs", fs), col_rows("dy_cq", "dy_cs", cs)
+        got = s["dW2"][e][torch.as_tensor(fs, device=dev)][:, torch.as_tensor(cs, device=dev)].cpu().numpy()
+        _frob_check(got, hT @ dyT.T, f"dW2[{e}] ({hi - lo} rows)")
+        xT, dabT = col_rows("xp_cq", "xp_cs", cs), col_rows("dab_cq", "dab_cs", js)
+        got = s["dW13"][e][torch.as_tensor(cs, device=dev)][:, torch.as_tensor(js, device=dev)].cpu().numpy()
+        _frob_check(got, xT @ dabT.T, f"dW13[{e}] ({hi - lo} rows)")
 
     # dgrad1: dxp entries on the GPU's row-quantized [da|db] and the row-quantized W13 row
     dabhat = _deq_sampled(_rows_u8(s["dab_rq"], rows), u8(s["dab_rs"]), rows, 2 * F)
