@@ -80,6 +80,56 @@ def test_small_integer_operands_bit_exact(dev, sizes, N, K):
     assert_bytes_equal(C[:P].view(np.uint32), ref[:P].astype(np.float32).view(np.uint32), "C")
 
 
+def _run_wgrad(dev, Xq, Xs, Yq, Ys, sizes, M_cap, N, K):
+    import mxfp8_mixture_experts_gb300 as m
+    E = len(sizes)
+    off = torch.from_numpy(_offsets(sizes)).to(dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    C = m.mx_grouped_gemm(m.MX_GEMM_WGRAD, to_dev_u8(Xq, dev), to_dev_u8(Xs, dev), to_dev_u8(Yq, dev),
+                          to_dev_u8(Ys, dev), off, E, M_cap, N, K, m.MX_OUT_F32, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    return C.cpu().numpy()
+
+
+# K = 256: the 256-wide part alone; 512: 256 + 128, then a 128-wide part in
+# the first accumulator; 1280: three full 384-column super-tiles and a 128 rest
+WGRAD_SHAPES = [([256, 0, 384], 256, 256), ([128, 256], 512, 512), ([384, 128, 0, 256], 256, 1280)]
+
+
+@pytest.mark.parametrize("sizes,N,K", WGRAD_SHAPES)
+def test_wgrad_small_integer_operands_bit_exact(dev, sizes, N, K):
+    """Token-grouped contraction on codes {0, +-1/2, +-1, +-2} with unit
+    scales: every product and partial sum is exact in fp32."""
+    g = np.random.default_rng(sum(sizes) + N + K + 1)
+    E = len(sizes)
+    M_cap = sum(sizes) + 128
+    Xq = g.choice(SMALL_CODES, (N, M_cap))
+    Yq = g.choice(SMALL_CODES, (K, M_cap))
+    Xs = mx.swizzle_scales(np.full((N, M_cap // 32), 127, np.uint8))
+    Ys = mx.swizzle_scales(np.full((K, M_cap // 32), 127, np.uint8))
+    C = _run_wgrad(dev, Xq, Xs, Yq, Ys, sizes, M_cap, N, K)
+    ref = moe.grouped_gemm_tokens(_deq(Xq, Xs), _deq(Yq, Ys), _offsets(sizes))
+    assert_bytes_equal(C.view(np.uint32), ref.astype(np.float32).view(np.uint32), "dW")
+
+
+@pytest.mark.parametrize("sizes,N,K", WGRAD_SHAPES)
+def test_wgrad_scale_layout_bit_exact(dev, sizes, N, K):
+    """All-ones codes with every (row, 32-token block) scale drawn from
+    2^-3..2^3 on both operands: each output is a sum of powers of two, exact
+    in fp32, so a scale chunk fetched for the wrong rows or tokens shows."""
+    g = np.random.default_rng(sum(sizes) + N + K + 2)
+    E = len(sizes)
+    M_cap = sum(sizes) + 128
+    Xq = np.full((N, M_cap), 0x38, np.uint8)
+    Yq = np.full((K, M_cap), 0x38, np.uint8)
+    Xs = mx.swizzle_scales(g.integers(124, 131, (N, M_cap // 32)).astype(np.uint8))
+    Ys = mx.swizzle_scales(g.integers(124, 131, (K, M_cap // 32)).astype(np.uint8))
+    C = _run_wgrad(dev, Xq, Xs, Yq, Ys, sizes, M_cap, N, K)
+    ref = moe.grouped_gemm_tokens(_deq(Xq, Xs), _deq(Yq, Ys), _offsets(sizes))
+    assert_bytes_equal(C.view(np.uint32), ref.astype(np.float32).view(np.uint32), "dW")
+
+
 def test_scale_layout_bit_exact(dev):
     """All-ones data, every (row, 32-block) scale drawn from 2^-3..2^3: C is a
     sum of K/32 powers of two, exact in fp32; a misplaced scale shows."""
@@ -291,3 +341,4 @@ def test_one_cta_kernel_variant():
                         "-m", "gpu", "-k", "not one_cta and not full_size", "-p", "no:cacheprovider"],
                        cwd=root, env=env, capture_output=True, text=True, timeout=600)
     assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-2000:]
+
