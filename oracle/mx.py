@@ -248,6 +248,46 @@ def quantize_margins(x: np.ndarray):
 
 
 # ----------------------------------------------------------------------------
+# Row-max-scaled FP8: one scale per row (a comparison to MX block scaling)
+# ----------------------------------------------------------------------------
+def quantize_rowmax(x: np.ndarray):
+    """One fp32 scale per row instead of one E8M0 scale per 32 elements.
+
+    NVIDIA/TransformerEngine issue "FP8 significantly slow down when scaling
+    up to 1000+ GPUs" describes casting a row to FP8 after computing its
+    row-max and dividing by it, and multiplying the row-max back after the
+    GEMM.  Readings (the issue gives no formula):
+    * the row-max is max |x| over the row;
+    * the scale maps it onto E4M3's largest finite value:
+      s = fp32(amax / 448), one IEEE fp32 division;
+    * each element is q = E4M3(fp32(x / s)) (IEEE fp32 division, then round to
+      nearest even with saturation at +-448); x is bf16, exact in fp32;
+    * the decoded value is q * s;
+    * a row of zeros gets s = 1 (its elements encode as signed zeros); a row
+      holding NaN or Inf gets s = NaN and every byte 0x7F.
+    The fp32 steps are the precision in which the GPU takes the same
+    decisions (one division each), so bytes and scales compare bit for bit.
+
+    Returns (q uint8 same shape, s float32 [..., rows])."""
+    x = np.asarray(x, dtype=np.float64)
+    fin = np.isfinite(x)
+    bad = ~np.all(fin, axis=-1)
+    amax = np.abs(np.where(fin, x, 0.0)).max(axis=-1)
+    s = (amax.astype(np.float32) / np.float32(E4M3_MAX)).astype(np.float32)
+    s = np.where(amax == 0, np.float32(1.0), s).astype(np.float32)
+    r = (np.where(fin, x, 0.0).astype(np.float32) / s[..., None]).astype(np.float32)
+    q = e4m3_encode(r.astype(np.float64))
+    q = np.where(bad[..., None], np.uint8(E4M3_NAN), q).astype(np.uint8)
+    s = np.where(bad, np.float32(np.nan), s).astype(np.float32)
+    return q, s
+
+
+def dequantize_rowmax(q: np.ndarray, s: np.ndarray) -> np.ndarray:
+    """Row-max-scaled FP8 bytes -> values: element value times its row scale."""
+    return e4m3_decode(q) * np.asarray(s, np.float64)[..., None]
+
+
+# ----------------------------------------------------------------------------
 # Scale layout for the block-scaled tensor-core MMA
 # ----------------------------------------------------------------------------
 def swizzled_offset(r, c, cols: int):
