@@ -341,6 +341,48 @@ def _dequant_bench(dev, iters=20):
             "l2": "flushed (256 MiB write) before each launch"}
 
 
+def _rowmax_bench(dev, iters=20):
+    """Row-max-scaled FP8 on the quantize workload (bf16 [16384, 7168]): the
+    quantize kernel's GB/s after an L2 flush, and the accuracy of both schemes
+    on the same data as SQNR of the decoded values against the bf16 input
+    (MX: 32-element blocks with E8M0 scales, decoded by mx_dequantize; row
+    max: E4M3 times the row's fp32 scale, decoded with torch for the
+    comparison only)."""
+    import mxfp8_mixture_experts_gb300 as m
+    R, C = workloads.QUANTIZE_SHAPE
+    x = workloads.quantize_input(R, C, seed=0, device=dev)
+    L = m.lib()
+    q = torch.empty((R, C), dtype=torch.uint8, device=dev)
+    sc = torch.empty(R, dtype=torch.float32, device=dev)
+    s = torch.cuda.current_stream(dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    times = []
+    for i in range(iters + 3):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        code = L.fp8_quantize_rowmax(x.data_ptr(), R, C, q.data_ptr(), sc.data_ptr(), s.cuda_stream)
+        e1.record(s)
+        assert code == 0
+        torch.cuda.synchronize()
+        if i >= 3:
+            times.append(e0.elapsed_time(e1) * 1e-3)
+    t = statistics.median(times)
+    nbytes = R * C * 2 + R * C + R * 4
+    xf = x.float()
+    sig = (xf.double() ** 2).sum()
+    rm = q.view(torch.float8_e4m3fn).float() * sc[:, None]
+    mq, ms, _, _ = m.mx_quantize(x, m.MX_MODE_ROW, m.MX_SCALE_PLAIN)
+    mxd = torch.empty((R, C), dtype=torch.float32, device=dev)
+    assert L.mx_dequantize(mq.data_ptr(), ms.data_ptr(), 1, R, C, 0, 1, mxd.data_ptr(), s.cuda_stream) == 0
+    torch.cuda.synchronize()
+    sqnr = lambda d: float(10 * torch.log10(sig / ((xf - d).double() ** 2).sum()))
+    return {"GB/s": nbytes / t / 1e9, "us": t * 1e6, "bytes": nbytes, "sqnr_db_rowmax": sqnr(rm),
+            "sqnr_db_mx": sqnr(mxd), "l2": "flushed (256 MiB write) before each launch",
+            "what": "one fp32 scale per row (amax / 448), E4M3 elements; SQNR of decoded values vs the bf16 input, "
+                    "beside MXFP8's on the same data"}
+
+
 def _permute_bench(dev, iters=10):
     """Token permute / unpermute workload: T=32768 tokens, H=5120, E=16
     experts, top-4 Zipf(1.1) expert choice over 14 live experts (two empty).
@@ -630,7 +672,8 @@ def main():
     ap.add_argument("--T", type=int, default=None, help="override the token count (profiling of small cases)")
     ap.add_argument("--E", type=int, default=None, help="override the expert count (profiling of small cases)")
     ap.add_argument("--k", type=int, default=None, help="override top-k (a variant; the bench line is top-1)")
-    ap.add_argument("--workload", default="layer", choices=["layer", "gemm", "quantize", "dequantize", "permute"],
+    ap.add_argument("--workload", default="layer",
+                    choices=["layer", "gemm", "quantize", "dequantize", "permute", "rowmax"],
                     help="layer: the full training step (the bench line); gemm / quantize / dequantize / "
                          "permute: one kernel family on its own workload, for profiling")
     args = ap.parse_args()
@@ -644,6 +687,8 @@ def main():
             r = _permute_bench(dev, max(args.steps, 1))
         elif args.workload == "dequantize":
             r = _dequant_bench(dev, max(args.steps, 1))
+        elif args.workload == "rowmax":
+            r = _rowmax_bench(dev, max(args.steps, 1))
         else:
             r = _quant_bench(dev, max(args.steps, 1))
         print(json.dumps({"workload": args.workload, **r}))
@@ -738,7 +783,7 @@ def main():
     gemm_time = sum(avg[n] for n in gf)
     gemm_tflops = total_flops / gemm_time / 1e12
 
-    quant = perm = deq = gemm = tiny = bf16 = None
+    quant = perm = deq = gemm = tiny = bf16 = rowmax = None
     if not args.no_quant:
         quant = _quant_bench(dev)
         quant["frac"] = quant["GB/s"] / hbm
@@ -749,6 +794,8 @@ def main():
             perm[key]["frac"] = perm[key]["GB/s"] / hbm
         deq = _dequant_bench(dev)
         deq["frac"] = deq["GB/s"] / hbm
+        rowmax = _rowmax_bench(dev)
+        rowmax["frac"] = rowmax["GB/s"] / hbm
         gemm = _gemm_bench(dev, args)
         for op in ("fwd", "dgrad", "wgrad"):
             gemm[op]["frac_burst"] = gemm[op]["TFLOP/s"] / pk["burst"]
@@ -786,6 +833,7 @@ def main():
             "quantize": quant,
             "permute": perm,
             "dequantize": deq,
+            "rowmax_fp8": rowmax,
             "grouped_gemm": gemm,
             "tiny_layer": tiny,
             "bf16_layer_context": bf16,

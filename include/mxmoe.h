@@ -176,6 +176,26 @@ mx_status mx_dequantize(const uint8_t *q, const uint8_t *s, int64_t batch, int64
                         mx_stream stream);
 
 /* ------------------------------------------------------------------------ */
+/* Row-max-scaled FP8, for comparison with MX block scaling                  */
+/* (NVIDIA/TransformerEngine issue "FP8 significantly slow down when scaling */
+/* up to 1000+ GPUs": compute the row max, divide by it before the cast to   */
+/* FP8, multiply it back after the GEMM)                                     */
+/* ------------------------------------------------------------------------ */
+/*
+ * x: bf16 [rows, cols].  Per row: amax = max |x| over the row; the scale
+ * s = amax / 448 (one IEEE fp32 division: the row max lands on E4M3's
+ * largest finite value); each element becomes q = E4M3(x / s) (IEEE fp32
+ * division, round to nearest even, saturating at +-448).  x is decoded as
+ * E4M3(q) * s.  A zero row gets s = 1 (its elements encode as signed zeros);
+ * a row holding NaN or Inf gets s = NaN and every byte 0x7F.
+ * q: E4M3 [rows, cols]; row_scale: fp32 [rows].
+ * rows >= 0 (0: nothing to do; pointers may be NULL), cols % 16 == 0,
+ * cols <= 102400; x and q 16-byte aligned, row_scale 4-byte aligned.
+ */
+mx_status fp8_quantize_rowmax(const void *x, int64_t rows, int64_t cols, uint8_t *q,
+                              float *row_scale, mx_stream stream);
+
+/* ------------------------------------------------------------------------ */
 /* R: router (helper; the pages name no router -- top-k with softmax gate)   */
 /* ------------------------------------------------------------------------ */
 /*

@@ -22,7 +22,7 @@ from ._lib import (MX_GEMM_DGRAD, MX_GEMM_FWD, MX_GEMM_WGRAD, MX_MODE_BOTH, MX_M
 __all__ = [
     "lib", "MxError", "mx_quantize", "mx_dequantize", "mx_scale_bytes", "moe_route", "moe_rows_cap", "moe_permute_map",
     "moe_permute", "moe_unpermute", "mx_grouped_gemm", "moe_gemm1_swiglu", "moe_swiglu_bwd",
-    "moe_gather_quant", "moe_gate_grad", "mx_selftest_sigmoid", "MoELayerDims", "moe_layer_prep_weights", "moe_layer_fwd",
+    "moe_gather_quant", "moe_gate_grad", "mx_selftest_sigmoid", "fp8_quantize_rowmax", "MoELayerDims", "moe_layer_prep_weights", "moe_layer_fwd",
     "moe_layer_bwd", "moe_layer_workspace_size", "moe_layer_weights_size",
 ]
 
@@ -210,6 +210,18 @@ def moe_gather_quant(x: torch.Tensor, gate, src: torch.Tensor, k: int, mode: int
     _lib.check(lib().moe_gather_quant(_ptr(x), _ptr(gate), _ptr(src), T, H, k, R, mode, _ptr(q_row), _ptr(s_row),
                                       _ptr(q_col), _ptr(s_col), _ptr(row_limit), _stream(dev)), "moe_gather_quant")
     return q_row, s_row, q_col, s_col
+
+
+def fp8_quantize_rowmax(x: torch.Tensor):
+    """bf16 [rows, cols] -> (q uint8 [rows, cols] E4M3, row_scale fp32 [rows]):
+    one scale per row, amax / 448 (see fp8_quantize_rowmax in mxmoe.h)."""
+    _req(x, torch.bfloat16, "x")
+    rows, cols = x.shape
+    q = torch.empty((rows, cols), dtype=torch.uint8, device=x.device)
+    s = torch.empty(rows, dtype=torch.float32, device=x.device)
+    _lib.check(lib().fp8_quantize_rowmax(_ptr(x), rows, cols, _ptr(q), _ptr(s), _stream(x.device)),
+               "fp8_quantize_rowmax")
+    return q, s
 
 
 def mx_selftest_sigmoid(a: torch.Tensor):

@@ -42,6 +42,7 @@ SIGNATURES = {
     "mx_scale_bytes": (_i64, [_i64, _i64, _i32]),
     "mx_quantize": (_i32, [_p, _i64, _i64, _i64, _i32, _i32, _p, _p, _p, _p, _p]),
     "mx_dequantize": (_i32, [_p, _p, _i64, _i64, _i64, _i32, _i32, _p, _p]),
+    "fp8_quantize_rowmax": (_i32, [_p, _i64, _i64, _p, _p, _p]),
     "moe_route": (_i32, [_p, _i64, _i32, _i32, _p, _p, _p]),
     "moe_rows_cap": (_i64, [_i64, _i32, _i32]),
     "moe_permute_map_workspace_size": (_i64, [_i64, _i32, _i32]),

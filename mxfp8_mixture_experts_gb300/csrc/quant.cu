@@ -471,9 +471,114 @@ __global__ void __launch_bounds__(DQ_THREADS) k_dequantize(const uint8_t *__rest
   }
 }
 
+// ---------------------------------------------------------------------------
+// Row-max-scaled FP8 (see fp8_quantize_rowmax in mxmoe.h): one CTA per row.
+// The row is read once from HBM into shared memory (16-byte loads, 8 bf16
+// each) while each thread keeps the largest |x| bit pattern it saw; a warp
+// shuffle and a shared-memory step give the row's amax.  Then s = amax / 448
+// and every element x / s (the IEEE fp32 division the reading defines; see
+// rowmax_cast2 for how the kernel reaches the same bytes mostly without
+// dividing) is cast to E4M3 with round-to-nearest-even and saturation, 16
+// bytes per store.  HBM-bound: 2 bytes read and 1 written per element.
+// ---------------------------------------------------------------------------
+// E4M3(RN(x / s)) for the two bf16 values of a word, without a division in
+// the common case.  q = RN(x * y) with y = RN(1/s) lies within 3 * 2^-24 of
+// x / s (relative), and so does RN(x / s).  The E4M3 cast is monotone: when
+// both ends of the bracket q * (1 -+ 2^-21) cast to the same byte, so does
+// every value between them, RN(x / s) included.  Otherwise (about one element
+// in 2^16, where the bracket straddles an E4M3 rounding decision) the byte
+// comes from the IEEE division itself; so does every byte of a row whose
+// scale is so small (below 2^-128, a row of bf16 subnormals) that 1/s
+// overflows.
+__device__ __forceinline__ uint16_t rowmax_cast2(float a, float b, float s, float y) {
+  const float qa = a * y, qb = b * y;
+  constexpr float lo = 1.0f - 0x1p-21f, hi = 1.0f + 0x1p-21f;
+  const uint16_t c0 = cvt_e4m3x2(qa * lo, qb * lo), c1 = cvt_e4m3x2(qa * hi, qb * hi);
+  return c0 == c1 && y <= 0x1.fffffep127f ? c0 : cvt_e4m3x2(__fdiv_rn(a, s), __fdiv_rn(b, s));
+}
+__device__ __forceinline__ uint32_t rowmax_cast4(uint32_t w0, uint32_t w1, float s, float y) {
+  return (uint32_t)rowmax_cast2(bf16_lo(w0), bf16_hi(w0), s, y) |
+         ((uint32_t)rowmax_cast2(bf16_lo(w1), bf16_hi(w1), s, y) << 16);
+}
+
+constexpr int RM_THREADS = 128;
+constexpr int RM_BATCH = 4;  // 16-byte loads in flight per thread
+
+__global__ void __launch_bounds__(RM_THREADS) k_quantize_rowmax(const uint16_t *__restrict__ x, int64_t cols,
+                                                                uint8_t *__restrict__ q, float *__restrict__ scale) {
+  extern __shared__ __align__(16) uint4 rm_row[];  // cols / 8 chunks
+  __shared__ uint32_t red[RM_THREADS / 32];
+  const int tid = threadIdx.x;
+  const int64_t r = blockIdx.x;
+  const int nch = (int)(cols / 8);
+  const uint4 *src = reinterpret_cast<const uint4 *>(x + r * cols);
+  uint32_t am = 0;
+  for (int i0 = tid; i0 < nch; i0 += RM_THREADS * RM_BATCH) {
+    uint4 v[RM_BATCH];
+#pragma unroll
+    for (int b = 0; b < RM_BATCH; ++b) {  // every load of the batch issued before any use
+      const int i = i0 + b * RM_THREADS;
+      v[b] = i < nch ? __ldg(src + i) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int b = 0; b < RM_BATCH; ++b) {
+      const int i = i0 + b * RM_THREADS;
+      if (i < nch) rm_row[i] = v[b];
+      const uint32_t m = vmax_u16x2(vmax_u16x2(v[b].x & 0x7fff7fffu, v[b].y & 0x7fff7fffu),
+                                    vmax_u16x2(v[b].z & 0x7fff7fffu, v[b].w & 0x7fff7fffu));
+      am = max(am, max(m << 16, m & 0xffff0000u));  // as fp32 bit patterns
+    }
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) am = max(am, __shfl_xor_sync(0xffffffffu, am, o));
+  if ((tid & 31) == 0) red[tid >> 5] = am;
+  __syncthreads();
+  am = red[0];
+#pragma unroll
+  for (int w = 1; w < RM_THREADS / 32; ++w) am = max(am, red[w]);
+  const bool bad = am >= 0x7f800000u;  // NaN or Inf in the row
+  const float amax = __uint_as_float(am);
+  const float s = bad ? __uint_as_float(0x7fc00000u) : (am == 0 ? 1.0f : __fdiv_rn(amax, 448.0f));
+  const float y = __frcp_rn(s);  // correctly rounded 1 / s
+  if (tid == 0) scale[r] = s;
+  uint4 *dst = reinterpret_cast<uint4 *>(q + r * cols);
+  for (int i = tid; i < nch / 2; i += RM_THREADS) {
+    const uint4 a = rm_row[2 * i], b = rm_row[2 * i + 1];
+    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) o[j] = bad ? 0x7f7f7f7fu : rowmax_cast4(w[2 * j], w[2 * j + 1], s, y);
+    dst[i] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
 }  // namespace mxmoe
 
 using namespace mxmoe;
+
+extern "C" mx_status fp8_quantize_rowmax(const void *x, int64_t rows, int64_t cols, uint8_t *q, float *row_scale,
+                                         mx_stream stream) {
+  MX_HOST_CHECK(rows >= 0 && cols > 0, MX_ERR_INVALID_ARG);
+  MX_HOST_CHECK(rows == 0 || (x && q && row_scale), MX_ERR_INVALID_ARG);
+  MX_HOST_CHECK(cols % 16 == 0 && cols <= 102400 && rows < (int64_t)1 << 31, MX_ERR_SHAPE);
+  MX_HOST_CHECK(aligned16(x) && aligned16(q) && aligned4(row_scale), MX_ERR_ALIGNMENT);
+  mx_status st = check_device_cached();
+  if (st != MX_OK) return st;
+  if (rows == 0) return MX_OK;
+  const int smem = (int)(cols * 2);
+  if (smem > 48 * 1024) {
+    static int set[64];
+    int dev = 0;
+    MX_CUDA_TRY(cudaGetDevice(&dev));
+    if (dev >= 0 && dev < 64 && !set[dev]) {
+      MX_CUDA_TRY(cudaFuncSetAttribute(k_quantize_rowmax, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024));
+      set[dev] = 1;
+    }
+  }
+  k_quantize_rowmax<<<(unsigned)rows, RM_THREADS, smem, stream>>>(static_cast<const uint16_t *>(x), cols, q,
+                                                                   row_scale);
+  return launch_status();
+}
 
 extern "C" int64_t mx_scale_bytes(int64_t rows, int64_t cols, int32_t layout) {
   if (rows < 0 || cols < 0 || cols % 32) return -1;

@@ -97,6 +97,11 @@ def test_host_side_argument_errors(lib):
         _lib.MX_ERR_SHAPE
     # route: k > E
     assert lib.moe_route(fake, 16, 4, 5, fake, fake, None) == _lib.MX_ERR_INVALID_ARG
+    # row-max FP8: cols not a multiple of 16, too wide, misaligned scale
+    assert lib.fp8_quantize_rowmax(fake, 4, 40, fake, fake, None) == _lib.MX_ERR_SHAPE
+    assert lib.fp8_quantize_rowmax(fake, 4, 102416, fake, fake, None) == _lib.MX_ERR_SHAPE
+    assert lib.fp8_quantize_rowmax(fake, 4, 64, fake, C.c_void_p((1 << 20) + 2), None) == _lib.MX_ERR_ALIGNMENT
+    assert lib.fp8_quantize_rowmax(None, 4, 64, fake, fake, None) == _lib.MX_ERR_INVALID_ARG
     # sigmoid self-test: negative count, null buffers
     assert lib.mx_selftest_sigmoid(fake, -1, fake, None) == _lib.MX_ERR_INVALID_ARG
     assert lib.mx_selftest_sigmoid(None, 4, fake, None) == _lib.MX_ERR_INVALID_ARG
