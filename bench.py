@@ -486,6 +486,8 @@ def _gemm_bench(dev, args):
     res["workload"] = (f"grouped GEMM: E={E}, {M} routed rows in Zipf(1.1) groups {sizes}, K={K}, N={N}; fwd and "
                        f"dgrad bf16 out, wgrad fp32 out")
     res["l2"] = "flushed (256 MiB write) before each launch"
+    del a_rq, a_rs, a_cq, a_cs, w_rq, w_rs, w_cq, w_cs, c_rq, c_rs, c_cq, c_cs, C, dA, dW
+    res["wgrad_splitk"] = _splitk_bench(dev, args)
     return res
 
 
@@ -591,6 +593,51 @@ def _bf16_layer_bench(dev, d, inp, steps, warmup):
             "what": "bf16 layer in plain PyTorch eager: torch.mm per expert (cuBLAS bf16, fp32 accumulation, bf16 "
                     "outputs incl. weight gradients), elementwise SwiGLU in fp32, index-based permute/combine; "
                     "context only, not part of the library"}
+
+
+def _splitk_bench(dev, args):
+    """Split-K wgrad (mx_grouped_gemm_wgrad_splitk) against the plain wgrad:
+    on the grouped-GEMM workload (E=8, 32768 tokens in Zipf groups, N=2048,
+    K=7168: 1792 output tiles, plenty for 74 CTA pairs) and on a few-tile
+    case (E=2, tokens 30720 + 2048, N=K=1024: 32 output tiles), each launch
+    after an L2 flush."""
+    import mxfp8_mixture_experts_gb300 as m
+    res = {}
+    cases = {"grouped_gemm_workload": (workloads.gemm_group_sizes(8, 32768, seed=0), 2048, 7168),
+             "few_tiles_E2_N1024_K1024": ([30720, 2048], 1024, 1024)}
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    s = torch.cuda.current_stream(dev)
+    g = workloads.generator(11, dev)
+    for name, (sizes, N, K) in cases.items():
+        E, M = len(sizes), sum(sizes)
+        off = torch.tensor(np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32), device=dev)
+        _, _, xq, xs = m.mx_quantize(workloads.randn_bf16((M, N), 1.0, g, dev), m.MX_MODE_COL, m.MX_SCALE_SWIZZLED)
+        _, _, yq, ys = m.mx_quantize(workloads.randn_bf16((M, K), 1.0, g, dev), m.MX_MODE_COL, m.MX_SCALE_SWIZZLED)
+        C = torch.empty((E, N, K), dtype=torch.float32, device=dev)
+        ws = torch.empty(int(m.lib().mx_wgrad_splitk_workspace_size(E, N, K, 4)), dtype=torch.uint8, device=dev)
+        flops = 2 * M * N * K
+        row = {}
+        for splits in (0, 1, 2, 4):
+            def fn():
+                if splits == 0:
+                    m.mx_grouped_gemm(m.MX_GEMM_WGRAD, xq, xs, yq, ys, off, E, M, N, K, m.MX_OUT_F32, out=C)
+                else:
+                    m.mx_grouped_gemm_wgrad_splitk(xq, xs, yq, ys, off, E, M, N, K, splits, out=C, ws=ws)
+            times = []
+            for i in range(max(args.warmup, 1) + max(args.steps, 1)):
+                flush.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(s)
+                fn()
+                e1.record(s)
+                torch.cuda.synchronize()
+                if i >= max(args.warmup, 1):
+                    times.append(e0.elapsed_time(e1) * 1e-3)
+            t = statistics.median(times)
+            row["plain" if splits == 0 else f"splits={splits}"] = {"us": t * 1e6, "TFLOP/s": flops / t / 1e12}
+        row["sizes"] = sizes
+        res[name] = row
+    return res
 
 
 def _cpu_baseline(d_full, seconds_hint=20.0):

@@ -327,6 +327,28 @@ mx_status mx_grouped_gemm(int32_t op, const uint8_t *A, const uint8_t *sA,
                           int64_t N, int64_t K, void *C, int32_t c_dtype,
                           int32_t *dev_status, mx_stream stream);
 
+/*
+ * Deterministic split-K weight gradient (a variant of MX_GEMM_WGRAD for
+ * skewed or few output tiles): the same C[e] as mx_grouped_gemm(WGRAD), with
+ * each group's tokens cut into `splits` 128-aligned chunks that separate
+ * CTA pairs contract, chunk s of group e covering its 128-token blocks
+ * [floor(n_e s / splits), floor(n_e (s+1) / splits)).  The partial products
+ * (fp32, in `ws`) are summed in the order s = 0, 1, ..., splits-1, so the
+ * result does not depend on scheduling; it differs from the unsplit call
+ * only by fp32 rounding of the partial sums (splits = 1: bit-identical).
+ * Operands as MX_GEMM_WGRAD; C fp32 [E, N, K].  1 <= splits <= 16,
+ * E * splits <= 1024, N % 256 == 0, K % 256 == 0, M_cap % 128 == 0.
+ * ws: device scratch of mx_wgrad_splitk_workspace_size(E, N, K, splits)
+ * bytes, 16-byte aligned (MX_ERR_WORKSPACE if smaller).
+ */
+int64_t mx_wgrad_splitk_workspace_size(int32_t E, int64_t N, int64_t K, int32_t splits);
+mx_status mx_grouped_gemm_wgrad_splitk(const uint8_t *A, const uint8_t *sA,
+                                       const uint8_t *B, const uint8_t *sB,
+                                       const int32_t *offsets, int32_t E, int64_t M_cap,
+                                       int64_t N, int64_t K, int32_t splits, void *ws,
+                                       int64_t ws_bytes, float *C, int32_t *dev_status,
+                                       mx_stream stream);
+
 /* ------------------------------------------------------------------------ */
 /* S: SwiGLU between the expert projections (forward fused into GEMM1)       */
 /* ------------------------------------------------------------------------ */

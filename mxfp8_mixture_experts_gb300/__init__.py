@@ -21,7 +21,7 @@ from ._lib import (MX_GEMM_DGRAD, MX_GEMM_FWD, MX_GEMM_WGRAD, MX_MODE_BOTH, MX_M
 
 __all__ = [
     "lib", "MxError", "mx_quantize", "mx_dequantize", "mx_scale_bytes", "moe_route", "moe_rows_cap", "moe_permute_map",
-    "moe_permute", "moe_unpermute", "mx_grouped_gemm", "moe_gemm1_swiglu", "moe_swiglu_bwd",
+    "moe_permute", "moe_unpermute", "mx_grouped_gemm", "mx_grouped_gemm_wgrad_splitk", "moe_gemm1_swiglu", "moe_swiglu_bwd",
     "moe_gather_quant", "moe_gate_grad", "mx_selftest_sigmoid", "fp8_quantize_rowmax", "MoELayerDims", "moe_layer_prep_weights", "moe_layer_fwd",
     "moe_layer_bwd", "moe_layer_workspace_size", "moe_layer_weights_size",
 ]
@@ -157,6 +157,24 @@ def mx_grouped_gemm(op: int, A, sA, B, sB, offsets, E: int, M_cap: int, N: int, 
         out = torch.empty(shape, dtype=dt, device=dev)
     _lib.check(lib().mx_grouped_gemm(op, _ptr(A), _ptr(sA), _ptr(B), _ptr(sB), _ptr(offsets), E, M_cap, N, K,
                                      _ptr(out), out_dtype, _ptr(dev_status), _stream(dev)), "mx_grouped_gemm")
+    return out
+
+
+def mx_grouped_gemm_wgrad_splitk(A, sA, B, sB, offsets, E: int, M_cap: int, N: int, K: int, splits: int,
+                                 out: torch.Tensor | None = None, ws: torch.Tensor | None = None,
+                                 dev_status: torch.Tensor | None = None):
+    """Deterministic split-K wgrad: C fp32 [E, N, K] (see include/mxmoe.h)."""
+    dev = A.device
+    need = int(lib().mx_wgrad_splitk_workspace_size(E, N, K, splits))
+    if need < 0:
+        raise ValueError("bad split-K sizes")
+    if ws is None:
+        ws = torch.empty(need, dtype=torch.uint8, device=dev)
+    if out is None:
+        out = torch.empty((E, N, K), dtype=torch.float32, device=dev)
+    _lib.check(lib().mx_grouped_gemm_wgrad_splitk(_ptr(A), _ptr(sA), _ptr(B), _ptr(sB), _ptr(offsets), E, M_cap, N,
+                                                  K, splits, _ptr(ws), ws.numel(), _ptr(out), _ptr(dev_status),
+                                                  _stream(dev)), "mx_grouped_gemm_wgrad_splitk")
     return out
 
 

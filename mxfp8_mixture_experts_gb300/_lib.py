@@ -51,6 +51,8 @@ SIGNATURES = {
     "moe_permute": (_i32, [_i32, _p, _p, _i64, _i64, _i32, _p, _p, _i64, _p, _p, _i32, _p]),
     "moe_unpermute": (_i32, [_p, _p, _p, _i64, _i64, _i32, _p, _p]),
     "mx_grouped_gemm": (_i32, [_i32, _p, _p, _p, _p, _p, _i32, _i64, _i64, _i64, _p, _i32, _p, _p]),
+    "mx_wgrad_splitk_workspace_size": (_i64, [_i32, _i64, _i64, _i32]),
+    "mx_grouped_gemm_wgrad_splitk": (_i32, [_p, _p, _p, _p, _p, _i32, _i64, _i64, _i64, _i32, _p, _i64, _p, _p, _p]),
     "moe_gemm1_swiglu": (_i32, [_p, _p, _p, _p, _p, _i32, _i64, _i64, _i64, _p, _p, _p, _p, _p]),
     "moe_swiglu_bwd": (_i32, [_p, _p, _i64, _i64, _p, _p, _p, _p, _p, _p, _p, _p]),
     "moe_gather_quant": (_i32, [_p, _p, _p, _i64, _i64, _i32, _i64, _i32, _p, _p, _p, _p, _p, _p]),

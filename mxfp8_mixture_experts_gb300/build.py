@@ -16,7 +16,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmxmoe.so")
-SOURCES = ["api.cu", "quant.cu", "route_permute.cu", "gemm.cu", "gemm_pair.cu", "layer.cu"]
+SOURCES = ["api.cu", "quant.cu", "route_permute.cu", "gemm.cu", "gemm_pair.cu", "splitk.cu", "layer.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O3",
          "--expt-relaxed-constexpr"]

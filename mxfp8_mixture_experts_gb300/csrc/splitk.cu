@@ -1,0 +1,101 @@
+// Deterministic split-K weight gradient: the token-grouped grouped GEMM with
+// each expert's tokens cut into `splits` chunks that separate CTA pairs
+// contract, then a fixed-order sum of the partial products.
+//
+// The contraction is the wgrad of the grouped GEMM ("1.5x faster MoE training
+// on Blackwell with MXFP8 kernels built from scratch", Key Questions Answered;
+// the workload's "wgrad quantized along the token dim"):
+//   C[e] = sum over the tokens r of group e of deq(A[:, r]) deq(B[:, r])^T.
+// The persistent wgrad kernel hands out output tiles; when an expert's output
+// has fewer tiles than there are CTA pairs (small N x K, or most tokens in
+// one expert), most of the GPU idles while a few pairs walk long token
+// ranges.  Splitting the tokens multiplies the tiles by `splits` and costs one
+// extra write and read of the fp32 partials.
+//
+//   1. k_split_offsets: virtual offsets over E * splits groups; chunk s of
+//      expert e covers tokens [off[e] + 128 * floor(n_e * s / splits),
+//      off[e] + 128 * floor(n_e * (s + 1) / splits)), n_e = 128-token blocks
+//      of the expert (chunks may be empty).
+//   2. The wgrad grouped GEMM on the virtual groups writes partial [e, s] to
+//      rows (e * splits + s) * N of the workspace: [E, splits, N, K] fp32.
+//   3. k_split_reduce: C[e] = ((P[e,0] + P[e,1]) + P[e,2]) + ..., fp32 adds in
+//      that order, so the result does not depend on scheduling.
+#include "common.cuh"
+
+namespace mxmoe {
+
+__global__ void k_split_offsets(const int32_t *__restrict__ off, int32_t E, int32_t splits, int64_t M_cap,
+                                int32_t *__restrict__ voff, int32_t *dev_status) {
+  for (int g = threadIdx.x; g <= E * splits; g += blockDim.x) {
+    if (g == E * splits) {
+      voff[g] = off[E];
+      continue;
+    }
+    const int e = g / splits, s = g % splits;
+    const int32_t lo = off[e], hi = off[e + 1];
+    if (hi < lo || (lo & 127) || (hi & 127) || hi > M_cap || lo < 0) {
+      set_status(dev_status, MX_ERR_DEVICE);
+      voff[g] = 0;  // the GEMM's own validation of the virtual offsets then skips all work
+      continue;
+    }
+    const int64_t n = (hi - lo) / 128;
+    voff[g] = lo + (int32_t)(128 * (n * s / splits));
+  }
+}
+
+// 4 fp32 per thread per step; total = E * N * K (a multiple of 4)
+__global__ void __launch_bounds__(256) k_split_reduce(const float4 *__restrict__ part, int64_t per_e4, int32_t E,
+                                                      int32_t splits, float4 *__restrict__ out) {
+  const int64_t total = per_e4 * E;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t e = i / per_e4, j = i % per_e4;
+    const float4 *p = part + (e * splits) * per_e4 + j;
+    float4 acc = __ldg(p);
+    for (int s = 1; s < splits; ++s) {
+      const float4 v = __ldg(p + s * per_e4);
+      acc.x = __fadd_rn(acc.x, v.x);
+      acc.y = __fadd_rn(acc.y, v.y);
+      acc.z = __fadd_rn(acc.z, v.z);
+      acc.w = __fadd_rn(acc.w, v.w);
+    }
+    out[i] = acc;
+  }
+}
+
+}  // namespace mxmoe
+
+using namespace mxmoe;
+
+extern "C" int64_t mx_wgrad_splitk_workspace_size(int32_t E, int64_t N, int64_t K, int32_t splits) {
+  if (E < 1 || N < 1 || K < 1 || splits < 1 || splits > 16) return -1;
+  return round_up(((int64_t)E * splits + 1) * 4, 256) + (int64_t)E * splits * N * K * 4;
+}
+
+extern "C" mx_status mx_grouped_gemm_wgrad_splitk(const uint8_t *A, const uint8_t *sA, const uint8_t *B,
+                                                  const uint8_t *sB, const int32_t *offsets, int32_t E,
+                                                  int64_t M_cap, int64_t N, int64_t K, int32_t splits, void *ws,
+                                                  int64_t ws_bytes, float *C, int32_t *dev_status,
+                                                  mx_stream stream) {
+  MX_HOST_CHECK(A && sA && B && sB && offsets && ws && C, MX_ERR_INVALID_ARG);
+  MX_HOST_CHECK(splits >= 1 && splits <= 16 && E >= 1 && (int64_t)E * splits <= 1024, MX_ERR_INVALID_ARG);
+  MX_HOST_CHECK(M_cap >= 0 && N > 0 && K > 0, MX_ERR_INVALID_ARG);
+  MX_HOST_CHECK(M_cap % 128 == 0 && N % 256 == 0 && K % 256 == 0, MX_ERR_SHAPE);
+  MX_HOST_CHECK(aligned16(ws) && aligned16(C), MX_ERR_ALIGNMENT);
+  MX_HOST_CHECK(ws_bytes >= mx_wgrad_splitk_workspace_size(E, N, K, splits), MX_ERR_WORKSPACE);
+  mx_status st = check_device_cached();
+  if (st != MX_OK) return st;
+  int32_t *voff = static_cast<int32_t *>(ws);
+  float *part = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + round_up(((int64_t)E * splits + 1) * 4, 256));
+  k_split_offsets<<<1, 256, 0, stream>>>(offsets, E, splits, M_cap, voff, dev_status);
+  st = launch_status();
+  if (st != MX_OK) return st;
+  st = mx_grouped_gemm(MX_GEMM_WGRAD, A, sA, B, sB, voff, E * splits, M_cap, N, K, part, MX_OUT_F32, dev_status,
+                       stream);
+  if (st != MX_OK) return st;
+  const int64_t per_e4 = N * K / 4;
+  int64_t blocks = (per_e4 * E + 255) / 256;
+  if (blocks > 152 * 16) blocks = 152 * 16;
+  k_split_reduce<<<(unsigned)blocks, 256, 0, stream>>>(reinterpret_cast<const float4 *>(part), per_e4, E, splits,
+                                                       reinterpret_cast<float4 *>(C));
+  return launch_status();
+}

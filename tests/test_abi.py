@@ -102,6 +102,18 @@ def test_host_side_argument_errors(lib):
     assert lib.fp8_quantize_rowmax(fake, 4, 102416, fake, fake, None) == _lib.MX_ERR_SHAPE
     assert lib.fp8_quantize_rowmax(fake, 4, 64, fake, C.c_void_p((1 << 20) + 2), None) == _lib.MX_ERR_ALIGNMENT
     assert lib.fp8_quantize_rowmax(None, 4, 64, fake, fake, None) == _lib.MX_ERR_INVALID_ARG
+    # split-K wgrad: splits out of range, E * splits > 1024, workspace too small
+    big = lib.mx_wgrad_splitk_workspace_size(4, 256, 256, 2)
+    assert big == 256 + 4 * 2 * 256 * 256 * 4
+    assert lib.mx_wgrad_splitk_workspace_size(4, 256, 256, 17) == -1
+    assert lib.mx_grouped_gemm_wgrad_splitk(fake, fake, fake, fake, fake, 4, 256, 256, 256, 0, fake, big, fake, None,
+                                            None) == _lib.MX_ERR_INVALID_ARG
+    assert lib.mx_grouped_gemm_wgrad_splitk(fake, fake, fake, fake, fake, 512, 256, 256, 256, 4, fake, 1 << 40, fake,
+                                            None, None) == _lib.MX_ERR_INVALID_ARG
+    assert lib.mx_grouped_gemm_wgrad_splitk(fake, fake, fake, fake, fake, 4, 256, 256, 256, 2, fake, big - 1, fake,
+                                            None, None) == _lib.MX_ERR_WORKSPACE
+    assert lib.mx_grouped_gemm_wgrad_splitk(fake, fake, fake, fake, fake, 4, 256, 256, 384, 2, fake, 1 << 40, fake,
+                                            None, None) == _lib.MX_ERR_SHAPE
     # sigmoid self-test: negative count, null buffers
     assert lib.mx_selftest_sigmoid(fake, -1, fake, None) == _lib.MX_ERR_INVALID_ARG
     assert lib.mx_selftest_sigmoid(None, 4, fake, None) == _lib.MX_ERR_INVALID_ARG

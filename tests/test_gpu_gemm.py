@@ -342,3 +342,46 @@ def test_one_cta_kernel_variant():
                        cwd=root, env=env, capture_output=True, text=True, timeout=600)
     assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-2000:]
 
+
+
+@pytest.mark.parametrize("splits", [1, 2, 3, 5])
+def test_wgrad_splitk(dev, splits):
+    """Deterministic split-K wgrad: groups of 128 tokens (fewer 128-token
+    blocks than splits: some chunks empty), 0 and 1152 tokens; within 1e-4
+    of the oracle, zeros for the empty group, bit-identical across two runs,
+    and bit-identical to the unsplit GEMM when splits = 1; small-integer
+    operands give exact sums in any order, so there every split is
+    bit-exact."""
+    import mxfp8_mixture_experts_gb300 as m
+    g = np.random.default_rng(40 + splits)
+    sizes, N, K = [1152, 0, 128, 640], 256, 768
+    E, M_cap = len(sizes), sum(sizes) + 128
+    off = torch.from_numpy(_offsets(sizes)).to(dev)
+    X = mx.bf16_to_f64(mx.f64_to_bf16_bits(g.standard_normal((M_cap, N))))
+    Y = mx.bf16_to_f64(mx.f64_to_bf16_bits(g.standard_normal((M_cap, K))))
+    Xq, Xs = _quant_operand(X.T.copy())
+    Yq, Ys = _quant_operand(Y.T.copy())
+    args = [to_dev_u8(a, dev) for a in (Xq, Xs, Yq, Ys)]
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    C1 = m.mx_grouped_gemm_wgrad_splitk(*args, off, E, M_cap, N, K, splits, dev_status=st)
+    C2 = m.mx_grouped_gemm_wgrad_splitk(*args, off, E, M_cap, N, K, splits, dev_status=st)
+    ref_gpu = m.mx_grouped_gemm(m.MX_GEMM_WGRAD, *args, off, E, M_cap, N, K, m.MX_OUT_F32)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert torch.equal(C1.view(torch.int32), C2.view(torch.int32))
+    if splits == 1:
+        assert torch.equal(C1.view(torch.int32), ref_gpu.view(torch.int32))
+    ref = moe.grouped_gemm_tokens(_deq(Xq, Xs), _deq(Yq, Ys), _offsets(sizes))
+    C = C1.cpu().numpy()
+    assert np.all(C[1] == 0)
+    for e in (0, 2, 3):
+        assert rel_frob(C[e], ref[e]) <= TOL, e
+
+    Xq = g.choice(SMALL_CODES, (N, M_cap))
+    Yq = g.choice(SMALL_CODES, (K, M_cap))
+    Xs = mx.swizzle_scales(np.full((N, M_cap // 32), 127, np.uint8))
+    Ys = mx.swizzle_scales(np.full((K, M_cap // 32), 127, np.uint8))
+    C = m.mx_grouped_gemm_wgrad_splitk(*[to_dev_u8(a, dev) for a in (Xq, Xs, Yq, Ys)], off, E, M_cap, N, K, splits)
+    torch.cuda.synchronize()
+    ref = moe.grouped_gemm_tokens(_deq(Xq, Xs), _deq(Yq, Ys), _offsets(sizes))
+    assert_bytes_equal(C.cpu().numpy().view(np.uint32), ref.astype(np.float32).view(np.uint32), "split-K exact")
