@@ -176,21 +176,22 @@ def swiglu_bwd(dh, a, b):
 # ----------------------------------------------------------------------------
 # MoE layer (forward and backward)
 # ----------------------------------------------------------------------------
-def _q_rows(v, quant):
+def _q_rows(v, quant, fmt="e4m3"):
     """Operand as the GEMM sees it: the dequantized MX values (blocks along the
-    last axis) when ``quant``, else the values themselves."""
+    last axis, elements of format ``fmt``) when ``quant``, else the values
+    themselves."""
     if not quant:
         return np.asarray(v, np.float64)
-    q, s = mx.quantize_rows(v)
-    return mx.dequantize_rows(q, s)
+    q, s = mx.quantize_rows(v, fmt)
+    return mx.dequantize_rows(q, s, fmt)
 
 
-def _q_cols(v, quant):
+def _q_cols(v, quant, fmt="e4m3"):
     """Transposed operand, quantized along the first axis (blocks of 32 rows)."""
     if not quant:
         return np.swapaxes(np.asarray(v, np.float64), -1, -2)
-    q, s = mx.quantize_cols(v)
-    return mx.dequantize_rows(q, s)
+    q, s = mx.quantize_cols(v, fmt)
+    return mx.dequantize_rows(q, s, fmt)
 
 
 def _vals(v):
@@ -242,8 +243,13 @@ def layer_forward(x_bits, W1_bits, W3_bits, W2_bits, ids, gate, quant: bool = Tr
                 h=h, y=y, out=out, gate=gate, k=k, quant=quant)
 
 
-def layer_backward(fwd, x_bits, W1_bits, W3_bits, W2_bits, dOut_bits):
+def layer_backward(fwd, x_bits, W1_bits, W3_bits, W2_bits, dOut_bits, grad_fmt: str = "e4m3"):
     """MoE SwiGLU layer backward from the saved forward state ``fwd``.
+
+    grad_fmt: element format of the two gradient operands the backward
+    quantizes, the routed output gradient dY and [da|db] ("e4m3", or "e5m2",
+    the gradient option; the pages name only E4M3); weights, h and the
+    permuted input stay E4M3.
 
     Returns dX [T, H], dW1, dW3 [E, H, F], dW2 [E, F, H], d_gate [T, k], plus
     intermediates (dY, dh, da, db, dxp)."""
@@ -268,8 +274,9 @@ def layer_backward(fwd, x_bits, W1_bits, W3_bits, W2_bits, dOut_bits):
         d_gate[:, j] = np.sum(dOut * fwd["y"][rows[:, j]], axis=1)
 
     # GEMM2 backward: dh = dY W2^T (dgrad), dW2 = h^T dY (wgrad)
-    dh = grouped_gemm_rows(_q_rows(dY, quant), _q_rows(W2, quant), off)        # W2[e] [F, H], blocks along H
-    dW2 = grouped_gemm_tokens(_q_cols(fwd["h"], quant), _q_cols(dY, quant), off)  # [E, F, H]
+    g = grad_fmt
+    dh = grouped_gemm_rows(_q_rows(dY, quant, g), _q_rows(W2, quant), off)     # W2[e] [F, H], blocks along H
+    dW2 = grouped_gemm_tokens(_q_cols(fwd["h"], quant), _q_cols(dY, quant, g), off)  # [E, F, H]
 
     # SwiGLU backward
     da, db = swiglu_bwd(dh, fwd["a"], fwd["b"])
@@ -277,9 +284,9 @@ def layer_backward(fwd, x_bits, W1_bits, W3_bits, W2_bits, dOut_bits):
 
     # GEMM1 backward: dxp = dab W13^T (dgrad), dW13 = xp^T dab (wgrad)
     W13 = np.concatenate([W1, W3], axis=2)                                      # [E, H, 2F]
-    dxp = _round_bf16(grouped_gemm_rows(_q_rows(dab, quant), _q_rows(W13, quant), off), quant)
+    dxp = _round_bf16(grouped_gemm_rows(_q_rows(dab, quant, g), _q_rows(W13, quant), off), quant)
     xp_hi = permute_rows(x, src, k)                                             # bf16 values, permuted
-    dW13 = grouped_gemm_tokens(_q_cols(xp_hi, quant), _q_cols(dab, quant), off)  # [E, H, 2F]
+    dW13 = grouped_gemm_tokens(_q_cols(xp_hi, quant), _q_cols(dab, quant, g), off)  # [E, H, 2F]
 
     # combine the routed-row gradients back to tokens (unit weights)
     if quant:

@@ -45,6 +45,9 @@ BLOCK = 32            # elements that share one scale
 E4M3_MAX = 448.0      # largest finite E4M3FN value, 1.75 * 2^8
 E4M3_EMAX = 8         # exponent of E4M3's largest power of two
 E4M3_NAN = 0x7F
+E5M2_MAX = 57344.0    # largest finite E5M2 value, 1.75 * 2^15
+E5M2_EMAX = 15        # exponent of E5M2's largest power of two
+E5M2_NAN = 0x7F       # S.11111.11
 E8M0_NAN = 0xFF
 SCALE_EXP_MIN = -127
 SCALE_EXP_MAX = 127
@@ -146,6 +149,68 @@ def e4m3_ulp(code: np.ndarray) -> np.ndarray:
 
 
 # ----------------------------------------------------------------------------
+# E5M2 (OCP: bias 15, infinities S.11111.00, NaN S.11111.xx (xx != 0),
+# max 57344) -- the gradient option; the pages name only MXFP8 with E4M3
+# ----------------------------------------------------------------------------
+def e5m2_decode(code: np.ndarray) -> np.ndarray:
+    """E5M2 byte -> exact value (fp64); +-Inf and NaN as such."""
+    c = np.asarray(code, dtype=np.uint8).astype(np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    E = (c >> 2) & 0x1F
+    m = c & 0x3
+    sub = m * 2.0 ** -16                                  # E == 0: m * 2^-16
+    norm = (1.0 + m / 4.0) * np.ldexp(1.0, E - 15)        # 1 <= E <= 30
+    v = sign * np.where(E == 0, sub, norm)
+    v = np.where(E == 31, np.where(m == 0, sign * np.inf, np.nan), v)
+    return v
+
+
+def e5m2_encode(r: np.ndarray) -> np.ndarray:
+    """Exact reals -> E5M2 bytes: saturate |r| > 57344 (and +-Inf) to
+    +-57344, otherwise round to the nearest E5M2 value with ties to an even
+    mantissa; the sign of zero is kept; NaN -> 0x7F.
+
+    E5M2 holds 3 significant bits: in the binade [2^p, 2^(p+1)), p >= -14, the
+    values are multiples of 2^(p-2); below 2^-14 (subnormals) multiples of
+    2^-16."""
+    r = np.asarray(r, dtype=np.float64)
+    neg = np.signbit(r)
+    a = np.abs(r)
+    fin = np.isfinite(a)
+    _, ex = np.frexp(np.where(fin, a, 0.0))
+    p = np.maximum(ex - 1, -14)
+    q_exp = p - 2                                         # exponent of the grid step
+    n = np.rint(np.ldexp(np.where(fin, a, 0.0), -q_exp)).astype(np.int64)   # RNE onto the grid
+    carry = n == 8                                        # rounded into the next binade
+    n = np.where(carry, 4, n)
+    q_exp = np.where(carry, q_exp + 1, q_exp)
+    normal = n >= 4
+    biased = q_exp + 2 + 15                               # value = (1 + m/4) * 2^(q_exp+2)
+    code = np.where(normal, (biased << 2) | (n - 4), n)   # subnormal: E = 0, m = n
+    code = np.where(a > E5M2_MAX, 0x7B, code)             # also +-Inf
+    code = code | np.where(neg, 0x80, 0)
+    code = np.where(np.isnan(r), E5M2_NAN, code)
+    return code.astype(np.uint8)
+
+
+def e5m2_ulp(code: np.ndarray) -> np.ndarray:
+    """Spacing of the E5M2 grid at the magnitude of ``code`` (fp64)."""
+    c = np.asarray(code, dtype=np.uint8).astype(np.int64)
+    E = (c >> 2) & 0x1F
+    return np.where(E == 0, 2.0 ** -16, np.ldexp(1.0, np.maximum(E, 1) - 15 - 2))
+
+
+def _fmt(fmt):
+    """Element format of an MX block: (encode, decode, exponent of the largest
+    power of two, largest finite value)."""
+    if fmt == "e4m3":
+        return e4m3_encode, e4m3_decode, E4M3_EMAX, E4M3_MAX
+    if fmt == "e5m2":
+        return e5m2_encode, e5m2_decode, E5M2_EMAX, E5M2_MAX
+    raise ValueError(fmt)
+
+
+# ----------------------------------------------------------------------------
 # E8M0 scale
 # ----------------------------------------------------------------------------
 def e8m0_decode(byte: np.ndarray) -> np.ndarray:
@@ -163,59 +228,63 @@ def floor_log2(a: np.ndarray) -> np.ndarray:
 # ----------------------------------------------------------------------------
 # Block quantizer
 # ----------------------------------------------------------------------------
-def quantize_blocks(v: np.ndarray):
+def quantize_blocks(v: np.ndarray, fmt: str = "e4m3"):
     """Quantize the last axis of ``v`` (length 32, exact reals) as one MX block.
 
     1. amax = max |v_i|.
-    2. Scale exponent e = floor(log2 amax) - 8 (amax = 0: e = -127), clamped to
-       [-127, 127]; the scale byte is e + 127.
-    3. Each element is cast to E4M3 from v_i * 2^-e (exact), with RNE and
-       saturation.
+    2. Scale exponent e = floor(log2 amax) - emax (amax = 0: e = -127), with
+       emax = 8 for E4M3 and 15 for E5M2 (the exponent of the element type's
+       largest power of two), clamped to [-127, 127]; the scale byte is
+       e + 127.
+    3. Each element is cast to the element type from v_i * 2^-e (exact), with
+       RNE and saturation.
     A block holding NaN/Inf gets scale 0xFF and element bytes 0x7F.
 
     Returns (codes uint8 [..., 32], scale bytes uint8 [...])."""
+    encode, _, emax, _ = _fmt(fmt)
     v = np.asarray(v, dtype=np.float64)
     assert v.shape[-1] == BLOCK
     bad = ~np.all(np.isfinite(v), axis=-1)
     a = np.abs(np.where(np.isfinite(v), v, 0.0))
     amax = a.max(axis=-1)
-    e = np.where(amax > 0, floor_log2(np.where(amax > 0, amax, 1.0)) - E4M3_EMAX, SCALE_EXP_MIN)
+    e = np.where(amax > 0, floor_log2(np.where(amax > 0, amax, 1.0)) - emax, SCALE_EXP_MIN)
     e = np.clip(e, SCALE_EXP_MIN, SCALE_EXP_MAX)
     r = np.ldexp(np.where(np.isfinite(v), v, 0.0), -e[..., None])
-    codes = e4m3_encode(r)
+    codes = encode(r)
     scale = (e + 127).astype(np.uint8)
     codes = np.where(bad[..., None], np.uint8(E4M3_NAN), codes)
     scale = np.where(bad, np.uint8(E8M0_NAN), scale)
     return codes.astype(np.uint8), scale.astype(np.uint8)
 
 
-def quantize_rows(x: np.ndarray):
+def quantize_rows(x: np.ndarray, fmt: str = "e4m3"):
     """ROW mode: blocks of 32 along the last axis of a 2-D (or batched) array.
     Returns (q same shape uint8, s [..., cols/32] uint8)."""
     x = np.asarray(x, dtype=np.float64)
     *lead, cols = x.shape
     assert cols % BLOCK == 0, "ROW mode needs cols % 32 == 0"
-    q, s = quantize_blocks(x.reshape(*lead, cols // BLOCK, BLOCK))
+    q, s = quantize_blocks(x.reshape(*lead, cols // BLOCK, BLOCK), fmt)
     return q.reshape(*lead, cols), s
 
 
-def quantize_cols(x: np.ndarray):
+def quantize_cols(x: np.ndarray, fmt: str = "e4m3"):
     """COL mode: blocks of 32 consecutive rows of one column, output stored
     transposed, i.e. ROW mode applied to X^T (last two axes swapped)."""
     x = np.asarray(x, dtype=np.float64)
     assert x.shape[-2] % BLOCK == 0, "COL mode needs rows % 32 == 0"
-    return quantize_rows(np.swapaxes(x, -1, -2))
+    return quantize_rows(np.swapaxes(x, -1, -2), fmt)
 
 
-def dequantize_rows(q: np.ndarray, s: np.ndarray) -> np.ndarray:
+def dequantize_rows(q: np.ndarray, s: np.ndarray, fmt: str = "e4m3") -> np.ndarray:
     """MX bytes -> exact values: element value times its block's scale."""
+    _, decode, _, _ = _fmt(fmt)
     q = np.asarray(q, dtype=np.uint8)
     *lead, cols = q.shape
-    v = e4m3_decode(q).reshape(*lead, cols // BLOCK, BLOCK)
+    v = decode(q).reshape(*lead, cols // BLOCK, BLOCK)
     return (v * e8m0_decode(s)[..., None]).reshape(*lead, cols)
 
 
-def quantize_margins(x: np.ndarray):
+def quantize_margins(x: np.ndarray, fmt: str = "e4m3"):
     """How close each element's quantization decision is to flipping, for
     values computed in a different precision (fp32 on a GPU, fp64 here).
 
@@ -235,13 +304,15 @@ def quantize_margins(x: np.ndarray):
     p = floor_log2(safe)
     lo = np.ldexp(1.0, p)
     block_rel = np.where(pos, np.minimum(safe - lo, 2 * lo - safe) / safe, np.inf)
-    e = np.clip(np.where(pos, p - E4M3_EMAX, SCALE_EXP_MIN), SCALE_EXP_MIN, SCALE_EXP_MAX)
+    _, _, emax, fmax = _fmt(fmt)
+    mbits, emin = (3, -6) if fmt == "e4m3" else (2, -14)
+    e = np.clip(np.where(pos, p - emax, SCALE_EXP_MIN), SCALE_EXP_MIN, SCALE_EXP_MAX)
     r = np.abs(np.ldexp(xb, -e[..., None]))
     _, ex = np.frexp(r)
-    q_exp = np.maximum(ex - 1, -6) - 3
+    q_exp = np.maximum(ex - 1, emin) - mbits
     t = np.ldexp(r, -q_exp)                  # position on the grid, in steps
     mid_dist = np.abs(t - np.floor(t) - 0.5) * np.ldexp(1.0, q_exp)
-    sat_dist = np.abs(r - E4M3_MAX)
+    sat_dist = np.abs(r - fmax)
     d = np.minimum(mid_dist, sat_dist)
     elem_rel = np.where(r > 0, d / np.where(r > 0, r, 1.0), np.inf)
     return elem_rel.reshape(*lead, cols), block_rel

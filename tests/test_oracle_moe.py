@@ -244,3 +244,30 @@ def test_quantized_layer_is_close_to_unquantized():
 def test_layer_flops_formula():
     f = moe.layer_flops(16384, 5120, 8192)
     assert abs(f["fwd"] / 1e12 - 4.123) < 1e-3 and abs(f["total"] / 1e12 - 12.37) < 1e-2
+
+
+def test_e5m2_gradient_option():
+    """With E5M2 gradients (dY and [da|db]: 3 significant bits instead of 4)
+    the backward still tracks the fp64 layer, less closely than with E4M3;
+    the forward is untouched.  Each gradient operand quantized in E5M2
+    decodes to the same values as quantizing it directly (the option changes
+    only the element format of those two operands)."""
+    ids, gate, x, W1, W3, W2, dOut = _tiny_layer(seed=2, T=64, H=128, E=3, F=128, k=2)
+    bits = [mx.f64_to_bf16_bits(v) for v in (x, W1, W3, W2, dOut)]
+    fq = moe.layer_forward(*bits[:4], ids, gate.astype(np.float32), quant=True)
+    fr = moe.layer_forward(*bits[:4], ids, gate.astype(np.float32), quant=False)
+    b4 = moe.layer_backward(fq, *bits[:4], bits[4])
+    b5 = moe.layer_backward(fq, *bits[:4], bits[4], grad_fmt="e5m2")
+    br = moe.layer_backward(fr, *bits[:4], bits[4])
+    assert np.array_equal(b4["dY"], b5["dY"])          # dY itself is formed the same way
+    for key in ("dX", "dW1", "dW3", "dW2"):
+        e4 = np.linalg.norm(b4[key] - br[key]) / np.linalg.norm(br[key])
+        e5 = np.linalg.norm(b5[key] - br[key]) / np.linalg.norm(br[key])
+        assert e4 < e5 < 0.2, (key, e4, e5)
+    # dW2 = h^T dY with dY blocked along tokens in E5M2
+    off = fq["offsets"]
+    q, s = mx.quantize_cols(b5["dY"], "e5m2")
+    dY5 = mx.dequantize_rows(q, s, "e5m2")
+    qh, sh = mx.quantize_cols(fq["h"])
+    ref = moe.grouped_gemm_tokens(mx.dequantize_rows(qh, sh), dY5, off)
+    assert np.allclose(b5["dW2"], ref, rtol=0, atol=0)

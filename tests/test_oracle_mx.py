@@ -22,9 +22,9 @@ def _parse_value(s):
     return float(s)
 
 
-def _golden_cases():
+def _golden_cases(path=GOLDEN):
     cases = []
-    for line in open(GOLDEN):
+    for line in open(path):
         line = line.strip()
         if not line or line.startswith("#"):
             continue
@@ -287,3 +287,70 @@ def test_rowmax_vs_blocks_on_wide_rows():
                      np.median(np.abs(mx.dequantize_rowmax(qr, sr) - v)[nz] / np.abs(v[nz])))
     assert med["plain"][0] < 1 / 16 and med["plain"][1] < 1 / 16, med
     assert med["wide"][1] > 10 * med["wide"][0], med
+
+
+# ----------------------------------------------------------------------------
+# E5M2 elements (the gradient option)
+# ----------------------------------------------------------------------------
+GOLDEN_E5M2 = os.path.join(os.path.dirname(__file__), "golden", "mx_blocks_e5m2.txt")
+
+
+@pytest.mark.parametrize("name,v,scale,codes", _golden_cases(GOLDEN_E5M2),
+                         ids=lambda c: c if isinstance(c, str) else "")
+def test_hand_worked_blocks_e5m2(name, v, scale, codes):
+    bits = torch.tensor(v, dtype=torch.float32).to(torch.bfloat16)
+    assert np.array_equal(np.nan_to_num(bits.float().numpy().astype(np.float64), nan=7.0),
+                          np.nan_to_num(v, nan=7.0)), name
+    q, s = mx.quantize_blocks(v, "e5m2")
+    assert int(s) == scale, (name, hex(int(s)))
+    assert np.array_equal(q, codes), (name, [hex(c) for c in q])
+
+
+def test_e5m2_decode_against_torch_and_roundtrip():
+    codes = np.arange(256, dtype=np.uint8)
+    ours = mx.e5m2_decode(codes)
+    ref = torch.from_numpy(codes).view(torch.float8_e5m2).double().numpy()
+    assert np.array_equal(np.isnan(ours), np.isnan(ref))
+    fin = ~np.isnan(ref)
+    assert np.array_equal(ours[fin], ref[fin])
+    finite = np.isfinite(ours)
+    back = mx.e5m2_encode(ours[finite])
+    assert np.array_equal(back, codes[finite])
+
+
+def test_exhaustive_e5m2_cast_vs_torch():
+    """Every finite bf16 value v at every exponent offset where it can sit in
+    an E5M2 block (from being its amax down to below the subnormals), cast by
+    the oracle and by torch's float8_e5m2 conversion (RNE) of the value
+    clamped to +-57344."""
+    v = _all_finite_bf16()
+    v = v[v != 0]
+    fl = mx.floor_log2(np.abs(v))
+    for d in range(-16, 19):
+        r = np.ldexp(v, -(fl + d))
+        ours = mx.e5m2_encode(r)
+        ref = torch.from_numpy(np.clip(r, -57344.0, 57344.0).astype(np.float32)) \
+            .to(torch.float8_e5m2).view(torch.uint8).numpy()
+        assert np.array_equal(ours, ref), d
+
+
+def test_e5m2_block_bound_and_layout():
+    """Non-saturated elements decode within half an E5M2 step of v (times the
+    scale); the amax lands in the top binade; COL mode is ROW of X^T."""
+    g = np.random.default_rng(8)
+    v = g.standard_normal((2048, 32)) * np.ldexp(1.0, g.integers(-40, 40, size=(2048, 1)))
+    v = mx.bf16_to_f64(mx.f64_to_bf16_bits(v))
+    q, s = mx.quantize_blocks(v, "e5m2")
+    scale = np.ldexp(1.0, s.astype(np.int64) - 127)[:, None]
+    r = v / scale
+    sat = np.abs(r) > 57344
+    _, ex = np.frexp(np.abs(r))
+    step = np.ldexp(1.0, np.maximum(ex - 1, -14) - 2)
+    err = np.abs(v - mx.e5m2_decode(q) * scale)
+    assert np.all(err[~sat] <= 0.5 * (step * scale)[~sat])
+    assert np.all(np.max(q & 0x7F, axis=1) >= 0x78)
+    x = v.reshape(64, 1024)
+    qc, sc = mx.quantize_cols(x, "e5m2")
+    qr, sr = mx.quantize_rows(x.T.copy(), "e5m2")
+    assert np.array_equal(qc, qr) and np.array_equal(sc, sr)
+    assert np.array_equal(mx.dequantize_rows(qr, sr, "e5m2"), mx.dequantize_rows(*mx.quantize_rows(x.T.copy(), "e5m2"), "e5m2"))
