@@ -149,8 +149,9 @@ class ClockSampler:
 # preallocated buffers, with CUDA events between launches
 # ----------------------------------------------------------------------------
 class LayerStep:
-    def __init__(self, d, inp, dev):
+    def __init__(self, d, inp, dev, grad_elem=0):
         import mxfp8_mixture_experts_gb300 as m
+        self.grad_elem = grad_elem  # element format of the backward's gradient operands (0 E4M3, 1 E5M2)
         self.m = m
         self.L = m.lib()
         self.d = d
@@ -227,8 +228,8 @@ class LayerStep:
                 raise RuntimeError(f"{what}: {L.mx_status_string(code).decode()}")
 
         mark()
-        chk(L.mx_quantize(self.W13.data_ptr(), E, H, 2 * F, 3, 1, p["w13_rq"], p["w13_rs"], p["w13_cq"], p["w13_cs"], s), "q W13"); mark()
-        chk(L.mx_quantize(self.W2.data_ptr(), E, F, H, 3, 1, p["w2_rq"], p["w2_rs"], p["w2_cq"], p["w2_cs"], s), "q W2"); mark()
+        chk(L.mx_quantize(self.W13.data_ptr(), E, H, 2 * F, 3, 1, 0, p["w13_rq"], p["w13_rs"], p["w13_cq"], p["w13_cs"], s), "q W13"); mark()
+        chk(L.mx_quantize(self.W2.data_ptr(), E, F, H, 3, 1, 0, p["w2_rq"], p["w2_rs"], p["w2_cq"], p["w2_cs"], s), "q W2"); mark()
         if self.routed:
             chk(L.moe_route(logits, T, E, k, p["ids"], p["gate"], s), "route")
         mark()
@@ -237,25 +238,26 @@ class LayerStep:
         chk(L.moe_permute(2, x, None, T, H, k, p["dst"], p["src"], R, p["xq"], p["xs"], 1, s), "permute"); mark()
         chk(L.moe_gemm1_swiglu(p["xq"], p["xs"], p["w13_cq"], p["w13_cs"], p["off"], E, R, F, H, p["ab"], p["hq"],
                                p["hs"], st, s), "gemm1"); mark()
-        chk(L.mx_grouped_gemm(0, p["hq"], p["hs"], p["w2_cq"], p["w2_cs"], p["off"], E, R, H, F, p["y"], 0, st, s),
+        ge = self.grad_elem
+        chk(L.mx_grouped_gemm(0, p["hq"], p["hs"], p["w2_cq"], p["w2_cs"], p["off"], E, R, H, F, p["y"], 0, 0, 0, st, s),
             "gemm2"); mark()
         chk(L.moe_unpermute(p["y"], p["dst"], p["gate"], T, H, k, p["out"], s), "combine"); mark()
         chk(L.moe_gate_grad(dOut, p["y"], p["dst"], T, H, k, p["d_gate"], s), "gate grad"); mark()
         lim = p["off"] + 4 * E  # offsets[E]: the routed rows end there
-        chk(L.moe_gather_quant(dOut, p["gate"], p["src"], T, H, k, R, 3, p["dy_rq"], p["dy_rs"], p["dy_cq"],
+        chk(L.moe_gather_quant(dOut, p["gate"], p["src"], T, H, k, R, 3, ge, p["dy_rq"], p["dy_rs"], p["dy_cq"],
                                p["dy_cs"], lim, s), "dY quant"); mark()
-        chk(L.mx_grouped_gemm(1, p["dy_rq"], p["dy_rs"], p["w2_rq"], p["w2_rs"], p["off"], E, R, F, H, p["dh"], 1, st,
+        chk(L.mx_grouped_gemm(1, p["dy_rq"], p["dy_rs"], p["w2_rq"], p["w2_rs"], p["off"], E, R, F, H, p["dh"], 1, ge, 0, st,
                               s), "dgrad2"); mark()
-        chk(L.moe_swiglu_bwd(p["dh"], p["ab"], R, F, p["dab_rq"], p["dab_rs"], p["dab_cq"], p["dab_cs"], p["h_cq"],
+        chk(L.moe_swiglu_bwd(p["dh"], p["ab"], R, F, ge, p["dab_rq"], p["dab_rs"], p["dab_cq"], p["dab_cs"], p["h_cq"],
                              p["h_cs"], lim, s), "swiglu bwd"); mark()
-        chk(L.mx_grouped_gemm(2, p["h_cq"], p["h_cs"], p["dy_cq"], p["dy_cs"], p["off"], E, R, F, H, p["dW2"], 1, st,
+        chk(L.mx_grouped_gemm(2, p["h_cq"], p["h_cs"], p["dy_cq"], p["dy_cs"], p["off"], E, R, F, H, p["dW2"], 1, 0, ge, st,
                               s), "wgrad2"); mark()
         chk(L.mx_grouped_gemm(1, p["dab_rq"], p["dab_rs"], p["w13_rq"], p["w13_rs"], p["off"], E, R, H, 2 * F,
-                              p["dxp"], 0, st, s), "dgrad1"); mark()
-        chk(L.moe_gather_quant(x, None, p["src"], T, H, k, R, 2, None, None, p["xp_cq"], p["xp_cs"], lim, s),
+                              p["dxp"], 0, ge, 0, st, s), "dgrad1"); mark()
+        chk(L.moe_gather_quant(x, None, p["src"], T, H, k, R, 2, 0, None, None, p["xp_cq"], p["xp_cs"], lim, s),
             "x col quant"); mark()
         chk(L.mx_grouped_gemm(2, p["xp_cq"], p["xp_cs"], p["dab_cq"], p["dab_cs"], p["off"], E, R, H, 2 * F,
-                              p["dW13"], 1, st, s), "wgrad1"); mark()
+                              p["dW13"], 1, 0, ge, st, s), "wgrad1"); mark()
         chk(L.moe_unpermute(p["dxp"], p["dst"], None, T, H, k, p["dX"], s), "combine dX"); mark()
 
     NAMES = ["quantize W13", "quantize W2", "route", "map", "permute+quant", "gemm1+swiglu", "gemm2", "combine",
@@ -301,7 +303,7 @@ def _quant_bench(dev, iters=20):
         flush.zero_()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(s)
-        code = L.mx_quantize(x.data_ptr(), 1, R, C, 3, 1, outs[0].data_ptr(), sc[0].data_ptr(), outs[1].data_ptr(),
+        code = L.mx_quantize(x.data_ptr(), 1, R, C, 3, 1, 0, outs[0].data_ptr(), sc[0].data_ptr(), outs[1].data_ptr(),
                              sc[1].data_ptr(), s.cuda_stream)
         e1.record(s)
         assert code == 0
@@ -329,7 +331,7 @@ def _dequant_bench(dev, iters=20):
         flush.zero_()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(s)
-        code = L.mx_dequantize(q.data_ptr(), sc.data_ptr(), 1, R, C, 1, 0, out.data_ptr(), s.cuda_stream)
+        code = L.mx_dequantize(q.data_ptr(), sc.data_ptr(), 1, R, C, 1, 0, 0, out.data_ptr(), s.cuda_stream)
         e1.record(s)
         assert code == 0
         torch.cuda.synchronize()
@@ -374,7 +376,7 @@ def _rowmax_bench(dev, iters=20):
     rm = q.view(torch.float8_e4m3fn).float() * sc[:, None]
     mq, ms, _, _ = m.mx_quantize(x, m.MX_MODE_ROW, m.MX_SCALE_PLAIN)
     mxd = torch.empty((R, C), dtype=torch.float32, device=dev)
-    assert L.mx_dequantize(mq.data_ptr(), ms.data_ptr(), 1, R, C, 0, 1, mxd.data_ptr(), s.cuda_stream) == 0
+    assert L.mx_dequantize(mq.data_ptr(), ms.data_ptr(), 1, R, C, 0, 0, 1, mxd.data_ptr(), s.cuda_stream) == 0
     torch.cuda.synchronize()
     sqnr = lambda d: float(10 * torch.log10(sig / ((xf - d).double() ** 2).sum()))
     return {"GB/s": nbytes / t / 1e9, "us": t * 1e6, "bytes": nbytes, "sqnr_db_rowmax": sqnr(rm),
@@ -719,6 +721,8 @@ def main():
     ap.add_argument("--T", type=int, default=None, help="override the token count (profiling of small cases)")
     ap.add_argument("--E", type=int, default=None, help="override the expert count (profiling of small cases)")
     ap.add_argument("--k", type=int, default=None, help="override top-k (a variant; the bench line is top-1)")
+    ap.add_argument("--grad-format", default="e4m3", choices=["e4m3", "e5m2"],
+                    help="element format of the backward's gradient operands (a variant; the bench line is e4m3)")
     ap.add_argument("--workload", default="layer",
                     choices=["layer", "gemm", "quantize", "dequantize", "permute", "rowmax"],
                     help="layer: the full training step (the bench line); gemm / quantize / dequantize / "
@@ -749,6 +753,8 @@ def main():
               "T": dims.T, "H": dims.H, "E": dims.E, "F": dims.F, "k": dims.k,
               "l2": "inputs larger than L2 (weights 4 GB, activations 168 MB per tensor); no flush",
               "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"}
+    if args.grad_format != "e4m3":
+        config["grad_format"] = args.grad_format
 
     if args.impl == "reference":
         if rank != 0:
@@ -778,7 +784,7 @@ def main():
     torch.cuda.set_device(dev)
     d = m.MoELayerDims(T=dims.T, H=dims.H, F=dims.F, E=dims.E, k=dims.k)
     inp = workloads.layer_inputs(dims, seed=rank, device=dev, router="logits")
-    step = LayerStep(d, inp, dev)
+    step = LayerStep(d, inp, dev, grad_elem=1 if args.grad_format == "e5m2" else 0)
     stream = torch.cuda.current_stream(dev)
 
     def barrier():

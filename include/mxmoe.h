@@ -73,6 +73,13 @@ typedef struct CUstream_st *mx_stream; /* same type as cudaStream_t */
                                Rows padded to 128, scale columns to 4, padding 0x00.
                                This is the layout the block-scaled tensor-core MMA reads. */
 
+/* element formats of an MX block (the scale rule takes the format's largest
+ * power of two: 2^8 for E4M3, 2^15 for E5M2).  E4M3 is the MXFP8 of the
+ * pages; E5M2 is the gradient option (two exponent bits more range, one
+ * mantissa bit less), a variant the pages do not name. */
+#define MX_ELEM_E4M3 0 /* OCP E4M3FN: max +-448, NaN 0x7F, no Inf          */
+#define MX_ELEM_E5M2 1 /* OCP E5M2: max +-57344, Inf 0x7C, NaN 0x7F        */
+
 /* grouped GEMM operations */
 #define MX_GEMM_FWD 0   /* C[rows of e] = A[rows of e] . B[e]^T, rows grouped by offsets */
 #define MX_GEMM_DGRAD 1 /* same contraction as FWD (operands differ, see mx_grouped_gemm) */
@@ -140,6 +147,8 @@ int64_t mx_scale_bytes(int64_t rows, int64_t cols, int32_t layout);
  * [-127, 127], scale byte e + 127; each element becomes the E4M3 round-to-
  * nearest-even of x * 2^-e, saturated to +-448.  A block holding NaN or Inf
  * gets scale 0xFF and elements 0x7F.
+ * elem = MX_ELEM_E5M2 instead: e = floor(log2 amax) - 15 and E5M2 elements
+ * saturated to +-57344 (same clamp, NaN rule and layouts).
  *   ROW: q_row [batch, rows, cols], s_row [batch] x scale array(rows, cols).
  *        Needs cols % 32 == 0.
  *   COL: blocks of 32 consecutive rows of one column; stored transposed:
@@ -151,7 +160,7 @@ int64_t mx_scale_bytes(int64_t rows, int64_t cols, int32_t layout);
  * padded scale array (mx_scale_bytes).
  */
 mx_status mx_quantize(const void *x, int64_t batch, int64_t rows, int64_t cols,
-                      int32_t mode, int32_t scale_layout, uint8_t *q_row,
+                      int32_t mode, int32_t scale_layout, int32_t elem, uint8_t *q_row,
                       uint8_t *s_row, uint8_t *q_col, uint8_t *s_col,
                       mx_stream stream);
 
@@ -168,12 +177,14 @@ mx_status mx_quantize(const void *x, int64_t batch, int64_t rows, int64_t cols,
  *   MX_OUT_F32:  out fp32, exact (fp32 subnormals kept; overflow to +-Inf);
  *   MX_OUT_BF16: out bf16, that exact value rounded to nearest even once.
  * Scale byte 0xFF and the E4M3 NaN codes (0x7F, 0xFF) give NaN.
+ * elem = MX_ELEM_E5M2: q holds E5M2 codes (their Inf and NaN codes decode as
+ * such).
  * out [batch, rows, cols].  cols % 32 == 0 (cols % 128 == 0 is not needed:
  * the swizzled array's padding is not read); q and out 16-byte aligned.
  */
 mx_status mx_dequantize(const uint8_t *q, const uint8_t *s, int64_t batch, int64_t rows,
-                        int64_t cols, int32_t scale_layout, int32_t out_dtype, void *out,
-                        mx_stream stream);
+                        int64_t cols, int32_t scale_layout, int32_t elem, int32_t out_dtype,
+                        void *out, mx_stream stream);
 
 /* ------------------------------------------------------------------------ */
 /* Row-max-scaled FP8, for comparison with MX block scaling                  */
@@ -318,6 +329,9 @@ mx_status moe_unpermute(const void *y, const int32_t *dst, const float *gate,
  *   C [E, N, K]; an empty group writes zeros.
  * Sizes: M_cap % 128 == 0, N % 256 == 0, K % 128 == 0, 1 <= E <= 1024.
  * c_dtype: MX_OUT_BF16 (round-to-nearest-even) or MX_OUT_F32.
+ * elem_a, elem_b: element formats of A and B (MX_ELEM_E4M3 or MX_ELEM_E5M2,
+ * independently: the layer's E5M2 gradient option multiplies E5M2 gradients
+ * by E4M3 weights or activations).
  * Alignment: A, B, sA, sB and C 16-byte aligned (the operands and their
  * scales are read by TMA).
  */
@@ -325,7 +339,8 @@ mx_status mx_grouped_gemm(int32_t op, const uint8_t *A, const uint8_t *sA,
                           const uint8_t *B, const uint8_t *sB,
                           const int32_t *offsets, int32_t E, int64_t M_cap,
                           int64_t N, int64_t K, void *C, int32_t c_dtype,
-                          int32_t *dev_status, mx_stream stream);
+                          int32_t elem_a, int32_t elem_b, int32_t *dev_status,
+                          mx_stream stream);
 
 /*
  * Deterministic split-K weight gradient (a variant of MX_GEMM_WGRAD for
@@ -336,7 +351,8 @@ mx_status mx_grouped_gemm(int32_t op, const uint8_t *A, const uint8_t *sA,
  * (fp32, in `ws`) are summed in the order s = 0, 1, ..., splits-1, so the
  * result does not depend on scheduling; it differs from the unsplit call
  * only by fp32 rounding of the partial sums (splits = 1: bit-identical).
- * Operands as MX_GEMM_WGRAD; C fp32 [E, N, K].  1 <= splits <= 16,
+ * Operands as MX_GEMM_WGRAD (element formats elem_a, elem_b as in
+ * mx_grouped_gemm); C fp32 [E, N, K].  1 <= splits <= 16,
  * E * splits <= 1024, N % 256 == 0, K % 256 == 0, M_cap % 128 == 0.
  * ws: device scratch of mx_wgrad_splitk_workspace_size(E, N, K, splits)
  * bytes, 16-byte aligned (MX_ERR_WORKSPACE if smaller).
@@ -345,9 +361,9 @@ int64_t mx_wgrad_splitk_workspace_size(int32_t E, int64_t N, int64_t K, int32_t 
 mx_status mx_grouped_gemm_wgrad_splitk(const uint8_t *A, const uint8_t *sA,
                                        const uint8_t *B, const uint8_t *sB,
                                        const int32_t *offsets, int32_t E, int64_t M_cap,
-                                       int64_t N, int64_t K, int32_t splits, void *ws,
-                                       int64_t ws_bytes, float *C, int32_t *dev_status,
-                                       mx_stream stream);
+                                       int64_t N, int64_t K, int32_t splits, int32_t elem_a,
+                                       int32_t elem_b, void *ws, int64_t ws_bytes, float *C,
+                                       int32_t *dev_status, mx_stream stream);
 
 /* ------------------------------------------------------------------------ */
 /* S: SwiGLU between the expert projections (forward fused into GEMM1)       */
@@ -382,6 +398,8 @@ mx_status moe_gemm1_swiglu(const uint8_t *A, const uint8_t *sA, const uint8_t *B
  * row_limit: optional device int32 (NULL = all `rows`): 128-row bands that
  * start at or past *row_limit are skipped and their outputs left untouched
  * (the layer passes offsets + E, the end of the routed rows).
+ * grad_elem: element format of [da|db] (MX_ELEM_E4M3 or MX_ELEM_E5M2, the
+ * gradient option); h is always E4M3.
  * Arithmetic: fp32; sigmoid(a) from the hardware's approximate base-2
  * exponential and reciprocal with an exactly rounded exponent (see
  * mx_selftest_sigmoid): a few fp32 ulps over bf16 a in [-128, 128].
@@ -389,7 +407,7 @@ mx_status moe_gemm1_swiglu(const uint8_t *A, const uint8_t *sA, const uint8_t *B
  * row-block scales are written as one 32-bit word); dab_rs may sit at any byte.
  */
 mx_status moe_swiglu_bwd(const float *dh, const void *ab, int64_t rows,
-                         int64_t F, uint8_t *dab_rq, uint8_t *dab_rs,
+                         int64_t F, int32_t grad_elem, uint8_t *dab_rq, uint8_t *dab_rs,
                          uint8_t *dab_cq, uint8_t *dab_cs, uint8_t *h_cq,
                          uint8_t *h_cs, const int32_t *row_limit,
                          mx_stream stream);
@@ -410,10 +428,11 @@ mx_status moe_swiglu_bwd(const float *dh, const void *ab, int64_t rows,
  * H % 128 == 0, rows_cap % 128 == 0.  row_limit: optional device int32 (NULL
  * = all rows_cap rows): 128-row bands that start at or past *row_limit are
  * skipped and their outputs left untouched (the layer passes offsets + E).
+ * elem: element format of both outputs (MX_ELEM_E4M3 or MX_ELEM_E5M2).
  */
 mx_status moe_gather_quant(const void *x, const float *gate, const int32_t *src,
                            int64_t T, int64_t H, int32_t k, int64_t rows_cap,
-                           int32_t mode, uint8_t *q_row, uint8_t *s_row,
+                           int32_t mode, int32_t elem, uint8_t *q_row, uint8_t *s_row,
                            uint8_t *q_col, uint8_t *s_col,
                            const int32_t *row_limit, mx_stream stream);
 
@@ -449,7 +468,10 @@ mx_status moe_gate_grad(const void *dOut, const void *y, const int32_t *dst,
  *
  * moe_layer_bwd: dOut bf16 [T, H] -> dX bf16 [T, H], dW13 fp32 [E, H, 2F],
  * dW2 fp32 [E, F, H], d_gate fp32 [T, k] (NULL: not computed).  Uses the `ws`
- * and `wq` of the matching forward.
+ * and `wq` of the matching forward.  grad_elem: element format of the two
+ * gradient operands the backward quantizes, dY = gate * dOut and [da|db]
+ * (MX_ELEM_E4M3; MX_ELEM_E5M2 is the gradient option); weights, h and the
+ * permuted input stay E4M3.
  */
 int64_t moe_layer_weights_size(int64_t H, int64_t F, int32_t E);
 int64_t moe_layer_workspace_size(int64_t T, int64_t H, int64_t F, int32_t E,
@@ -464,7 +486,7 @@ mx_status moe_layer_fwd(const void *x, const float *logits, int32_t *ids,
                         mx_stream stream);
 mx_status moe_layer_bwd(const void *x, const void *dOut, const float *gate,
                         const void *wq, int64_t T, int64_t H, int64_t F,
-                        int32_t E, int32_t k, void *ws, int64_t ws_bytes,
+                        int32_t E, int32_t k, int32_t grad_elem, void *ws, int64_t ws_bytes,
                         void *dX, float *dW13, float *dW2, float *d_gate,
                         int32_t *dev_status, mx_stream stream);
 

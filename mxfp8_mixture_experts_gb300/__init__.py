@@ -17,7 +17,7 @@ import torch
 from . import _lib
 from ._lib import (MX_GEMM_DGRAD, MX_GEMM_FWD, MX_GEMM_WGRAD, MX_MODE_BOTH, MX_MODE_COL,  # noqa: F401
                    MX_MODE_ROW, MX_OUT_BF16, MX_OUT_F32, MX_PERMUTE_BF16, MX_PERMUTE_BF16_QUANT,
-                   MX_PERMUTE_FP8, MX_SCALE_PLAIN, MX_SCALE_SWIZZLED, MxError)
+                   MX_PERMUTE_FP8, MX_SCALE_PLAIN, MX_SCALE_SWIZZLED, MX_ELEM_E4M3, MX_ELEM_E5M2, MxError)
 
 __all__ = [
     "lib", "MxError", "mx_quantize", "mx_dequantize", "mx_scale_bytes", "moe_route", "moe_rows_cap", "moe_permute_map",
@@ -56,9 +56,11 @@ def mx_scale_bytes(rows: int, cols: int, layout: int) -> int:
     return int(lib().mx_scale_bytes(rows, cols, layout))
 
 
-def mx_quantize(x: torch.Tensor, mode: int = MX_MODE_ROW, scale_layout: int = MX_SCALE_PLAIN):
+def mx_quantize(x: torch.Tensor, mode: int = MX_MODE_ROW, scale_layout: int = MX_SCALE_PLAIN,
+                elem: int = MX_ELEM_E4M3):
     """x bf16 [rows, cols] or [batch, rows, cols] -> (q_row, s_row, q_col, s_col);
-    unused outputs are None.  q_col is [.., cols, rows]."""
+    unused outputs are None.  q_col is [.., cols, rows].  elem: element format
+    (MX_ELEM_E4M3 or MX_ELEM_E5M2)."""
     _req(x, torch.bfloat16, "x")
     batched = x.dim() == 3
     b, r, c = (x.shape if batched else (1, *x.shape))
@@ -71,20 +73,20 @@ def mx_quantize(x: torch.Tensor, mode: int = MX_MODE_ROW, scale_layout: int = MX
     if mode & MX_MODE_COL:
         q_col = torch.empty((*lead, c, r), dtype=torch.uint8, device=dev)
         s_col = _u8(b * mx_scale_bytes(c, r, scale_layout), dev)
-    _lib.check(lib().mx_quantize(_ptr(x), b, r, c, mode, scale_layout, _ptr(q_row), _ptr(s_row), _ptr(q_col),
+    _lib.check(lib().mx_quantize(_ptr(x), b, r, c, mode, scale_layout, elem, _ptr(q_row), _ptr(s_row), _ptr(q_col),
                                  _ptr(s_col), _stream(dev)), "mx_quantize")
     return q_row, s_row, q_col, s_col
 
 
 def mx_dequantize(q: torch.Tensor, s: torch.Tensor, scale_layout: int = MX_SCALE_PLAIN,
-                  out_dtype: int = MX_OUT_F32):
+                  out_dtype: int = MX_OUT_F32, elem: int = MX_ELEM_E4M3):
     """q uint8 [rows, cols] or [batch, rows, cols] with its scales -> fp32 or
     bf16 of the same shape."""
     _req(q, torch.uint8, "q")
     batched = q.dim() == 3
     b, r, c = (q.shape if batched else (1, *q.shape))
     out = torch.empty(q.shape, dtype=torch.float32 if out_dtype == MX_OUT_F32 else torch.bfloat16, device=q.device)
-    _lib.check(lib().mx_dequantize(_ptr(q), _ptr(s), b, r, c, scale_layout, out_dtype, _ptr(out),
+    _lib.check(lib().mx_dequantize(_ptr(q), _ptr(s), b, r, c, scale_layout, elem, out_dtype, _ptr(out),
                                    _stream(q.device)), "mx_dequantize")
     return out
 
@@ -148,7 +150,7 @@ def moe_unpermute(y: torch.Tensor, dst: torch.Tensor, gate: torch.Tensor | None,
 
 def mx_grouped_gemm(op: int, A, sA, B, sB, offsets, E: int, M_cap: int, N: int, K: int,
                     out_dtype: int = MX_OUT_F32, out: torch.Tensor | None = None,
-                    dev_status: torch.Tensor | None = None):
+                    dev_status: torch.Tensor | None = None, elem_a: int = MX_ELEM_E4M3, elem_b: int = MX_ELEM_E4M3):
     """FWD/DGRAD: C [M_cap, N]; WGRAD: C [E, N, K] (see include/mxmoe.h)."""
     dev = A.device
     dt = torch.float32 if out_dtype == MX_OUT_F32 else torch.bfloat16
@@ -156,13 +158,15 @@ def mx_grouped_gemm(op: int, A, sA, B, sB, offsets, E: int, M_cap: int, N: int, 
         shape = (E, N, K) if op == MX_GEMM_WGRAD else (M_cap, N)
         out = torch.empty(shape, dtype=dt, device=dev)
     _lib.check(lib().mx_grouped_gemm(op, _ptr(A), _ptr(sA), _ptr(B), _ptr(sB), _ptr(offsets), E, M_cap, N, K,
-                                     _ptr(out), out_dtype, _ptr(dev_status), _stream(dev)), "mx_grouped_gemm")
+                                     _ptr(out), out_dtype, elem_a, elem_b, _ptr(dev_status), _stream(dev)),
+               "mx_grouped_gemm")
     return out
 
 
 def mx_grouped_gemm_wgrad_splitk(A, sA, B, sB, offsets, E: int, M_cap: int, N: int, K: int, splits: int,
                                  out: torch.Tensor | None = None, ws: torch.Tensor | None = None,
-                                 dev_status: torch.Tensor | None = None):
+                                 dev_status: torch.Tensor | None = None, elem_a: int = MX_ELEM_E4M3,
+                                 elem_b: int = MX_ELEM_E4M3):
     """Deterministic split-K wgrad: C fp32 [E, N, K] (see include/mxmoe.h)."""
     dev = A.device
     need = int(lib().mx_wgrad_splitk_workspace_size(E, N, K, splits))
@@ -173,8 +177,8 @@ def mx_grouped_gemm_wgrad_splitk(A, sA, B, sB, offsets, E: int, M_cap: int, N: i
     if out is None:
         out = torch.empty((E, N, K), dtype=torch.float32, device=dev)
     _lib.check(lib().mx_grouped_gemm_wgrad_splitk(_ptr(A), _ptr(sA), _ptr(B), _ptr(sB), _ptr(offsets), E, M_cap, N,
-                                                  K, splits, _ptr(ws), ws.numel(), _ptr(out), _ptr(dev_status),
-                                                  _stream(dev)), "mx_grouped_gemm_wgrad_splitk")
+                                                  K, splits, elem_a, elem_b, _ptr(ws), ws.numel(), _ptr(out),
+                                                  _ptr(dev_status), _stream(dev)), "mx_grouped_gemm_wgrad_splitk")
     return out
 
 
@@ -190,7 +194,8 @@ def moe_gemm1_swiglu(A, sA, B, sB, offsets, E: int, M_cap: int, F: int, H: int,
     return ab, hq, hs
 
 
-def moe_swiglu_bwd(dh: torch.Tensor, ab: torch.Tensor, row_limit: torch.Tensor | None = None):
+def moe_swiglu_bwd(dh: torch.Tensor, ab: torch.Tensor, row_limit: torch.Tensor | None = None,
+                   grad_elem: int = MX_ELEM_E4M3):
     """-> (dab_rq, dab_rs, dab_cq, dab_cs, h_cq, h_cs), scales swizzled.
     row_limit: optional device int32 tensor whose first element bounds the
     rows processed (128-row bands at or past it are left unwritten)."""
@@ -204,14 +209,14 @@ def moe_swiglu_bwd(dh: torch.Tensor, ab: torch.Tensor, row_limit: torch.Tensor |
     dab_cs = _u8(mx_scale_bytes(2 * F, rows, MX_SCALE_SWIZZLED), dev)
     h_cq = torch.empty((F, rows), dtype=torch.uint8, device=dev)
     h_cs = _u8(mx_scale_bytes(F, rows, MX_SCALE_SWIZZLED), dev)
-    _lib.check(lib().moe_swiglu_bwd(_ptr(dh), _ptr(ab), rows, F, _ptr(dab_rq), _ptr(dab_rs), _ptr(dab_cq),
+    _lib.check(lib().moe_swiglu_bwd(_ptr(dh), _ptr(ab), rows, F, grad_elem, _ptr(dab_rq), _ptr(dab_rs), _ptr(dab_cq),
                                     _ptr(dab_cs), _ptr(h_cq), _ptr(h_cs), _ptr(row_limit), _stream(dev)),
                "moe_swiglu_bwd")
     return dab_rq, dab_rs, dab_cq, dab_cs, h_cq, h_cs
 
 
 def moe_gather_quant(x: torch.Tensor, gate, src: torch.Tensor, k: int, mode: int = MX_MODE_BOTH,
-                     row_limit: torch.Tensor | None = None):
+                     row_limit: torch.Tensor | None = None, elem: int = MX_ELEM_E4M3):
     """-> (q_row, s_row, q_col, s_col) of the gathered [rows_cap, H] matrix.
     row_limit: as in moe_swiglu_bwd."""
     _req(x, torch.bfloat16, "x")
@@ -225,7 +230,7 @@ def moe_gather_quant(x: torch.Tensor, gate, src: torch.Tensor, k: int, mode: int
     if mode & MX_MODE_COL:
         q_col = torch.empty((H, R), dtype=torch.uint8, device=dev)
         s_col = _u8(mx_scale_bytes(H, R, MX_SCALE_SWIZZLED), dev)
-    _lib.check(lib().moe_gather_quant(_ptr(x), _ptr(gate), _ptr(src), T, H, k, R, mode, _ptr(q_row), _ptr(s_row),
+    _lib.check(lib().moe_gather_quant(_ptr(x), _ptr(gate), _ptr(src), T, H, k, R, mode, elem, _ptr(q_row), _ptr(s_row),
                                       _ptr(q_col), _ptr(s_col), _ptr(row_limit), _stream(dev)), "moe_gather_quant")
     return q_row, s_row, q_col, s_col
 
@@ -312,7 +317,7 @@ def moe_layer_fwd(x: torch.Tensor, wq: torch.Tensor, d: MoELayerDims, ws: torch.
 
 def moe_layer_bwd(x: torch.Tensor, dOut: torch.Tensor, gate, wq: torch.Tensor, d: MoELayerDims,
                   ws: torch.Tensor, *, dX=None, dW13=None, dW2=None, d_gate=None, want_d_gate: bool = True,
-                  dev_status: torch.Tensor | None = None):
+                  dev_status: torch.Tensor | None = None, grad_elem: int = MX_ELEM_E4M3):
     """Backward -> (dX bf16 [T,H], dW13 fp32 [E,H,2F], dW2 fp32 [E,F,H], d_gate fp32 [T,k] or None)."""
     dev = x.device
     dX = torch.empty((d.T, d.H), dtype=torch.bfloat16, device=dev) if dX is None else dX
@@ -320,7 +325,7 @@ def moe_layer_bwd(x: torch.Tensor, dOut: torch.Tensor, gate, wq: torch.Tensor, d
     dW2 = torch.empty((d.E, d.F, d.H), dtype=torch.float32, device=dev) if dW2 is None else dW2
     if want_d_gate and d_gate is None:
         d_gate = torch.empty((d.T, d.k), dtype=torch.float32, device=dev)
-    _lib.check(lib().moe_layer_bwd(_ptr(x), _ptr(dOut), _ptr(gate), _ptr(wq), d.T, d.H, d.F, d.E, d.k, _ptr(ws),
+    _lib.check(lib().moe_layer_bwd(_ptr(x), _ptr(dOut), _ptr(gate), _ptr(wq), d.T, d.H, d.F, d.E, d.k, grad_elem, _ptr(ws),
                                    ws.numel(), _ptr(dX), _ptr(dW13), _ptr(dW2), _ptr(d_gate), _ptr(dev_status),
                                    _stream(dev)), "moe_layer_bwd")
     return dX, dW13, dW2, d_gate

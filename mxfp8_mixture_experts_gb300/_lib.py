@@ -27,6 +27,7 @@ MX_SCALE_PLAIN, MX_SCALE_SWIZZLED = 0, 1
 MX_GEMM_FWD, MX_GEMM_DGRAD, MX_GEMM_WGRAD = 0, 1, 2
 MX_OUT_BF16, MX_OUT_F32 = 0, 1
 MX_PERMUTE_FP8, MX_PERMUTE_BF16, MX_PERMUTE_BF16_QUANT = 0, 1, 2
+MX_ELEM_E4M3, MX_ELEM_E5M2 = 0, 1
 
 _p = C.c_void_p
 _i32 = C.c_int32
@@ -40,8 +41,8 @@ SIGNATURES = {
     "mx_selftest_wait_timeout": (_i32, [_i64, _p, _p]),
     "mx_selftest_sigmoid": (_i32, [_p, _i64, _p, _p]),
     "mx_scale_bytes": (_i64, [_i64, _i64, _i32]),
-    "mx_quantize": (_i32, [_p, _i64, _i64, _i64, _i32, _i32, _p, _p, _p, _p, _p]),
-    "mx_dequantize": (_i32, [_p, _p, _i64, _i64, _i64, _i32, _i32, _p, _p]),
+    "mx_quantize": (_i32, [_p, _i64, _i64, _i64, _i32, _i32, _i32, _p, _p, _p, _p, _p]),
+    "mx_dequantize": (_i32, [_p, _p, _i64, _i64, _i64, _i32, _i32, _i32, _p, _p]),
     "fp8_quantize_rowmax": (_i32, [_p, _i64, _i64, _p, _p, _p]),
     "moe_route": (_i32, [_p, _i64, _i32, _i32, _p, _p, _p]),
     "moe_rows_cap": (_i64, [_i64, _i32, _i32]),
@@ -50,18 +51,19 @@ SIGNATURES = {
     "moe_permute_map_noalloc": (_i32, [_p, _i64, _i32, _i32, _i64, _p, _p, _p, _p, _p, _p]),
     "moe_permute": (_i32, [_i32, _p, _p, _i64, _i64, _i32, _p, _p, _i64, _p, _p, _i32, _p]),
     "moe_unpermute": (_i32, [_p, _p, _p, _i64, _i64, _i32, _p, _p]),
-    "mx_grouped_gemm": (_i32, [_i32, _p, _p, _p, _p, _p, _i32, _i64, _i64, _i64, _p, _i32, _p, _p]),
+    "mx_grouped_gemm": (_i32, [_i32, _p, _p, _p, _p, _p, _i32, _i64, _i64, _i64, _p, _i32, _i32, _i32, _p, _p]),
     "mx_wgrad_splitk_workspace_size": (_i64, [_i32, _i64, _i64, _i32]),
-    "mx_grouped_gemm_wgrad_splitk": (_i32, [_p, _p, _p, _p, _p, _i32, _i64, _i64, _i64, _i32, _p, _i64, _p, _p, _p]),
+    "mx_grouped_gemm_wgrad_splitk": (_i32, [_p, _p, _p, _p, _p, _i32, _i64, _i64, _i64, _i32, _i32, _i32, _p, _i64, _p,
+                                            _p, _p]),
     "moe_gemm1_swiglu": (_i32, [_p, _p, _p, _p, _p, _i32, _i64, _i64, _i64, _p, _p, _p, _p, _p]),
-    "moe_swiglu_bwd": (_i32, [_p, _p, _i64, _i64, _p, _p, _p, _p, _p, _p, _p, _p]),
-    "moe_gather_quant": (_i32, [_p, _p, _p, _i64, _i64, _i32, _i64, _i32, _p, _p, _p, _p, _p, _p]),
+    "moe_swiglu_bwd": (_i32, [_p, _p, _i64, _i64, _i32, _p, _p, _p, _p, _p, _p, _p, _p]),
+    "moe_gather_quant": (_i32, [_p, _p, _p, _i64, _i64, _i32, _i64, _i32, _i32, _p, _p, _p, _p, _p, _p]),
     "moe_gate_grad": (_i32, [_p, _p, _p, _i64, _i64, _i32, _p, _p]),
     "moe_layer_weights_size": (_i64, [_i64, _i64, _i32]),
     "moe_layer_workspace_size": (_i64, [_i64, _i64, _i64, _i32, _i32]),
     "moe_layer_prep_weights": (_i32, [_p, _p, _i64, _i64, _i32, _p, _i64, _p]),
     "moe_layer_fwd": (_i32, [_p, _p, _p, _p, _p, _i64, _i64, _i64, _i32, _i32, _p, _i64, _p, _p, _p]),
-    "moe_layer_bwd": (_i32, [_p, _p, _p, _p, _i64, _i64, _i64, _i32, _i32, _p, _i64, _p, _p, _p, _p, _p, _p]),
+    "moe_layer_bwd": (_i32, [_p, _p, _p, _p, _i64, _i64, _i64, _i32, _i32, _i32, _p, _i64, _p, _p, _p, _p, _p, _p]),
 }
 
 _lib = None

@@ -55,16 +55,23 @@ struct MxScale {
 };
 
 // amax_bits: max over the block of (float_bits & 0x7fffffff), compared as
-// unsigned integers (NaN patterns compare above +Inf).
-__device__ __forceinline__ MxScale mx_scale_from_amax_bits(uint32_t amax_bits) {
+// unsigned integers (NaN patterns compare above +Inf).  E5: E5M2 elements,
+// whose largest power of two is 2^15 (the scale exponent is then
+// floor(log2 amax) - 15); otherwise E4M3 (2^8).
+template <bool E5>
+__device__ __forceinline__ MxScale mx_scale_from_amax_bits_t(uint32_t amax_bits) {
+  constexpr uint32_t EMAX = E5 ? 15u : 8u;
   MxScale s;
   uint32_t ef = amax_bits >> 23;            // biased exponent of amax
   s.bad = amax_bits >= 0x7f800000u;
-  uint32_t b = ef >= 8u ? ef - 8u : 0u;      // = max(floor(log2 amax) - 8, -127) + 127
+  uint32_t b = ef >= EMAX ? ef - EMAX : 0u;  // = max(floor(log2 amax) - EMAX, -127) + 127
   s.byte = s.bad ? 0xffu : b;
   // 2^-e = 2^(127 - b): biased fp32 exponent 254 - b (b <= 246 for finite inputs)
   s.inv = __uint_as_float((254u - (s.bad ? 127u : b)) << 23);
   return s;
+}
+__device__ __forceinline__ MxScale mx_scale_from_amax_bits(uint32_t amax_bits) {
+  return mx_scale_from_amax_bits_t<false>(amax_bits);
 }
 
 // two fp32 -> two E4M3 bytes (lo = first argument), RNE + saturate to +-448
@@ -73,10 +80,24 @@ __device__ __forceinline__ uint16_t cvt_e4m3x2(float lo, float hi) {
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
   return r;
 }
+// two fp32 -> two E5M2 bytes (lo = first argument), RNE + saturate to +-57344
+__device__ __forceinline__ uint16_t cvt_e5m2x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+template <bool E5>
+__device__ __forceinline__ uint16_t cvt_fp8x2(float lo, float hi) {
+  return E5 ? cvt_e5m2x2(lo, hi) : cvt_e4m3x2(lo, hi);
+}
 
 // four fp32 already multiplied by the inverse scale -> packed 4 bytes
+template <bool E5>
+__device__ __forceinline__ uint32_t pack_fp8x4(float a, float b, float c, float d) {
+  return (uint32_t)cvt_fp8x2<E5>(a, b) | ((uint32_t)cvt_fp8x2<E5>(c, d) << 16);
+}
 __device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float d) {
-  return (uint32_t)cvt_e4m3x2(a, b) | ((uint32_t)cvt_e4m3x2(c, d) << 16);
+  return pack_fp8x4<false>(a, b, c, d);
 }
 
 __device__ __forceinline__ uint32_t abs_bits(float v) { return __float_as_uint(v) & 0x7fffffffu; }
@@ -145,8 +166,10 @@ __device__ __forceinline__ uint32_t vmax_u16x2(uint32_t a, uint32_t b) {
 
 // Four fp32 scaled by `inv` (an exact power of two: every product is exact
 // or an IEEE round-to-nearest result, as with scalar multiplies) in two packed
-// fp32x2 multiplies, then cast to E4M3 and packed, first element lowest.
-__device__ __forceinline__ uint32_t scale_pack_e4m3x4(float a, float b, float c, float d, float inv) {
+// fp32x2 multiplies, then cast to E4M3 (E5: E5M2) and packed, first element
+// lowest.
+template <bool E5>
+__device__ __forceinline__ uint32_t scale_pack_fp8x4(float a, float b, float c, float d, float inv) {
   uint64_t x, y, s2, r1, r2;
   asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(a), "f"(b));
   asm("mov.b64 %0, {%1, %2};" : "=l"(y) : "f"(c), "f"(d));
@@ -155,7 +178,10 @@ __device__ __forceinline__ uint32_t scale_pack_e4m3x4(float a, float b, float c,
   asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r2) : "l"(y), "l"(s2));
   asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r1));
   asm("mov.b64 {%0, %1}, %2;" : "=f"(c), "=f"(d) : "l"(r2));
-  return pack_e4m3x4(a, b, c, d);
+  return pack_fp8x4<E5>(a, b, c, d);
+}
+__device__ __forceinline__ uint32_t scale_pack_e4m3x4(float a, float b, float c, float d, float inv) {
+  return scale_pack_fp8x4<false>(a, b, c, d, inv);
 }
 
 // bf16 helpers (storage as uint16)

@@ -237,7 +237,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           for (int kk = 0; kk < BK / 32; ++kk) {
             const uint64_t ad = smem_desc(sa + kk * 32, 16, 1024, 2);
             const uint64_t bd = smem_desc(sb + kk * 32, 16, 1024, 2);
-            const uint32_t id = idesc_base() | ((uint32_t)kk << 4) | ((uint32_t)kk << 29);
+            const uint32_t id = idesc_base() | p.idesc_fmt | ((uint32_t)kk << 4) | ((uint32_t)kk << 29);
             tc_mma_mxf8(d_tmem, ad, bd, id, sfa_t, sfb_t, (kb | kk) != 0);
           }
           tc_commit(&empty[stage]);
@@ -456,8 +456,11 @@ using namespace mxmoe;
 
 extern "C" mx_status mx_grouped_gemm(int32_t op, const uint8_t *A, const uint8_t *sA, const uint8_t *B,
                                      const uint8_t *sB, const int32_t *offsets, int32_t E, int64_t M_cap, int64_t N,
-                                     int64_t K, void *C, int32_t c_dtype, int32_t *dev_status, mx_stream stream) {
+                                     int64_t K, void *C, int32_t c_dtype, int32_t elem_a, int32_t elem_b,
+                                     int32_t *dev_status, mx_stream stream) {
   MX_HOST_CHECK(op == MX_GEMM_FWD || op == MX_GEMM_DGRAD || op == MX_GEMM_WGRAD, MX_ERR_INVALID_ARG);
+  MX_HOST_CHECK((elem_a == MX_ELEM_E4M3 || elem_a == MX_ELEM_E5M2) && (elem_b == MX_ELEM_E4M3 || elem_b == MX_ELEM_E5M2),
+                MX_ERR_INVALID_ARG);
   MX_HOST_CHECK(A && sA && B && sB && offsets && C, MX_ERR_INVALID_ARG);
   MX_HOST_CHECK(c_dtype == MX_OUT_BF16 || c_dtype == MX_OUT_F32, MX_ERR_INVALID_ARG);
   MX_HOST_CHECK(E >= 1 && E <= gemm::MAX_E && M_cap >= 0 && N > 0 && K > 0, MX_ERR_INVALID_ARG);
@@ -478,6 +481,7 @@ extern "C" mx_status mx_grouped_gemm(int32_t op, const uint8_t *A, const uint8_t
   p.hq = nullptr;
   p.hs = nullptr;
   p.dev_status = dev_status;
+  p.idesc_fmt = gemm::idesc_formats(elem_a == MX_ELEM_E5M2, elem_b == MX_ELEM_E5M2);
   p.epi = c_dtype == MX_OUT_F32 ? gemm::EPI_F32 : gemm::EPI_BF16;
   if (op == MX_GEMM_WGRAD) {
     MX_HOST_CHECK(N % 128 == 0 && K % 256 == 0, MX_ERR_SHAPE);
@@ -521,6 +525,7 @@ extern "C" mx_status moe_gemm1_swiglu(const uint8_t *A, const uint8_t *sA, const
   p.hq = hq;
   p.hs = hs;
   p.dev_status = dev_status;
+  p.idesc_fmt = gemm::idesc_formats(0, 0);
   const int64_t tiles = (M_cap / 128) * (F / 128);
   return gemm::dispatch(p, A, H, M_cap, B, H, (int64_t)E * 2 * F, tiles, M_cap * H / 32, (int64_t)E * 2 * F * H / 32,
                         stream);

@@ -321,7 +321,7 @@ __global__ void __launch_bounds__(P_THREADS, 1)
       int stage = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool dead = false;
-      const uint32_t idesc = idesc_mxf8(2 * BM, C::TN);
+      const uint32_t idesc = idesc_mxf8(2 * BM, C::TN) | p.idesc_fmt;
       const uint32_t d_tmem = tmem_base + C::ACC_COL;
       for (int64_t t = cid; t < ntiles && !dead; t += ncl) {
         const PairTile tl = decode_pair(p, s_off, s_pp, t, rank);

@@ -27,6 +27,7 @@ struct Params {
   uint16_t *ab;
   uint8_t *hq, *hs;
   int32_t *dev_status;
+  uint32_t idesc_fmt;  // element formats of A and B as instruction-descriptor bits (idesc_formats)
 };
 
 // Instruction descriptor, kind::mxf8f6f4 with block scales: E4M3 x E4M3 (format
@@ -36,6 +37,12 @@ struct Params {
 // column in TMEM; they are OR-ed in per MMA.
 __host__ __device__ constexpr uint32_t idesc_mxf8(int M, int N) {
   return (0u << 7) | (0u << 10) | ((uint32_t)(N >> 3) << 17) | (1u << 23) | ((uint32_t)(M >> 4) << 24);
+}
+// Element formats of the two operands in the same descriptor: A's in bits
+// 7-9, B's in bits 10-12, E4M3 = 0 and E5M2 = 1 (kind::mxf8f6f4 takes the two
+// independently).
+__host__ __device__ constexpr uint32_t idesc_formats(int a_e5m2, int b_e5m2) {
+  return ((uint32_t)(a_e5m2 ? 1 : 0) << 7) | ((uint32_t)(b_e5m2 ? 1 : 0) << 10);
 }
 
 // h = silu(a) * b = a * sigma(a) * b in fp32 for bf16 a, b (sigma from

@@ -14,8 +14,9 @@
 #include "common.cuh"
 
 extern "C" mx_status moe_gather_quant(const void *x, const float *gate, const int32_t *src, int64_t T, int64_t H,
-                                      int32_t k, int64_t rows_cap, int32_t mode, uint8_t *q_row, uint8_t *s_row,
-                                      uint8_t *q_col, uint8_t *s_col, const int32_t *row_limit, mx_stream stream);
+                                      int32_t k, int64_t rows_cap, int32_t mode, int32_t elem, uint8_t *q_row,
+                                      uint8_t *s_row, uint8_t *q_col, uint8_t *s_col, const int32_t *row_limit,
+                                      mx_stream stream);
 extern "C" mx_status moe_gate_grad(const void *dOut, const void *y, const int32_t *dst, int64_t T, int64_t H,
                                    int32_t k, float *d_gate, mx_stream stream);
 
@@ -141,10 +142,11 @@ extern "C" mx_status moe_layer_prep_weights(const void *W13, const void *W2, int
   WeightsView v;
   carve_weights(wq, H, F, E, &v);
   // W13[e] is [H, 2F]: ROW blocks run along 2F (dgrad1), COL blocks along H (forward)
-  MX_TRY(mx_quantize(W13, E, H, 2 * F, MX_MODE_BOTH, MX_SCALE_SWIZZLED, v.w13_rq, v.w13_rs, v.w13_cq, v.w13_cs,
-                     stream));
+  MX_TRY(mx_quantize(W13, E, H, 2 * F, MX_MODE_BOTH, MX_SCALE_SWIZZLED, MX_ELEM_E4M3, v.w13_rq, v.w13_rs, v.w13_cq,
+                     v.w13_cs, stream));
   // W2[e] is [F, H]: ROW blocks along H (dgrad2), COL blocks along F (forward)
-  MX_TRY(mx_quantize(W2, E, F, H, MX_MODE_BOTH, MX_SCALE_SWIZZLED, v.w2_rq, v.w2_rs, v.w2_cq, v.w2_cs, stream));
+  MX_TRY(mx_quantize(W2, E, F, H, MX_MODE_BOTH, MX_SCALE_SWIZZLED, MX_ELEM_E4M3, v.w2_rq, v.w2_rs, v.w2_cq, v.w2_cs,
+                     stream));
   return MX_OK;
 }
 
@@ -168,15 +170,18 @@ extern "C" mx_status moe_layer_fwd(const void *x, const float *logits, int32_t *
   MX_TRY(moe_gemm1_swiglu(w.xq, w.xs, v.w13_cq, v.w13_cs, w.offsets, E, R, F, H, w.ab, w.hq, w.hs, dev_status,
                           stream));
   MX_TRY(mx_grouped_gemm(MX_GEMM_FWD, w.hq, w.hs, v.w2_cq, v.w2_cs, w.offsets, E, R, H, F, w.y, MX_OUT_BF16,
-                         dev_status, stream));
+                         MX_ELEM_E4M3, MX_ELEM_E4M3, dev_status, stream));
   MX_TRY(moe_unpermute(w.y, w.dst, gate, T, H, k, out, stream));
   return MX_OK;
 }
 
 extern "C" mx_status moe_layer_bwd(const void *x, const void *dOut, const float *gate, const void *wq, int64_t T,
-                                   int64_t H, int64_t F, int32_t E, int32_t k, void *ws, int64_t ws_bytes, void *dX,
-                                   float *dW13, float *dW2, float *d_gate, int32_t *dev_status, mx_stream stream) {
+                                   int64_t H, int64_t F, int32_t E, int32_t k, int32_t grad_elem, void *ws,
+                                   int64_t ws_bytes, void *dX, float *dW13, float *dW2, float *d_gate,
+                                   int32_t *dev_status, mx_stream stream) {
   MX_HOST_CHECK(wq && ws && dW13 && dW2 && (T == 0 || (x && dOut && dX)), MX_ERR_INVALID_ARG);
+  MX_HOST_CHECK(grad_elem == MX_ELEM_E4M3 || grad_elem == MX_ELEM_E5M2, MX_ERR_INVALID_ARG);
+  const int32_t ge = grad_elem, e4 = MX_ELEM_E4M3;
   MX_TRY(check_dims(T, H, F, E, k));
   MX_HOST_CHECK(ws_bytes >= moe_layer_workspace_size(T, H, F, E, k), MX_ERR_WORKSPACE);
   WeightsView v;
@@ -188,25 +193,25 @@ extern "C" mx_status moe_layer_bwd(const void *x, const void *dOut, const float 
   // dY rows = gate * dOut, quantized along H (dgrad2) and along tokens (wgrad2)
   // (rows past offsets[E], the end of the routed rows, are skipped on the device)
   const int32_t *row_limit = w.offsets + E;
-  MX_TRY(moe_gather_quant(dOut, gate, w.src, T, H, k, R, MX_MODE_BOTH, w.dy_rq, w.dy_rs, w.dy_cq, w.dy_cs, row_limit,
-                          stream));
+  MX_TRY(moe_gather_quant(dOut, gate, w.src, T, H, k, R, MX_MODE_BOTH, ge, w.dy_rq, w.dy_rs, w.dy_cq, w.dy_cs,
+                          row_limit, stream));
   // dh = dY W2^T : B = W2[e] [F, H] quantized along H
   MX_TRY(mx_grouped_gemm(MX_GEMM_DGRAD, w.dy_rq, w.dy_rs, v.w2_rq, v.w2_rs, w.offsets, E, R, F, H, w.dh,
-                         MX_OUT_F32, dev_status, stream));
-  MX_TRY(moe_swiglu_bwd(w.dh, w.ab, R, F, w.dab_rq, w.dab_rs, w.dab_cq, w.dab_cs, w.h_cq, w.h_cs, row_limit,
+                         MX_OUT_F32, ge, e4, dev_status, stream));
+  MX_TRY(moe_swiglu_bwd(w.dh, w.ab, R, F, ge, w.dab_rq, w.dab_rs, w.dab_cq, w.dab_cs, w.h_cq, w.h_cs, row_limit,
                         stream));
   // dW2[e] = h^T dY over the expert's tokens -> [F, H]
   MX_TRY(mx_grouped_gemm(MX_GEMM_WGRAD, w.h_cq, w.h_cs, w.dy_cq, w.dy_cs, w.offsets, E, R, F, H, dW2, MX_OUT_F32,
-                         dev_status, stream));
+                         e4, ge, dev_status, stream));
   // dxp = dab W13^T : B = W13[e] [H, 2F] quantized along 2F
   MX_TRY(mx_grouped_gemm(MX_GEMM_DGRAD, w.dab_rq, w.dab_rs, v.w13_rq, v.w13_rs, w.offsets, E, R, H, 2 * F, w.dxp,
-                         MX_OUT_BF16, dev_status, stream));
+                         MX_OUT_BF16, ge, e4, dev_status, stream));
   // x permuted (bf16) and quantized along tokens for wgrad1
-  MX_TRY(moe_gather_quant(x, nullptr, w.src, T, H, k, R, MX_MODE_COL, nullptr, nullptr, w.xp_cq, w.xp_cs, row_limit,
-                          stream));
+  MX_TRY(moe_gather_quant(x, nullptr, w.src, T, H, k, R, MX_MODE_COL, e4, nullptr, nullptr, w.xp_cq, w.xp_cs,
+                          row_limit, stream));
   // dW13[e] = xp^T dab over the expert's tokens -> [H, 2F]
   MX_TRY(mx_grouped_gemm(MX_GEMM_WGRAD, w.xp_cq, w.xp_cs, w.dab_cq, w.dab_cs, w.offsets, E, R, H, 2 * F, dW13,
-                         MX_OUT_F32, dev_status, stream));
+                         MX_OUT_F32, e4, ge, dev_status, stream));
   MX_TRY(moe_unpermute(w.dxp, w.dst, nullptr, T, H, k, dX, stream));
   return MX_OK;
 }

@@ -38,22 +38,8 @@ struct QuantArgs {
   int32_t swizzled;
 };
 
-// Quantize 32 values that one thread holds; writes 32 bytes to dst (16-B aligned).
-__device__ __forceinline__ uint32_t quant32_store(const float *v, uint8_t *dst) {
-  uint32_t am = 0;
-#pragma unroll
-  for (int i = 0; i < 32; ++i) am = max(am, abs_bits(v[i]));
-  MxScale s = mx_scale_from_amax_bits(am);
-  uint32_t w[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i)
-    w[i] = s.bad ? 0x7f7f7f7fu : scale_pack_e4m3x4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3], s.inv);
-  reinterpret_cast<uint4 *>(dst)[0] = make_uint4(w[0], w[1], w[2], w[3]);
-  reinterpret_cast<uint4 *>(dst)[1] = make_uint4(w[4], w[5], w[6], w[7]);
-  return s.byte;
-}
-
-template <bool ROW, bool COL, bool GATHER>
+template <bool ROW, bool COL, bool GATHER, bool E5 = false>
+// E5: E5M2 elements (the gradient option); otherwise E4M3.
 // 6 resident CTAs per SM (registers capped at 42): 1.5-2% faster than the
 // register-limited 5, measured side by side in one process.  The row amax on
 // packed bf16 pairs and the packed fp32x2 scaling each save ~2.5% (the kernel
@@ -158,10 +144,10 @@ __global__ void __launch_bounds__(QT_THREADS, 6) k_quantize_bf16(QuantArgs a) {
       am = max(am << 16, am & 0xffff0000u);
       am = max(am, __shfl_xor_sync(0xffffffffu, am, 1));
       am = max(am, __shfl_xor_sync(0xffffffffu, am, 2));
-      const MxScale s = mx_scale_from_amax_bits(am);
+      const MxScale s = mx_scale_from_amax_bits_t<E5>(am);
       uint2 o;
-      o.x = s.bad ? 0x7f7f7f7fu : scale_pack_e4m3x4(f[0], f[1], f[2], f[3], s.inv);
-      o.y = s.bad ? 0x7f7f7f7fu : scale_pack_e4m3x4(f[4], f[5], f[6], f[7], s.inv);
+      o.x = s.bad ? 0x7f7f7f7fu : scale_pack_fp8x4<E5>(f[0], f[1], f[2], f[3], s.inv);
+      o.y = s.bad ? 0x7f7f7f7fu : scale_pack_fp8x4<E5>(f[4], f[5], f[6], f[7], s.inv);
       if (valid) {
         *reinterpret_cast<uint2 *>(a.q_row + tile_off + (t_off + (uint32_t)(it * 32) * ucols)) = o;
         if ((tid & 3) == 0) a.s_row[b * a.s_row_stride + rs_base + it * rs_step] = (uint8_t)s.byte;
@@ -181,11 +167,11 @@ __global__ void __launch_bounds__(QT_THREADS, 6) k_quantize_bf16(QuantArgs a) {
     uint32_t am = 0;
 #pragma unroll
     for (int i = 0; i < 32; ++i) am = max(am, abs_bits(f[i]));
-    const MxScale s = mx_scale_from_amax_bits(am);
+    const MxScale s = mx_scale_from_amax_bits_t<E5>(am);
     uint32_t w[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i)
-      w[i] = s.bad ? 0x7f7f7f7fu : scale_pack_e4m3x4(f[4 * i], f[4 * i + 1], f[4 * i + 2], f[4 * i + 3], s.inv);
+      w[i] = s.bad ? 0x7f7f7f7fu : scale_pack_fp8x4<E5>(f[4 * i], f[4 * i + 1], f[4 * i + 2], f[4 * i + 3], s.inv);
     uint4 *dst = reinterpret_cast<uint4 *>(&qcol[col][rb * 32]);
     dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
     dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
@@ -235,6 +221,7 @@ constexpr int SB_Q_STRIDE = SB_ROWS + 16;             // transposed byte row (pa
 constexpr int SB_SMEM = 3 * SB_ROWS * SB_VAL_STRIDE * 4 + 3 * SB_COLS * SB_Q_STRIDE + 3 * SB_COLS * 4;
 
 
+template <bool E5>  // E5: [da|db] with E5M2 elements (the gradient option); h stays E4M3
 __global__ void __launch_bounds__(SB_THREADS) k_swiglu_bwd(const float *__restrict__ dh, const uint16_t *__restrict__ ab,
                                                            int64_t rows, int64_t F, uint8_t *dab_rq, uint8_t *dab_rs,
                                                            uint8_t *dab_cq, uint8_t *dab_cs, uint8_t *h_cq,
@@ -304,12 +291,12 @@ __global__ void __launch_bounds__(SB_THREADS) k_swiglu_bwd(const float *__restri
     ama = max(ama, __shfl_xor_sync(0xffffffffu, ama, 2));
     amb = max(amb, __shfl_xor_sync(0xffffffffu, amb, 1));
     amb = max(amb, __shfl_xor_sync(0xffffffffu, amb, 2));
-    const MxScale sa = mx_scale_from_amax_bits(ama), sbb = mx_scale_from_amax_bits(amb);
+    const MxScale sa = mx_scale_from_amax_bits_t<E5>(ama), sbb = mx_scale_from_amax_bits_t<E5>(amb);
     uint2 oa, ob;
-    oa.x = sa.bad ? 0x7f7f7f7fu : scale_pack_e4m3x4(da[0], da[1], da[2], da[3], sa.inv);
-    oa.y = sa.bad ? 0x7f7f7f7fu : scale_pack_e4m3x4(da[4], da[5], da[6], da[7], sa.inv);
-    ob.x = sbb.bad ? 0x7f7f7f7fu : scale_pack_e4m3x4(db[0], db[1], db[2], db[3], sbb.inv);
-    ob.y = sbb.bad ? 0x7f7f7f7fu : scale_pack_e4m3x4(db[4], db[5], db[6], db[7], sbb.inv);
+    oa.x = sa.bad ? 0x7f7f7f7fu : scale_pack_fp8x4<E5>(da[0], da[1], da[2], da[3], sa.inv);
+    oa.y = sa.bad ? 0x7f7f7f7fu : scale_pack_fp8x4<E5>(da[4], da[5], da[6], da[7], sa.inv);
+    ob.x = sbb.bad ? 0x7f7f7f7fu : scale_pack_fp8x4<E5>(db[0], db[1], db[2], db[3], sbb.inv);
+    ob.y = sbb.bad ? 0x7f7f7f7fu : scale_pack_fp8x4<E5>(db[4], db[5], db[6], db[7], sbb.inv);
     *reinterpret_cast<uint2 *>(dab_t + (uint32_t)r * u2F) = oa;
     *reinterpret_cast<uint2 *>(dab_t + (uint32_t)r * u2F + uF) = ob;
     if (ch == 0) {
@@ -330,11 +317,15 @@ __global__ void __launch_bounds__(SB_THREADS) k_swiglu_bwd(const float *__restri
     uint32_t am = 0;
 #pragma unroll
     for (int i = 0; i < 32; ++i) am = max(am, abs_bits(v[i]));
-    const MxScale s = mx_scale_from_amax_bits(am);
+    // matrices 0, 1 ([da|db]) in the gradient format, 2 (h) in E4M3
+    const bool e5 = E5 && m < 2;
+    const MxScale s = e5 ? mx_scale_from_amax_bits_t<true>(am) : mx_scale_from_amax_bits_t<false>(am);
     uint32_t w[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i)
-      w[i] = s.bad ? 0x7f7f7f7fu : scale_pack_e4m3x4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3], s.inv);
+      w[i] = s.bad ? 0x7f7f7f7fu
+             : e5  ? scale_pack_fp8x4<true>(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3], s.inv)
+                   : scale_pack_fp8x4<false>(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3], s.inv);
     uint4 *dst = reinterpret_cast<uint4 *>(qst + (m * SB_COLS + col) * SB_Q_STRIDE + rb * 32);
     dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
     dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
@@ -385,9 +376,15 @@ constexpr int DQ_THREADS = 128;
 constexpr int DQ_CHUNKS = 4;
 constexpr int DQ_COLS = DQ_THREADS * 16 * DQ_CHUNKS;
 
-__device__ __forceinline__ float2 e4m3x2_to_f32x2(uint32_t two_bytes) {
+// two fp8 bytes -> fp32 pair, exactly (every E4M3 and E5M2 value, +-Inf and
+// NaN included, is an f16 value)
+template <bool E5>
+__device__ __forceinline__ float2 fp8x2_to_f32x2(uint32_t two_bytes) {
   uint32_t h2;
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((uint16_t)two_bytes));
+  if (E5)
+    asm("cvt.rn.f16x2.e5m2x2 %0, %1;" : "=r"(h2) : "h"((uint16_t)two_bytes));
+  else
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((uint16_t)two_bytes));
   return __half22float2(*reinterpret_cast<const __half2 *>(&h2));
 }
 
@@ -431,7 +428,7 @@ __device__ __forceinline__ void dq_store16(void *out, int64_t idx, const float (
   }
 }
 
-template <bool F32>
+template <bool F32, bool E5>
 __global__ void __launch_bounds__(DQ_THREADS) k_dequantize(const uint8_t *__restrict__ q, const uint8_t *__restrict__ s,
                                                            int64_t rows, int64_t cols, int64_t s_stride, int swizzled,
                                                            void *out) {
@@ -461,7 +458,7 @@ __global__ void __launch_bounds__(DQ_THREADS) k_dequantize(const uint8_t *__rest
     float v[16];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const float2 lo = e4m3x2_to_f32x2(wd[i] & 0xffffu), hi = e4m3x2_to_f32x2(wd[i] >> 16);
+      const float2 lo = fp8x2_to_f32x2<E5>(wd[i] & 0xffffu), hi = fp8x2_to_f32x2<E5>(wd[i] >> 16);
       v[4 * i] = lo.x * sc;
       v[4 * i + 1] = lo.y * sc;
       v[4 * i + 2] = hi.x * sc;
@@ -552,6 +549,21 @@ __global__ void __launch_bounds__(RM_THREADS) k_quantize_rowmax(const uint16_t *
   }
 }
 
+// The quantize kernel for one combination of outputs, gather mode and
+// element format (E5: E5M2).
+template <bool GATHER>
+static void launch_quantize(const QuantArgs &a, bool row, bool col, bool e5, dim3 grid, mx_stream stream) {
+  if (e5) {
+    if (row && col) k_quantize_bf16<true, true, GATHER, true><<<grid, QT_THREADS, 0, stream>>>(a);
+    else if (row) k_quantize_bf16<true, false, GATHER, true><<<grid, QT_THREADS, 0, stream>>>(a);
+    else k_quantize_bf16<false, true, GATHER, true><<<grid, QT_THREADS, 0, stream>>>(a);
+  } else {
+    if (row && col) k_quantize_bf16<true, true, GATHER, false><<<grid, QT_THREADS, 0, stream>>>(a);
+    else if (row) k_quantize_bf16<true, false, GATHER, false><<<grid, QT_THREADS, 0, stream>>>(a);
+    else k_quantize_bf16<false, true, GATHER, false><<<grid, QT_THREADS, 0, stream>>>(a);
+  }
+}
+
 }  // namespace mxmoe
 
 using namespace mxmoe;
@@ -587,11 +599,12 @@ extern "C" int64_t mx_scale_bytes(int64_t rows, int64_t cols, int32_t layout) {
 }
 
 extern "C" mx_status mx_quantize(const void *x, int64_t batch, int64_t rows, int64_t cols, int32_t mode,
-                                 int32_t scale_layout, uint8_t *q_row, uint8_t *s_row, uint8_t *q_col,
+                                 int32_t scale_layout, int32_t elem, uint8_t *q_row, uint8_t *s_row, uint8_t *q_col,
                                  uint8_t *s_col, mx_stream stream) {
   MX_HOST_CHECK(x != nullptr, MX_ERR_INVALID_ARG);
   MX_HOST_CHECK(mode == MX_MODE_ROW || mode == MX_MODE_COL || mode == MX_MODE_BOTH, MX_ERR_INVALID_ARG);
   MX_HOST_CHECK(scale_layout == MX_SCALE_PLAIN || scale_layout == MX_SCALE_SWIZZLED, MX_ERR_INVALID_ARG);
+  MX_HOST_CHECK(elem == MX_ELEM_E4M3 || elem == MX_ELEM_E5M2, MX_ERR_INVALID_ARG);
   MX_HOST_CHECK(batch >= 1 && rows >= 1 && cols >= 1, MX_ERR_INVALID_ARG);
   const bool row = mode & MX_MODE_ROW, col = mode & MX_MODE_COL;
   MX_HOST_CHECK(!row || (q_row && s_row), MX_ERR_INVALID_ARG);
@@ -625,19 +638,16 @@ extern "C" mx_status mx_quantize(const void *x, int64_t batch, int64_t rows, int
   }
   const unsigned nrb = (unsigned)((rows + QT_ROWS - 1) / QT_ROWS), ncb = (unsigned)((cols + QT_COLS - 1) / QT_COLS);
   const dim3 grid = row ? dim3(ncb, nrb, (unsigned)batch) : dim3(nrb, ncb, (unsigned)batch);
-  if (row && col)
-    k_quantize_bf16<true, true, false><<<grid, QT_THREADS, 0, stream>>>(a);
-  else if (row)
-    k_quantize_bf16<true, false, false><<<grid, QT_THREADS, 0, stream>>>(a);
-  else
-    k_quantize_bf16<false, true, false><<<grid, QT_THREADS, 0, stream>>>(a);
+  launch_quantize<false>(a, row, col, elem == MX_ELEM_E5M2, grid, stream);
   return launch_status();
 }
 
 extern "C" mx_status mx_dequantize(const uint8_t *q, const uint8_t *s, int64_t batch, int64_t rows, int64_t cols,
-                                   int32_t scale_layout, int32_t out_dtype, void *out, mx_stream stream) {
+                                   int32_t scale_layout, int32_t elem, int32_t out_dtype, void *out,
+                                   mx_stream stream) {
   MX_HOST_CHECK(q && s && out, MX_ERR_INVALID_ARG);
   MX_HOST_CHECK(scale_layout == MX_SCALE_PLAIN || scale_layout == MX_SCALE_SWIZZLED, MX_ERR_INVALID_ARG);
+  MX_HOST_CHECK(elem == MX_ELEM_E4M3 || elem == MX_ELEM_E5M2, MX_ERR_INVALID_ARG);
   MX_HOST_CHECK(out_dtype == MX_OUT_BF16 || out_dtype == MX_OUT_F32, MX_ERR_INVALID_ARG);
   MX_HOST_CHECK(batch >= 1 && rows > 0 && cols > 0, MX_ERR_INVALID_ARG);
   MX_HOST_CHECK(cols % 32 == 0, MX_ERR_SHAPE);
@@ -648,18 +658,25 @@ extern "C" mx_status mx_dequantize(const uint8_t *q, const uint8_t *s, int64_t b
   const dim3 grid((unsigned)(batch * rows), (unsigned)((cols + DQ_COLS - 1) / DQ_COLS));
   const int64_t s_stride = mx_scale_bytes(rows, cols, scale_layout);
   const int swz = scale_layout == MX_SCALE_SWIZZLED;
-  if (out_dtype == MX_OUT_F32)
-    k_dequantize<true><<<grid, DQ_THREADS, 0, stream>>>(q, s, rows, cols, s_stride, swz, out);
+  const bool e5 = elem == MX_ELEM_E5M2;
+  if (out_dtype == MX_OUT_F32 && e5)
+    k_dequantize<true, true><<<grid, DQ_THREADS, 0, stream>>>(q, s, rows, cols, s_stride, swz, out);
+  else if (out_dtype == MX_OUT_F32)
+    k_dequantize<true, false><<<grid, DQ_THREADS, 0, stream>>>(q, s, rows, cols, s_stride, swz, out);
+  else if (e5)
+    k_dequantize<false, true><<<grid, DQ_THREADS, 0, stream>>>(q, s, rows, cols, s_stride, swz, out);
   else
-    k_dequantize<false><<<grid, DQ_THREADS, 0, stream>>>(q, s, rows, cols, s_stride, swz, out);
+    k_dequantize<false, false><<<grid, DQ_THREADS, 0, stream>>>(q, s, rows, cols, s_stride, swz, out);
   return launch_status();
 }
 
 extern "C" mx_status moe_gather_quant(const void *x, const float *gate, const int32_t *src, int64_t T, int64_t H,
-                                      int32_t k, int64_t rows_cap, int32_t mode, uint8_t *q_row, uint8_t *s_row,
-                                      uint8_t *q_col, uint8_t *s_col, const int32_t *row_limit, mx_stream stream) {
+                                      int32_t k, int64_t rows_cap, int32_t mode, int32_t elem, uint8_t *q_row,
+                                      uint8_t *s_row, uint8_t *q_col, uint8_t *s_col, const int32_t *row_limit,
+                                      mx_stream stream) {
   MX_HOST_CHECK(src && (T == 0 || x), MX_ERR_INVALID_ARG);  // T = 0: every row is a zero pad row
   MX_HOST_CHECK(mode == MX_MODE_ROW || mode == MX_MODE_COL || mode == MX_MODE_BOTH, MX_ERR_INVALID_ARG);
+  MX_HOST_CHECK(elem == MX_ELEM_E4M3 || elem == MX_ELEM_E5M2, MX_ERR_INVALID_ARG);
   MX_HOST_CHECK(T >= 0 && H > 0 && k >= 1 && rows_cap >= 0, MX_ERR_INVALID_ARG);
   const bool row = mode & MX_MODE_ROW, col = mode & MX_MODE_COL;
   MX_HOST_CHECK(!row || (q_row && s_row), MX_ERR_INVALID_ARG);
@@ -687,19 +704,15 @@ extern "C" mx_status moe_gather_quant(const void *x, const float *gate, const in
   const unsigned nrb = (unsigned)(rows_cap / QT_ROWS), ncb = (unsigned)(H / QT_COLS);
   MX_HOST_CHECK(nrb < 65535 || !row, MX_ERR_SHAPE);
   const dim3 grid = row ? dim3(ncb, nrb, 1) : dim3(nrb, ncb, 1);
-  if (row && col)
-    k_quantize_bf16<true, true, true><<<grid, QT_THREADS, 0, stream>>>(a);
-  else if (row)
-    k_quantize_bf16<true, false, true><<<grid, QT_THREADS, 0, stream>>>(a);
-  else
-    k_quantize_bf16<false, true, true><<<grid, QT_THREADS, 0, stream>>>(a);
+  launch_quantize<true>(a, row, col, elem == MX_ELEM_E5M2, grid, stream);
   return launch_status();
 }
 
-extern "C" mx_status moe_swiglu_bwd(const float *dh, const void *ab, int64_t rows, int64_t F, uint8_t *dab_rq,
-                                    uint8_t *dab_rs, uint8_t *dab_cq, uint8_t *dab_cs, uint8_t *h_cq,
+extern "C" mx_status moe_swiglu_bwd(const float *dh, const void *ab, int64_t rows, int64_t F, int32_t grad_elem,
+                                    uint8_t *dab_rq, uint8_t *dab_rs, uint8_t *dab_cq, uint8_t *dab_cs, uint8_t *h_cq,
                                     uint8_t *h_cs, const int32_t *row_limit, mx_stream stream) {
   MX_HOST_CHECK(dh && ab && dab_rq && dab_rs && dab_cq && dab_cs && h_cq && h_cs, MX_ERR_INVALID_ARG);
+  MX_HOST_CHECK(grad_elem == MX_ELEM_E4M3 || grad_elem == MX_ELEM_E5M2, MX_ERR_INVALID_ARG);
   MX_HOST_CHECK(rows >= 0 && F > 0, MX_ERR_INVALID_ARG);
   MX_HOST_CHECK(rows % SB_ROWS == 0 && F % SB_COLS == 0 && F / SB_COLS < 65535, MX_ERR_SHAPE);
   MX_HOST_CHECK(aligned16(dh) && aligned16(ab) && aligned16(dab_rq) && aligned16(dab_cq) && aligned16(h_cq),
@@ -713,11 +726,17 @@ extern "C" mx_status moe_swiglu_bwd(const float *dh, const void *ab, int64_t row
   int dev = 0;
   MX_CUDA_TRY(cudaGetDevice(&dev));
   if (dev >= 0 && dev < 64 && !smem_set[dev]) {
-    MX_CUDA_TRY(cudaFuncSetAttribute(k_swiglu_bwd, cudaFuncAttributeMaxDynamicSharedMemorySize, SB_SMEM));
+    MX_CUDA_TRY(cudaFuncSetAttribute(k_swiglu_bwd<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, SB_SMEM));
+    MX_CUDA_TRY(cudaFuncSetAttribute(k_swiglu_bwd<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, SB_SMEM));
     smem_set[dev] = 1;
   }
   dim3 grid((unsigned)(rows / SB_ROWS), (unsigned)(F / SB_COLS));
-  k_swiglu_bwd<<<grid, SB_THREADS, SB_SMEM, stream>>>(dh, static_cast<const uint16_t *>(ab), rows, F, dab_rq, dab_rs,
-                                                      dab_cq, dab_cs, h_cq, h_cs, row_limit);
+  const uint16_t *abp = static_cast<const uint16_t *>(ab);
+  if (grad_elem == MX_ELEM_E5M2)
+    k_swiglu_bwd<true><<<grid, SB_THREADS, SB_SMEM, stream>>>(dh, abp, rows, F, dab_rq, dab_rs, dab_cq, dab_cs, h_cq,
+                                                              h_cs, row_limit);
+  else
+    k_swiglu_bwd<false><<<grid, SB_THREADS, SB_SMEM, stream>>>(dh, abp, rows, F, dab_rq, dab_rs, dab_cq, dab_cs, h_cq,
+                                                               h_cs, row_limit);
   return launch_status();
 }

@@ -73,12 +73,14 @@ extern "C" int64_t mx_wgrad_splitk_workspace_size(int32_t E, int64_t N, int64_t 
 
 extern "C" mx_status mx_grouped_gemm_wgrad_splitk(const uint8_t *A, const uint8_t *sA, const uint8_t *B,
                                                   const uint8_t *sB, const int32_t *offsets, int32_t E,
-                                                  int64_t M_cap, int64_t N, int64_t K, int32_t splits, void *ws,
-                                                  int64_t ws_bytes, float *C, int32_t *dev_status,
-                                                  mx_stream stream) {
+                                                  int64_t M_cap, int64_t N, int64_t K, int32_t splits, int32_t elem_a,
+                                                  int32_t elem_b, void *ws, int64_t ws_bytes, float *C,
+                                                  int32_t *dev_status, mx_stream stream) {
   MX_HOST_CHECK(A && sA && B && sB && offsets && ws && C, MX_ERR_INVALID_ARG);
   MX_HOST_CHECK(splits >= 1 && splits <= 16 && E >= 1 && (int64_t)E * splits <= 1024, MX_ERR_INVALID_ARG);
   MX_HOST_CHECK(M_cap >= 0 && N > 0 && K > 0, MX_ERR_INVALID_ARG);
+  MX_HOST_CHECK((elem_a == MX_ELEM_E4M3 || elem_a == MX_ELEM_E5M2) && (elem_b == MX_ELEM_E4M3 || elem_b == MX_ELEM_E5M2),
+                MX_ERR_INVALID_ARG);
   MX_HOST_CHECK(M_cap % 128 == 0 && N % 256 == 0 && K % 256 == 0, MX_ERR_SHAPE);
   MX_HOST_CHECK(aligned16(ws) && aligned16(C), MX_ERR_ALIGNMENT);
   MX_HOST_CHECK(ws_bytes >= mx_wgrad_splitk_workspace_size(E, N, K, splits), MX_ERR_WORKSPACE);
@@ -89,8 +91,8 @@ extern "C" mx_status mx_grouped_gemm_wgrad_splitk(const uint8_t *A, const uint8_
   k_split_offsets<<<1, 256, 0, stream>>>(offsets, E, splits, M_cap, voff, dev_status);
   st = launch_status();
   if (st != MX_OK) return st;
-  st = mx_grouped_gemm(MX_GEMM_WGRAD, A, sA, B, sB, voff, E * splits, M_cap, N, K, part, MX_OUT_F32, dev_status,
-                       stream);
+  st = mx_grouped_gemm(MX_GEMM_WGRAD, A, sA, B, sB, voff, E * splits, M_cap, N, K, part, MX_OUT_F32, elem_a, elem_b,
+                       dev_status, stream);
   if (st != MX_OK) return st;
   const int64_t per_e4 = N * K / 4;
   int64_t blocks = (per_e4 * E + 255) / 256;

@@ -67,15 +67,15 @@ def assert_bf16_within_one_ulp(got_bits: np.ndarray, ref: np.ndarray, what: str)
     return float(np.mean(diff != 0))
 
 
-def quant_mismatches_outside_margin(got_q, got_s, values, what, rel_margin=2e-6, max_frac=1e-3):
+def quant_mismatches_outside_margin(got_q, got_s, values, what, rel_margin=2e-6, max_frac=1e-3, fmt="e4m3"):
     """Row-quantized bytes of values that the GPU computed in fp32 and the
     oracle in fp64: they must match except where the fp64 value lies within
     ``rel_margin`` (relative) of an E4M3 rounding decision or the block amax
     lies that close to a power of two.  ``rel_margin`` is a number or an array
     of per-element bounds of the GPU's relative error (a block then takes the
     largest bound of its elements).  Returns the count of excused elements."""
-    q_ref, s_ref = mx.quantize_rows(values)
-    elem_rel, block_rel = mx.quantize_margins(values)
+    q_ref, s_ref = mx.quantize_rows(values, fmt)
+    elem_rel, block_rel = mx.quantize_margins(values, fmt)
     rel_margin = np.asarray(rel_margin, np.float64)
     if rel_margin.ndim:
         # the computed amax can reach max_i |v_i| (1 + m_i): a small element

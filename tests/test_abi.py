@@ -43,7 +43,7 @@ def test_status_strings(lib):
     for code in range(0, 10):
         s = lib.mx_status_string(code).decode()
         assert s.startswith("MX_")
-    assert lib.mx_abi_version() == 2
+    assert lib.mx_abi_version() == 3
 
 
 def test_size_queries(lib):
@@ -60,32 +60,32 @@ def test_host_side_argument_errors(lib):
     fake = C.c_void_p(1 << 20)        # never dereferenced: the checks fail first
     odd = C.c_void_p((1 << 20) + 4)
     # null input
-    assert lib.mx_quantize(None, 1, 64, 64, 1, 0, fake, fake, None, None, None) == _lib.MX_ERR_INVALID_ARG
-    assert lib.mx_dequantize(None, fake, 1, 64, 64, 0, 1, fake, None) == _lib.MX_ERR_INVALID_ARG
+    assert lib.mx_quantize(None, 1, 64, 64, 1, 0, 0, fake, fake, None, None, None) == _lib.MX_ERR_INVALID_ARG
+    assert lib.mx_dequantize(None, fake, 1, 64, 64, 0, 0, 1, fake, None) == _lib.MX_ERR_INVALID_ARG
     # T = 0: the token arrays may be NULL (the argument checks pass; without a
     # GPU the device check then fails)
     assert lib.moe_route(None, 0, 4, 1, None, None, None) != _lib.MX_ERR_INVALID_ARG
     assert lib.moe_route(None, 5, 4, 1, None, None, None) == _lib.MX_ERR_INVALID_ARG
     assert lib.moe_unpermute(None, None, None, 0, 64, 1, None, None) != _lib.MX_ERR_INVALID_ARG
-    assert lib.mx_dequantize(fake, fake, 1, 64, 64, 2, 1, fake, None) == _lib.MX_ERR_INVALID_ARG
-    assert lib.mx_dequantize(fake, fake, 1, 64, 64, 0, 5, fake, None) == _lib.MX_ERR_INVALID_ARG
-    assert lib.mx_dequantize(fake, fake, 1, 64, 48, 0, 1, fake, None) == _lib.MX_ERR_SHAPE
-    assert lib.mx_dequantize(C.c_void_p((1 << 20) + 8), fake, 1, 64, 64, 0, 1, fake, None) == _lib.MX_ERR_ALIGNMENT
+    assert lib.mx_dequantize(fake, fake, 1, 64, 64, 2, 0, 1, fake, None) == _lib.MX_ERR_INVALID_ARG
+    assert lib.mx_dequantize(fake, fake, 1, 64, 64, 0, 0, 5, fake, None) == _lib.MX_ERR_INVALID_ARG
+    assert lib.mx_dequantize(fake, fake, 1, 64, 48, 0, 0, 1, fake, None) == _lib.MX_ERR_SHAPE
+    assert lib.mx_dequantize(C.c_void_p((1 << 20) + 8), fake, 1, 64, 64, 0, 0, 1, fake, None) == _lib.MX_ERR_ALIGNMENT
     # unknown mode / layout
-    assert lib.mx_quantize(fake, 1, 64, 64, 7, 0, fake, fake, None, None, None) == _lib.MX_ERR_INVALID_ARG
-    assert lib.mx_quantize(fake, 1, 64, 64, 1, 5, fake, fake, None, None, None) == _lib.MX_ERR_INVALID_ARG
+    assert lib.mx_quantize(fake, 1, 64, 64, 7, 0, 0, fake, fake, None, None, None) == _lib.MX_ERR_INVALID_ARG
+    assert lib.mx_quantize(fake, 1, 64, 64, 1, 5, 0, fake, fake, None, None, None) == _lib.MX_ERR_INVALID_ARG
     # cols not a multiple of 32
-    assert lib.mx_quantize(fake, 1, 64, 48, 1, 0, fake, fake, None, None, None) == _lib.MX_ERR_SHAPE
+    assert lib.mx_quantize(fake, 1, 64, 48, 1, 0, 0, fake, fake, None, None, None) == _lib.MX_ERR_SHAPE
     # misaligned
-    assert lib.mx_quantize(odd, 1, 64, 64, 1, 0, fake, fake, None, None, None) == _lib.MX_ERR_ALIGNMENT
+    assert lib.mx_quantize(odd, 1, 64, 64, 1, 0, 0, fake, fake, None, None, None) == _lib.MX_ERR_ALIGNMENT
     # GEMM shape rules
-    assert lib.mx_grouped_gemm(0, fake, fake, fake, fake, fake, 4, 256, 200, 256, fake, 1, None, None) == \
+    assert lib.mx_grouped_gemm(0, fake, fake, fake, fake, fake, 4, 256, 200, 256, fake, 1, 0, 0, None, None) == \
         _lib.MX_ERR_SHAPE
-    assert lib.mx_grouped_gemm(0, fake, fake, fake, fake, fake, 4, 100, 256, 256, fake, 1, None, None) == \
+    assert lib.mx_grouped_gemm(0, fake, fake, fake, fake, fake, 4, 100, 256, 256, fake, 1, 0, 0, None, None) == \
         _lib.MX_ERR_SHAPE
-    assert lib.mx_grouped_gemm(9, fake, fake, fake, fake, fake, 4, 256, 256, 256, fake, 1, None, None) == \
+    assert lib.mx_grouped_gemm(9, fake, fake, fake, fake, fake, 4, 256, 256, 256, fake, 1, 0, 0, None, None) == \
         _lib.MX_ERR_INVALID_ARG
-    assert lib.mx_grouped_gemm(0, fake, fake, fake, fake, fake, 0, 256, 256, 256, fake, 1, None, None) == \
+    assert lib.mx_grouped_gemm(0, fake, fake, fake, fake, fake, 0, 256, 256, 256, fake, 1, 0, 0, None, None) == \
         _lib.MX_ERR_INVALID_ARG
     # permute map: rows_cap too small, workspace too small
     assert lib.moe_permute_map(fake, 100, 2, 4, 128, fake, fake, fake, fake, fake, 1 << 20, None, None) == \
@@ -106,14 +106,19 @@ def test_host_side_argument_errors(lib):
     big = lib.mx_wgrad_splitk_workspace_size(4, 256, 256, 2)
     assert big == 256 + 4 * 2 * 256 * 256 * 4
     assert lib.mx_wgrad_splitk_workspace_size(4, 256, 256, 17) == -1
-    assert lib.mx_grouped_gemm_wgrad_splitk(fake, fake, fake, fake, fake, 4, 256, 256, 256, 0, fake, big, fake, None,
+    assert lib.mx_grouped_gemm_wgrad_splitk(fake, fake, fake, fake, fake, 4, 256, 256, 256, 0, 0, 0, fake, big, fake, None,
                                             None) == _lib.MX_ERR_INVALID_ARG
-    assert lib.mx_grouped_gemm_wgrad_splitk(fake, fake, fake, fake, fake, 512, 256, 256, 256, 4, fake, 1 << 40, fake,
+    assert lib.mx_grouped_gemm_wgrad_splitk(fake, fake, fake, fake, fake, 512, 256, 256, 256, 4, 0, 0, fake, 1 << 40, fake,
                                             None, None) == _lib.MX_ERR_INVALID_ARG
-    assert lib.mx_grouped_gemm_wgrad_splitk(fake, fake, fake, fake, fake, 4, 256, 256, 256, 2, fake, big - 1, fake,
+    assert lib.mx_grouped_gemm_wgrad_splitk(fake, fake, fake, fake, fake, 4, 256, 256, 256, 2, 0, 0, fake, big - 1, fake,
                                             None, None) == _lib.MX_ERR_WORKSPACE
-    assert lib.mx_grouped_gemm_wgrad_splitk(fake, fake, fake, fake, fake, 4, 256, 256, 384, 2, fake, 1 << 40, fake,
+    assert lib.mx_grouped_gemm_wgrad_splitk(fake, fake, fake, fake, fake, 4, 256, 256, 384, 2, 0, 0, fake, 1 << 40, fake,
                                             None, None) == _lib.MX_ERR_SHAPE
+    # element formats: only E4M3 (0) and E5M2 (1)
+    assert lib.mx_quantize(fake, 1, 64, 64, 1, 0, 2, fake, fake, None, None, None) == _lib.MX_ERR_INVALID_ARG
+    assert lib.mx_dequantize(fake, fake, 1, 64, 64, 0, 7, 1, fake, None) == _lib.MX_ERR_INVALID_ARG
+    assert lib.mx_grouped_gemm(0, fake, fake, fake, fake, fake, 4, 256, 256, 256, fake, 1, 0, 3, None, None) == \
+        _lib.MX_ERR_INVALID_ARG
     # sigmoid self-test: negative count, null buffers
     assert lib.mx_selftest_sigmoid(fake, -1, fake, None) == _lib.MX_ERR_INVALID_ARG
     assert lib.mx_selftest_sigmoid(None, 4, fake, None) == _lib.MX_ERR_INVALID_ARG
@@ -129,7 +134,7 @@ def test_swiglu_bwd_word_written_scales_must_be_4_byte_aligned(lib):
     from mxfp8_mixture_experts_gb300 import _lib
     base = 1 << 20
     f = C.c_void_p(base)
-    args = lambda dab_rs, dab_cs, h_cs: (f, f, 256, 64, f, dab_rs, f, dab_cs, f, h_cs, None, None)
+    args = lambda dab_rs, dab_cs, h_cs: (f, f, 256, 64, 0, f, dab_rs, f, dab_cs, f, h_cs, None, None)
     for off in (1, 2, 3):
         assert lib.moe_swiglu_bwd(*args(f, C.c_void_p(base + off), f)) == _lib.MX_ERR_ALIGNMENT
         assert lib.moe_swiglu_bwd(*args(f, f, C.c_void_p(base + off))) == _lib.MX_ERR_ALIGNMENT

@@ -304,7 +304,7 @@ def test_row_limit_skips_rows_past_the_groups(dev):
 
     def run(limit):
         o = {n: torch.full((k,), 0xAB, dtype=torch.uint8, device=dev) for n, k in shapes.items()}
-        assert L.moe_swiglu_bwd(dh.data_ptr(), ab.data_ptr(), R, F, *(o[n].data_ptr() for n in shapes),
+        assert L.moe_swiglu_bwd(dh.data_ptr(), ab.data_ptr(), R, F, 0, *(o[n].data_ptr() for n in shapes),
                                 None if limit is None else limit.data_ptr(), s) == 0
         return o
 
@@ -335,7 +335,7 @@ def test_row_limit_skips_rows_past_the_groups(dev):
 
     def gq(limit):
         o = {n: torch.full((k_,), 0xAB, dtype=torch.uint8, device=dev) for n, k_ in shapes.items()}
-        assert L.moe_gather_quant(x.data_ptr(), None, src.data_ptr(), T, H, k, R, m.MX_MODE_BOTH,
+        assert L.moe_gather_quant(x.data_ptr(), None, src.data_ptr(), T, H, k, R, m.MX_MODE_BOTH, 0,
                                   *(o[n].data_ptr() for n in shapes), None if limit is None else limit.data_ptr(),
                                   s) == 0
         return o

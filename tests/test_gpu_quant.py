@@ -82,7 +82,7 @@ def test_quantize_unaligned_scale_pointers(dev):
     sr = torch.zeros(nb + 16, dtype=torch.uint8, device=dev)
     sc = torch.zeros(nbc + 16, dtype=torch.uint8, device=dev)
     s = torch.cuda.current_stream(dev).cuda_stream
-    code = L.mx_quantize(x.data_ptr(), 1, R, Cc, 3, 1, qr.data_ptr(), sr.data_ptr() + 1, qc.data_ptr(),
+    code = L.mx_quantize(x.data_ptr(), 1, R, Cc, 3, 1, 0, qr.data_ptr(), sr.data_ptr() + 1, qc.data_ptr(),
                          sc.data_ptr() + 1, s)
     assert code == 0
     torch.cuda.synchronize()
