@@ -43,10 +43,12 @@ FP8_PER_BF16 = 2.0   # nominal dense fp8 / bf16 tensor rate (4.5 / 2.25 PFLOP/s)
 # (dram__bytes_read.sum + dram__bytes_write.sum per launch, summed), from an
 # ncu capture of those launches alone.  Valid only for the GEMM sources it was
 # taken on (checked by hash); reported as null otherwise.
-GEMM_TRAFFIC_BYTES_PER_STEP = None
-GEMM_TRAFFIC_HOW = None
+GEMM_TRAFFIC_BYTES_PER_STEP = 15317935872
+GEMM_TRAFFIC_HOW = ("ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum -k regex:k_grouped_gemm_pair "
+                    "-s 6 -c 6 on this full-size layer step (T=16384, H=5120, E=16, F=8192, top-1): "
+                    "1.026x the algorithmic bytes")
 GEMM_TRAFFIC_SOURCES = ("gemm_pair.cu", "gemm_shared.cuh", "common.cuh")
-GEMM_TRAFFIC_SHA256 = None
+GEMM_TRAFFIC_SHA256 = "7ca34d9aec1d585cfd07be39157d46e3962ddfab5c43591c54397d640d905dcc"
 
 
 def _gemm_sources_sha256():
@@ -859,7 +861,10 @@ def main():
         bf16 = _bf16_layer_bench(dev, d, inp, steps=min(args.steps, 10), warmup=2)
         bf16["mxfp8_speedup"] = bf16["ms_per_step"] / ms
 
-    traffic = GEMM_TRAFFIC_BYTES_PER_STEP if GEMM_TRAFFIC_SHA256 == _gemm_sources_sha256() else None
+    # the capture is of the default workload only: full sizes, top-1, E4M3 gradients
+    default_work = args.T is None and args.E is None and args.k in (None, 1) and args.grad_format == "e4m3"
+    traffic = (GEMM_TRAFFIC_BYTES_PER_STEP if default_work and GEMM_TRAFFIC_SHA256 == _gemm_sources_sha256()
+               else None)
     line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "fp8",
@@ -875,7 +880,7 @@ def main():
                          "traffic": traffic,
                          "traffic_unit": "DRAM bytes per step of the 6 GEMM launches",
                          "traffic_how": GEMM_TRAFFIC_HOW if traffic is not None else
-                         "null: no ncu capture of the current GEMM sources",
+                         "null: no ncu capture of the current GEMM sources on this workload",
                          "algorithmic_bytes": _gemm_alg_bytes(d, R=routed),
                          "peak_source": f"{src} bf16_tflops / bf16_tflops_sustained x {FP8_PER_BF16} (nominal "
                                         f"dense fp8/bf16 ratio)"},
