@@ -403,8 +403,8 @@ mx_status moe_gemm1_swiglu(const uint8_t *A, const uint8_t *sA, const uint8_t *B
  * Arithmetic: fp32; sigmoid(a) from the hardware's approximate base-2
  * exponential and reciprocal with an exactly rounded exponent (see
  * mx_selftest_sigmoid): a few fp32 ulps over bf16 a in [-128, 128].
- * Alignment: dab_cs and h_cs must be 4-byte aligned (each column's four
- * row-block scales are written as one 32-bit word); dab_rs may sit at any byte.
+ * Alignment: dh, ab, dab_rq, dab_cq and h_cq 16-byte aligned; the scale
+ * arrays dab_rs, dab_cs and h_cs may sit at any byte.
  */
 mx_status moe_swiglu_bwd(const float *dh, const void *ab, int64_t rows,
                          int64_t F, int32_t grad_elem, uint8_t *dab_rq, uint8_t *dab_rs,

@@ -206,20 +206,108 @@ __global__ void __launch_bounds__(QT_THREADS, 6) k_quantize_bf16(QuantArgs a) {
 // SwiGLU backward + quantization (see moe_swiglu_bwd in mxmoe.h).
 // Tile: 128 rows x 32 columns of F, 256 threads.
 //   phase 1  two (row, 8-column) chunks per thread, all loads issued first;
-//            da, db, h in fp32; ROW quant of da and db (4 lanes per block);
-//            da, db, h staged in shared memory;
+//            da, db, h in fp32, two columns per packed f32x2 instruction;
+//            ROW quant of da and db (4 lanes per block); da, db, h staged
+//            in shared memory;
 //   phase 2  COL quant of the three staged matrices (32 x 4 column blocks
 //            each) into a staged transposed tile;
 //   phase 3  full 128-byte line writes of the transposed tiles and their
 //            scales.
+// The kernel issues about as many instructions as its bytes take at HBM
+// speed, so the arithmetic is packed: the products and fused multiply-adds
+// of two columns share one f32x2 instruction (each lane is an IEEE fp32
+// operation, identical to the scalar one) and a block amax takes one
+// max-of-magnitudes per element.  Measured side by side on the layer's
+// 17792 x 8192 case, bytes identical: 6% faster than the scalar form.  (A
+// lane-per-column variant without the fp32 staging, and 16-byte staging
+// stores, were both slower.)
 // ---------------------------------------------------------------------------
 constexpr int SB_ROWS = 128;
 constexpr int SB_COLS = 32;
 constexpr int SB_THREADS = 256;
-constexpr int SB_VAL_STRIDE = SB_COLS + 1;            // fp32 staging row (padded)
+constexpr int SB_VAL_STRIDE = SB_COLS + 1;            // fp32 staging row (padded: conflict-free)
 constexpr int SB_Q_STRIDE = SB_ROWS + 16;             // transposed byte row (padded)
 constexpr int SB_SMEM = 3 * SB_ROWS * SB_VAL_STRIDE * 4 + 3 * SB_COLS * SB_Q_STRIDE + 3 * SB_COLS * 4;
 
+// packed fp32 pairs (lane 0 = the first element)
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float &lo, float &hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+
+// max(|a|, |b|) as a magnitude (its sign bit is meaningless: callers take
+// abs_bits of the result); NaN in either input gives NaN, so abs_bits of a
+// chain of these is the block's abs_bits maximum with NaN and Inf above
+// every finite value, as mx_scale_from_amax_bits_t expects.
+__device__ __forceinline__ float max_mag(float a, float b) {
+  float r;
+  asm("max.NaN.xorsign.abs.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+  return r;
+}
+
+// The sigmoid pieces of sigmoid_parts for two bf16 values at once: the same
+// operations, with the products and fused multiply-adds packed.
+struct SigParts2 {
+  uint64_t s, oms, back;
+};
+__device__ __forceinline__ SigParts2 sigmoid_parts2(float a0, float a1) {
+  const float aa0 = fminf(fabsf(a0), 256.0f), aa1 = fminf(fabsf(a1), 256.0f);
+  const bool far0 = a0 < -64.0f, far1 = a1 < -64.0f;
+  const uint64_t aa = f2_pack(aa0, aa1);
+  const uint64_t arg = f2_fma(aa, f2_pack(-LOG2E_HI, -LOG2E_HI), f2_pack(far0 ? 64.0f : 0.0f, far1 ? 64.0f : 0.0f));
+  float x0, x1;
+  f2_unpack(arg, x0, x1);
+  const uint64_t t0 = f2_pack(ex2_approx(x0), ex2_approx(x1));
+  const uint64_t y = f2_mul(aa, f2_pack(LOG2E_REM_LN, LOG2E_REM_LN));
+  const uint64_t q = f2_fma(y, f2_fma(f2_pack(0.5f, 0.5f), y, f2_pack(-1.0f, -1.0f)), f2_pack(1.0f, 1.0f));
+  const uint64_t t = f2_mul(t0, q);
+  float u0, u1;
+  f2_unpack(f2_add(f2_pack(1.0f, 1.0f), t), u0, u1);
+  const uint64_t r = f2_pack(rcp_approx(far0 ? 1.0f : u0), rcp_approx(far1 ? 1.0f : u1));
+  const uint64_t tr = f2_mul(t, r);
+  float r0, r1, tr0, tr1;
+  f2_unpack(r, r0, r1);
+  f2_unpack(tr, tr0, tr1);
+  SigParts2 p;
+  p.s = f2_pack(a0 >= 0.0f ? r0 : tr0, a1 >= 0.0f ? r1 : tr1);
+  p.oms = f2_pack(a0 >= 0.0f ? tr0 : r0, a1 >= 0.0f ? tr1 : r1);
+  p.back = f2_pack(far0 ? 0x1p-64f : 1.0f, far1 ? 0x1p-64f : 1.0f);
+  return p;
+}
+
+// da, db, h of two columns (d, a, b packed): the operations of the scalar
+// reading, in the same order,
+//   silu = a s,  h = (silu b) back,  db = (d silu) back,
+//   da = (((d b) s) (1 + a oms)) back
+__device__ __forceinline__ void swiglu_bwd2(uint64_t d, float a0, float a1, uint64_t b, uint64_t &da, uint64_t &db,
+                                            uint64_t &h) {
+  const SigParts2 p = sigmoid_parts2(a0, a1);
+  const uint64_t a = f2_pack(a0, a1);
+  const uint64_t silu = f2_mul(a, p.s);
+  const uint64_t g = f2_fma(a, p.oms, f2_pack(1.0f, 1.0f));
+  da = f2_mul(f2_mul(f2_mul(f2_mul(d, b), p.s), g), p.back);
+  db = f2_mul(f2_mul(d, silu), p.back);
+  h = f2_mul(f2_mul(silu, b), p.back);
+}
 
 template <bool E5>  // E5: [da|db] with E5M2 elements (the gradient option); h stays E4M3
 __global__ void __launch_bounds__(SB_THREADS) k_swiglu_bwd(const float *__restrict__ dh, const uint16_t *__restrict__ ab,
@@ -246,13 +334,13 @@ __global__ void __launch_bounds__(SB_THREADS) k_swiglu_bwd(const float *__restri
   const float *dh_t = dh + row0 * F + gf;
   const uint16_t *ab_t = ab + row0 * twoF + gf;
   uint8_t *dab_t = dab_rq + row0 * twoF + gf;
-  float4 d0[2], d1[2];
+  ulonglong2 d0[2], d1[2];  // dh columns 0..3 and 4..7 as packed pairs
   uint4 av[2], bv[2];
 #pragma unroll
   for (int it = 0; it < 2; ++it) {
     const uint32_t r = (uint32_t)(it * 64 + rt);
-    d0[it] = *reinterpret_cast<const float4 *>(dh_t + r * uF);
-    d1[it] = *reinterpret_cast<const float4 *>(dh_t + r * uF + 4);
+    d0[it] = *reinterpret_cast<const ulonglong2 *>(dh_t + r * uF);
+    d1[it] = *reinterpret_cast<const ulonglong2 *>(dh_t + r * uF + 4);
     av[it] = *reinterpret_cast<const uint4 *>(ab_t + r * u2F);
     bv[it] = *reinterpret_cast<const uint4 *>(ab_t + r * u2F + uF);
   }
@@ -266,32 +354,32 @@ __global__ void __launch_bounds__(SB_THREADS) k_swiglu_bwd(const float *__restri
 #pragma unroll
   for (int it = 0; it < 2; ++it) {
     const int r = it * 64 + rt;
-    const float d[8] = {d0[it].x, d0[it].y, d0[it].z, d0[it].w, d1[it].x, d1[it].y, d1[it].z, d1[it].w};
-    const float A[8] = {bf16_lo(av[it].x), bf16_hi(av[it].x), bf16_lo(av[it].y), bf16_hi(av[it].y),
-                        bf16_lo(av[it].z), bf16_hi(av[it].z), bf16_lo(av[it].w), bf16_hi(av[it].w)};
-    const float B[8] = {bf16_lo(bv[it].x), bf16_hi(bv[it].x), bf16_lo(bv[it].y), bf16_hi(bv[it].y),
-                        bf16_lo(bv[it].z), bf16_hi(bv[it].z), bf16_lo(bv[it].w), bf16_hi(bv[it].w)};
-    float da[8], db[8];
-    uint32_t ama = 0, amb = 0;
+    const uint64_t dp[4] = {d0[it].x, d0[it].y, d1[it].x, d1[it].y};
+    const uint32_t aw[4] = {av[it].x, av[it].y, av[it].z, av[it].w};
+    const uint32_t bw[4] = {bv[it].x, bv[it].y, bv[it].z, bv[it].w};
+    float da[8], db[8], hh[8];
+    float ma = 0.0f, mb = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      uint64_t da2, db2, h2;
+      swiglu_bwd2(dp[j], bf16_lo(aw[j]), bf16_hi(aw[j]), f2_pack(bf16_lo(bw[j]), bf16_hi(bw[j])), da2, db2, h2);
+      f2_unpack(da2, da[2 * j], da[2 * j + 1]);
+      f2_unpack(db2, db[2 * j], db[2 * j + 1]);
+      f2_unpack(h2, hh[2 * j], hh[2 * j + 1]);
+      ma = max_mag(ma, max_mag(da[2 * j], da[2 * j + 1]));
+      mb = max_mag(mb, max_mag(db[2 * j], db[2 * j + 1]));
+    }
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      // sigma(a) (scaled by 2^64 for a < -64, undone by `back` in the last
-      // product) and 1 - sigma(a), each without cancellation
-      const SigParts p = sigmoid_parts(A[i]);
-      const float silu = A[i] * p.s;
-      da[i] = ((d[i] * B[i]) * p.s * (1.0f + A[i] * p.oms)) * p.back;
-      db[i] = (d[i] * silu) * p.back;
       vals[(0 * SB_ROWS + r) * SB_VAL_STRIDE + ch * 8 + i] = da[i];
       vals[(1 * SB_ROWS + r) * SB_VAL_STRIDE + ch * 8 + i] = db[i];
-      vals[(2 * SB_ROWS + r) * SB_VAL_STRIDE + ch * 8 + i] = (silu * B[i]) * p.back;
-      ama = max(ama, abs_bits(da[i]));
-      amb = max(amb, abs_bits(db[i]));
+      vals[(2 * SB_ROWS + r) * SB_VAL_STRIDE + ch * 8 + i] = hh[i];
     }
-    ama = max(ama, __shfl_xor_sync(0xffffffffu, ama, 1));
-    ama = max(ama, __shfl_xor_sync(0xffffffffu, ama, 2));
-    amb = max(amb, __shfl_xor_sync(0xffffffffu, amb, 1));
-    amb = max(amb, __shfl_xor_sync(0xffffffffu, amb, 2));
-    const MxScale sa = mx_scale_from_amax_bits_t<E5>(ama), sbb = mx_scale_from_amax_bits_t<E5>(amb);
+    ma = max_mag(ma, __shfl_xor_sync(0xffffffffu, ma, 1));
+    ma = max_mag(ma, __shfl_xor_sync(0xffffffffu, ma, 2));
+    mb = max_mag(mb, __shfl_xor_sync(0xffffffffu, mb, 1));
+    mb = max_mag(mb, __shfl_xor_sync(0xffffffffu, mb, 2));
+    const MxScale sa = mx_scale_from_amax_bits_t<E5>(abs_bits(ma)), sbb = mx_scale_from_amax_bits_t<E5>(abs_bits(mb));
     uint2 oa, ob;
     oa.x = sa.bad ? 0x7f7f7f7fu : scale_pack_fp8x4<E5>(da[0], da[1], da[2], da[3], sa.inv);
     oa.y = sa.bad ? 0x7f7f7f7fu : scale_pack_fp8x4<E5>(da[4], da[5], da[6], da[7], sa.inv);
@@ -314,9 +402,14 @@ __global__ void __launch_bounds__(SB_THREADS) k_swiglu_bwd(const float *__restri
     float v[32];
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = vals[(m * SB_ROWS + rb * 32 + i) * SB_VAL_STRIDE + col];
-    uint32_t am = 0;
+    float mm[16];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) am = max(am, abs_bits(v[i]));
+    for (int i = 0; i < 16; ++i) mm[i] = max_mag(v[2 * i], v[2 * i + 1]);
+#pragma unroll
+    for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+      for (int i = 0; i < w; ++i) mm[i] = max_mag(mm[i], mm[i + w]);
+    const uint32_t am = abs_bits(mm[0]);
     // matrices 0, 1 ([da|db]) in the gradient format, 2 (h) in E4M3
     const bool e5 = E5 && m < 2;
     const MxScale s = e5 ? mx_scale_from_amax_bits_t<true>(am) : mx_scale_from_amax_bits_t<false>(am);
@@ -348,16 +441,15 @@ __global__ void __launch_bounds__(SB_THREADS) k_swiglu_bwd(const float *__restri
       *reinterpret_cast<uint4 *>(h_cq + (f0 + col) * rows + row0 + part * 16) = val;
     }
   }
-  if (tid < 3 * SB_COLS) {
-    const int m = tid / SB_COLS, col = tid % SB_COLS;
-    const uint32_t sc = *reinterpret_cast<const uint32_t *>(sst + tid * 4);
-    // 4 consecutive row blocks of one transposed row: 4 contiguous bytes of the tiled layout
-    if (m < 2) {
-      const int64_t orow = (m == 0 ? 0 : F) + f0 + col;
-      *reinterpret_cast<uint32_t *>(dab_cs + sf_swizzle_offset(orow, row0 / 32, round_up(rblocks_total, 4))) = sc;
-    } else {
-      *reinterpret_cast<uint32_t *>(h_cs + sf_swizzle_offset(f0 + col, row0 / 32, round_up(rblocks_total, 4))) = sc;
-    }
+  for (int i = tid; i < 3 * SB_COLS * 4; i += SB_THREADS) {
+    // one scale byte per (transposed row, row block); the 4 row blocks of a
+    // transposed row are 4 consecutive bytes of the tiled layout
+    const int mr = i >> 2, rb = i & 3;
+    const int m = mr / SB_COLS, col = mr % SB_COLS;
+    const uint8_t sc = sst[i];
+    const int64_t orow = (m == 1 ? F : 0) + f0 + col;
+    uint8_t *base = m < 2 ? dab_cs : h_cs;
+    base[sf_swizzle_offset(orow, row0 / 32 + rb, round_up(rblocks_total, 4))] = sc;
   }
 }
 
@@ -717,8 +809,6 @@ extern "C" mx_status moe_swiglu_bwd(const float *dh, const void *ab, int64_t row
   MX_HOST_CHECK(rows % SB_ROWS == 0 && F % SB_COLS == 0 && F / SB_COLS < 65535, MX_ERR_SHAPE);
   MX_HOST_CHECK(aligned16(dh) && aligned16(ab) && aligned16(dab_rq) && aligned16(dab_cq) && aligned16(h_cq),
                 MX_ERR_ALIGNMENT);
-  // the column scales leave as 32-bit words (four row blocks of one column)
-  MX_HOST_CHECK(aligned4(dab_cs) && aligned4(h_cs), MX_ERR_ALIGNMENT);
   mx_status st = check_device_cached();
   if (st != MX_OK) return st;
   if (rows == 0) return MX_OK;

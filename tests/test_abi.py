@@ -124,22 +124,28 @@ def test_host_side_argument_errors(lib):
     assert lib.mx_selftest_sigmoid(None, 4, fake, None) == _lib.MX_ERR_INVALID_ARG
 
 
-def test_swiglu_bwd_word_written_scales_must_be_4_byte_aligned(lib):
-    """moe_swiglu_bwd writes each column's four row-block scales of dab_cs and
-    h_cs as one 32-bit word: a scale pointer off a 4-byte boundary is refused
-    on the host with MX_ERR_ALIGNMENT before anything is launched (the same
-    call with aligned pointers gets past every argument check and stops only
-    at the device check of this GPU-less machine).  dab_rs is written byte by
-    byte and may sit at any offset."""
+def test_swiglu_bwd_alignment_rules(lib):
+    """moe_swiglu_bwd writes every scale byte by byte, so dab_rs, dab_cs and
+    h_cs may sit at any offset: such calls get past every argument check and
+    stop only at the device check of this GPU-less machine.  Its data
+    pointers (dh, ab, dab_rq, dab_cq, h_cq) take 16-byte vector accesses: one
+    off a 16-byte boundary is refused on the host with MX_ERR_ALIGNMENT before
+    anything is launched."""
     from mxfp8_mixture_experts_gb300 import _lib
     base = 1 << 20
     f = C.c_void_p(base)
+    ok = {_lib.MX_ERR_UNSUPPORTED_DEVICE, _lib.MX_ERR_CUDA}
     args = lambda dab_rs, dab_cs, h_cs: (f, f, 256, 64, 0, f, dab_rs, f, dab_cs, f, h_cs, None, None)
     for off in (1, 2, 3):
-        assert lib.moe_swiglu_bwd(*args(f, C.c_void_p(base + off), f)) == _lib.MX_ERR_ALIGNMENT
-        assert lib.moe_swiglu_bwd(*args(f, f, C.c_void_p(base + off))) == _lib.MX_ERR_ALIGNMENT
-    ok = {_lib.MX_ERR_UNSUPPORTED_DEVICE, _lib.MX_ERR_CUDA}
-    assert lib.moe_swiglu_bwd(*args(C.c_void_p(base + 1), C.c_void_p(base + 4), C.c_void_p(base + 8))) in ok
+        o = C.c_void_p(base + off)
+        assert lib.moe_swiglu_bwd(*args(o, f, f)) in ok
+        assert lib.moe_swiglu_bwd(*args(f, o, f)) in ok
+        assert lib.moe_swiglu_bwd(*args(f, f, o)) in ok
+    for pos in (0, 1, 5, 7, 9):  # dh, ab, dab_rq, dab_cq, h_cq
+        for off in (4, 8):
+            a = list(args(f, f, f))
+            a[pos] = C.c_void_p(base + off)
+            assert lib.moe_swiglu_bwd(*a) == _lib.MX_ERR_ALIGNMENT
 
 
 def test_package_imports_and_fails_loudly_without_library(tmp_path):

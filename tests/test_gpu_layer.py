@@ -285,6 +285,38 @@ def test_swiglu_bwd_standalone(dev, rows, F):
     quant_mismatches_outside_margin(u8(h_cq), mx.unswizzle_scales(u8(h_cs), F, rows // 32), h.T.copy(), "h cols")
 
 
+def test_swiglu_bwd_scales_at_any_byte(dev):
+    """moe_swiglu_bwd writes every scale byte on its own, so its three scale
+    arrays may start at any byte: with dab_rs, dab_cs and h_cs placed 1, 2
+    and 3 bytes past a 16-byte boundary, every output is bit-identical to
+    the call with aligned scale arrays, and the bytes before each array are
+    untouched."""
+    import mxfp8_mixture_experts_gb300 as m
+    L = m.lib()
+    s = torch.cuda.current_stream(dev).cuda_stream
+    R, F = 256, 96
+    g = workloads.generator(33, dev)
+    ab = workloads.randn_bf16((R, 2 * F), 1.0, g, dev)
+    dh = torch.randn((R, F), generator=g, device=dev)
+    sb = lambda r, c: m.mx_scale_bytes(r, c, m.MX_SCALE_SWIZZLED)
+    sizes = {"dab_rq": R * 2 * F, "dab_rs": sb(R, 2 * F), "dab_cq": 2 * F * R, "dab_cs": sb(2 * F, R),
+             "h_cq": F * R, "h_cs": sb(F, R)}
+    shift = {"dab_rq": 0, "dab_rs": 1, "dab_cq": 0, "dab_cs": 2, "h_cq": 0, "h_cs": 3}
+
+    def run(offsets):
+        bufs = {n: torch.full((k + 16,), 0xAB, dtype=torch.uint8, device=dev) for n, k in sizes.items()}
+        assert L.moe_swiglu_bwd(dh.data_ptr(), ab.data_ptr(), R, F, 0,
+                                *(bufs[n].data_ptr() + offsets[n] for n in sizes), None, s) == 0
+        return bufs
+
+    ref, shifted = run({n: 0 for n in sizes}), run(shift)
+    torch.cuda.synchronize()
+    for n, k in sizes.items():
+        o = shift[n]
+        assert np.array_equal(u8(shifted[n])[o:o + k], u8(ref[n])[:k]), n
+        assert np.all(u8(shifted[n])[:o] == 0xAB), n
+
+
 def test_row_limit_skips_rows_past_the_groups(dev):
     """moe_swiglu_bwd and moe_gather_quant with a device row limit (the layer
     passes offsets[E], where the routed rows end): every output of a row
