@@ -330,15 +330,12 @@ mx_status make_map_u8_128x128(CUtensorMap *m, const void *base, int64_t inner, i
   return make_map_u8_128x128_swz(m, base, inner, outer, (int)CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-static mx_status make_map_u8_box_swz(CUtensorMap *m, const void *base, int64_t inner, int64_t outer, int box_rows,
-                                     int swizzle);
-
 mx_status make_map_u8_128x128_swz(CUtensorMap *m, const void *base, int64_t inner, int64_t outer, int swizzle) {
   return make_map_u8_box_swz(m, base, inner, outer, 128, swizzle);
 }
 
-static mx_status make_map_u8_box_swz(CUtensorMap *m, const void *base, int64_t inner, int64_t outer, int box_rows,
-                                     int swizzle) {
+mx_status make_map_u8_box_swz(CUtensorMap *m, const void *base, int64_t inner, int64_t outer, int box_rows,
+                              int swizzle) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return MX_ERR_CUDA;
   if (box_rows < 1 || box_rows > 256) return MX_ERR_INVALID_ARG;

@@ -21,8 +21,15 @@
 // the accumulator (bf16/fp32 outputs leave through swizzled shared-memory
 // staging and TMA tensor stores, so each global write is a full 64-byte row
 // segment).  Row groups are 128-row aligned; a group with an odd number of
-// 128-row tiles ends in a "lone" tile, computed by the pair with both halves
-// on the same rows and stored by the even CTA only.
+// 128-row tiles ends in a "lone" tile.  With bf16 or fp32 outputs the pair
+// computes it transposed: the 256 weight rows of the column tile are the
+// M=256 operand (each CTA its own 128, as the B half it loads for a full
+// tile) and the lone tile's 128 rows are an N=128 operand (64 per CTA), so
+// no product is computed twice; each CTA stores its 128 output columns, one
+// per TMEM lane, as coalesced row segments.  In the SwiGLU epilogue the two
+// halves of a feature pair would land in different CTAs, so there the pair
+// computes the lone tile with both halves on the same rows and the even CTA
+// stores it.
 #include "gemm_shared.cuh"
 
 #include <mutex>
@@ -42,6 +49,7 @@ struct PairCfg {
   static constexpr int B_TILE = 128 * BK;              // 16 KB: this CTA's half of the B tile
   static constexpr int SF_STAGE = 3 * 512;             // own SFA chunk + both SFB chunks
   static constexpr uint32_t STAGE_TX = A_TILE + B_TILE + SF_STAGE;
+  static constexpr uint32_t TR_STAGE_TX = A_TILE + B_TILE / 2 + 2 * 512;  // transposed lone tile
   static constexpr uint32_t ACC_COL = 0;               // accumulator: TMEM columns [0, 256)
   static constexpr uint32_t SF_COL = 256;              // scales: 12 columns per stage from here
   static constexpr uint32_t SF_COLS = 12;
@@ -68,6 +76,7 @@ struct PairTile {
   int64_t sfa_chunk, sfb_chunk0, sfb_chunk1;  // chunk index of the k=0 scales
   int64_t out_row, out_col;                   // this CTA's output rows / first column
   bool store;                                 // false: lone tile, odd CTA
+  bool tr;                                    // transposed lone tile (see the header)
 };
 
 __device__ __forceinline__ int64_t pair_tiles(const Params &p, const int32_t *pp) {
@@ -111,6 +120,19 @@ __device__ __forceinline__ PairTile decode_pair(const Params &p, const int32_t *
     }
     tl.k0 = 0;
     tl.num_k = (int)kblocks;
+    tl.tr = lone && p.epi != EPI_GLU;
+    if (tl.tr) {
+      // M side: this CTA's 128 weight rows; N side: 64 of the lone tile's 128
+      // rows; the accumulator is [weight row, token row]
+      tl.a_row = rank == 0 ? tl.b_row0 : tl.b_row1;
+      tl.b_row = mt0 * BM + rank * 64;
+      tl.sfa_chunk = (tl.a_row / 128) * kblocks;
+      tl.sfb_chunk0 = tl.sfb_chunk1 = mt0 * kblocks;
+      tl.out_row = mt0 * BM;
+      tl.out_col += rank * 128;
+      tl.store = true;
+      return tl;
+    }
     tl.sfa_chunk = my_mt * kblocks;
     tl.sfb_chunk0 = (tl.b_row0 / 128) * kblocks;
     tl.sfb_chunk1 = (tl.b_row1 / 128) * kblocks;
@@ -142,6 +164,7 @@ __device__ __forceinline__ PairTile decode_pair(const Params &p, const int32_t *
     tl.out_row = (int64_t)e * p.N + rt * 256 + rank * 128;
     tl.out_col = ct * BN;
     tl.store = true;
+    tl.tr = false;
   }
   tl.b_row = rank == 0 ? tl.b_row0 : tl.b_row1;
   return tl;
@@ -218,7 +241,7 @@ __global__ void __launch_bounds__(P_THREADS, 1)
     k_grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
                         const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmH,
-                        Params p) {
+                        const __grid_constant__ CUtensorMap tmA64, Params p) {
   using C = PairCfg;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -263,6 +286,7 @@ __global__ void __launch_bounds__(P_THREADS, 1)
     prefetch_tmap(&tmSFB);
     prefetch_tmap(&tmC);
     if (p.epi == EPI_GLU) prefetch_tmap(&tmH);
+    else prefetch_tmap(&tmA64);
   }
   __syncthreads();
   if (!*s_flag) return;  // identical decision in both CTAs of the pair
@@ -293,17 +317,25 @@ __global__ void __launch_bounds__(P_THREADS, 1)
             break;
           }
           if (elect_one_sync()) {
-            if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * C::STAGE_TX);
+            if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * (tl.tr ? C::TR_STAGE_TX : C::STAGE_TX));
             const uint32_t bar = leader_full0 + stage * 8;
             uint8_t *sa = smem + C::SMEM_A + stage * C::A_TILE;
             uint8_t *sb = smem + C::SMEM_B + stage * C::B_TILE;
             uint8_t *sf = smem + C::SMEM_SF + stage * C::SF_STAGE;
             const int32_t kc = (int32_t)(tl.k0 + (int64_t)kb * BK);
-            tma_load_2d_pair(sa, &tmA, bar, kc, (int32_t)tl.a_row);
-            tma_load_2d_pair(sb, &tmB, bar, kc, (int32_t)tl.b_row);
-            tma_load_2d_pair(sf, &tmSFA, bar, 0, (int32_t)(tl.sfa_chunk + kb));
-            tma_load_2d_pair(sf + 512, &tmSFB, bar, 0, (int32_t)(tl.sfb_chunk0 + kb));
-            tma_load_2d_pair(sf + 1024, &tmSFB, bar, 0, (int32_t)(tl.sfb_chunk1 + kb));
+            if (tl.tr) {
+              // weights as the M operand, 64 token rows as this CTA's N half
+              tma_load_2d_pair(sa, &tmB, bar, kc, (int32_t)tl.a_row);
+              tma_load_2d_pair(sb, &tmA64, bar, kc, (int32_t)tl.b_row);
+              tma_load_2d_pair(sf, &tmSFB, bar, 0, (int32_t)(tl.sfa_chunk + kb));
+              tma_load_2d_pair(sf + 512, &tmSFA, bar, 0, (int32_t)(tl.sfb_chunk0 + kb));
+            } else {
+              tma_load_2d_pair(sa, &tmA, bar, kc, (int32_t)tl.a_row);
+              tma_load_2d_pair(sb, &tmB, bar, kc, (int32_t)tl.b_row);
+              tma_load_2d_pair(sf, &tmSFA, bar, 0, (int32_t)(tl.sfa_chunk + kb));
+              tma_load_2d_pair(sf + 512, &tmSFB, bar, 0, (int32_t)(tl.sfb_chunk0 + kb));
+              tma_load_2d_pair(sf + 1024, &tmSFB, bar, 0, (int32_t)(tl.sfb_chunk1 + kb));
+            }
           }
           __syncwarp();
           if (++stage == C::STAGES) {
@@ -321,11 +353,15 @@ __global__ void __launch_bounds__(P_THREADS, 1)
       int stage = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool dead = false;
-      const uint32_t idesc = idesc_mxf8(2 * BM, C::TN) | p.idesc_fmt;
+      const uint32_t idesc_full = idesc_mxf8(2 * BM, C::TN) | p.idesc_fmt;
+      // transposed lone tile: N = 128, and the operands' formats trade places
+      const uint32_t idesc_tr = idesc_mxf8(2 * BM, 128) | (((p.idesc_fmt >> 7) & 7u) << 10) |
+                                (((p.idesc_fmt >> 10) & 7u) << 7);
       const uint32_t d_tmem = tmem_base + C::ACC_COL;
       for (int64_t t = cid; t < ntiles && !dead; t += ncl) {
         const PairTile tl = decode_pair(p, s_off, s_pp, t, rank);
         if (tl.num_k == 0) continue;
+        const uint32_t idesc = tl.tr ? idesc_tr : idesc_full;
         if (!mbar_wait_warp(tmem_empty, acc_phase ^ 1, WAIT_TIMEOUT_NS)) {
           if (lane == 0) set_status(p.dev_status, MX_ERR_TIMEOUT);
           break;
@@ -347,7 +383,7 @@ __global__ void __launch_bounds__(P_THREADS, 1)
             // scales of this stage -> TMEM (in tensor-pipe order before the MMAs that read them)
             tc_cp_32x128b_warpx4_pair(sfa_t, smem_desc(sf, 0, 128, 0));
             tc_cp_32x128b_warpx4_pair(sfb_t, smem_desc(sf + 512, 0, 128, 0));
-            tc_cp_32x128b_warpx4_pair(sfb_t + 4, smem_desc(sf + 1024, 0, 128, 0));
+            if (!tl.tr) tc_cp_32x128b_warpx4_pair(sfb_t + 4, smem_desc(sf + 1024, 0, 128, 0));
 #pragma unroll
             for (int kk = 0; kk < BK / 32; ++kk) {
               const uint64_t ad = smem_desc(sa + kk * 32, 16, 1024, 2);
@@ -396,6 +432,29 @@ __global__ void __launch_bounds__(P_THREADS, 1)
       tc_fence_after();
       const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16) + C::ACC_COL;
       uint32_t r[EC];
+      if (tl.tr) {
+        // transposed lone tile: lane = output column out_col + q*32 + lane,
+        // accumulator columns [h*64, h*64 + 64) = token rows out_row + h*64 + j
+        MX_TMEM_LD_32x32b_x32(t_row + h * 64, r);
+        MX_TMEM_LD_32x32b_x32(t_row + h * 64 + 32, (r + 32));
+        tc_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster_relaxed(leader_tmem_empty);
+        acc_phase ^= 1;
+        const int64_t row0 = tl.out_row + h * 64;
+        const int64_t col = tl.out_col + q * 32 + lane;
+        if (p.epi == EPI_F32) {
+          float *c = static_cast<float *>(p.C) + row0 * p.N + col;
+#pragma unroll
+          for (int j = 0; j < 64; ++j) c[j * p.N] = __uint_as_float(r[j]);
+        } else {
+          uint16_t *c = static_cast<uint16_t *>(p.C) + row0 * p.N + col;
+#pragma unroll
+          for (int j = 0; j < 64; ++j) c[j * p.N] = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(r[j])));
+        }
+        continue;
+      }
       if (p.epi == EPI_GLU) {
         // GEMM1: columns [0,128) hold a, [128,256) the matching b
         MX_TMEM_LD_32x32b_x32(t_row + h * 64, r);
@@ -502,8 +561,9 @@ mx_status launch_pair(const Params &p, const uint8_t *A, int64_t a_inner, int64_
     }
     clusters = g_pclusters[dev];
   }
-  CUtensorMap ma, mb, msa, msb, mc, mh;
+  CUtensorMap ma, mb, msa, msb, mc, mh, ma64;
   mx_status st = make_map_u8_128x128(&ma, A, a_inner, a_outer);
+  if (st == MX_OK) st = make_map_u8_box_swz(&ma64, A, a_inner, a_outer, 64, (int)CU_TENSOR_MAP_SWIZZLE_128B);
   if (st == MX_OK) st = make_map_u8_128x128(&mb, B, b_inner, b_outer);
   if (st == MX_OK) st = make_map_sf_chunks(&msa, p.sA, sfa_bytes / 512);
   if (st == MX_OK) st = make_map_sf_chunks(&msb, p.sB, sfb_bytes / 512);
@@ -521,7 +581,7 @@ mx_status launch_pair(const Params &p, const uint8_t *A, int64_t a_inner, int64_
   cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attr;
   pair_config(&cfg, &attr, 2 * clusters, stream);
-  MX_CUDA_TRY(cudaLaunchKernelEx(&cfg, k_grouped_gemm_pair, ma, mb, msa, msb, mc, mh, p));
+  MX_CUDA_TRY(cudaLaunchKernelEx(&cfg, k_grouped_gemm_pair, ma, mb, msa, msb, mc, mh, ma64, p));
   return launch_status();
 }
 

@@ -150,6 +150,9 @@ __device__ __forceinline__ void epi_store(const Params &p, int64_t orow, int64_t
 // host
 mx_status make_map_u8_128x128(CUtensorMap *m, const void *base, int64_t inner, int64_t outer);
 mx_status make_map_u8_128x128_swz(CUtensorMap *m, const void *base, int64_t inner, int64_t outer, int swizzle);
+// 2-D uint8 map over [outer, inner], boxes of 128 bytes x box_rows
+mx_status make_map_u8_box_swz(CUtensorMap *m, const void *base, int64_t inner, int64_t outer, int box_rows,
+                              int swizzle);
 mx_status make_map_sf_chunks(CUtensorMap *m, const void *base, int64_t nchunks);
 mx_status make_map_store_64b(CUtensorMap *m, void *base, bool f32, int64_t cols, int64_t rows);
 mx_status make_map_store_64b_u8(CUtensorMap *m, void *base, int64_t cols, int64_t rows);
