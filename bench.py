@@ -43,12 +43,12 @@ FP8_PER_BF16 = 2.0   # nominal dense fp8 / bf16 tensor rate (4.5 / 2.25 PFLOP/s)
 # (dram__bytes_read.sum + dram__bytes_write.sum per launch, summed), from an
 # ncu capture of those launches alone.  Valid only for the GEMM sources it was
 # taken on (checked by hash); reported as null otherwise.
-GEMM_TRAFFIC_BYTES_PER_STEP = 15317935872
+GEMM_TRAFFIC_BYTES_PER_STEP = 15318272512
 GEMM_TRAFFIC_HOW = ("ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum -k regex:k_grouped_gemm_pair "
                     "-s 6 -c 6 on this full-size layer step (T=16384, H=5120, E=16, F=8192, top-1): "
                     "1.026x the algorithmic bytes")
 GEMM_TRAFFIC_SOURCES = ("gemm_pair.cu", "gemm_shared.cuh", "common.cuh")
-GEMM_TRAFFIC_SHA256 = "7ca34d9aec1d585cfd07be39157d46e3962ddfab5c43591c54397d640d905dcc"
+GEMM_TRAFFIC_SHA256 = "209c16daa081ddbd940ce69fcca380ae8bcdb83f873e53bab285e56ff65e6220"
 
 
 def _gemm_sources_sha256():
