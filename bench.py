@@ -499,7 +499,10 @@ def _tiny_layer_bench(dev, iters=20):
     """Tiny MoE layer workload (T=512, H=256, E=4, F=512, top-1 ids uniform
     over experts, gate 1): one fwd+bwd step of the same launches as the full
     layer (no router: the ids are given), each step timed with CUDA events
-    after an L2 flush.  Launch- and latency-bound at this size."""
+    after an L2 flush.  Launch- and latency-bound at this size, so the step
+    is also captured once into a CUDA graph and timed as graph replays (the
+    library makes no host synchronisation, so the whole step captures); the
+    eager time is reported beside it."""
     import mxfp8_mixture_experts_gb300 as m
     dims = workloads.TINY_LAYER
     d = m.MoELayerDims(T=dims.T, H=dims.H, F=dims.F, E=dims.E, k=dims.k)
@@ -507,20 +510,37 @@ def _tiny_layer_bench(dev, iters=20):
     step = LayerStep(d, inp, dev)
     s = torch.cuda.current_stream(dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
-    times = []
-    for i in range(iters + 3):
-        flush.zero_()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(s)
-        step.run(s)
-        e1.record(s)
-        torch.cuda.synchronize()
-        if i >= 3:
-            times.append(e0.elapsed_time(e1) * 1e-3)
+
+    def timed(fn):
+        times = []
+        for i in range(iters + 3):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s)
+            fn()
+            e1.record(s)
+            torch.cuda.synchronize()
+            if i >= 3:
+                times.append(e0.elapsed_time(e1) * 1e-3)
+        return statistics.median(times)
+
+    t_eager = timed(lambda: step.run(s))
     assert int(step.b["status"].item()) == 0
-    t = statistics.median(times)
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(s)
+    with torch.cuda.stream(side):
+        step.run(side)
+    s.wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step.run(torch.cuda.current_stream(dev))
+    t = timed(graph.replay)
+    assert int(step.b["status"].item()) == 0
     flops = sum(_gemm_flops(d, dims.T * dims.k).values())
     return {"us_per_step": t * 1e6, "TFLOP/s": flops / t / 1e12, "flops": flops,
+            "us_per_step_eager": t_eager * 1e6,
+            "how": "CUDA graph of the step's launches, replayed (eager launches beside it)",
             "workload": f"tiny MoE layer fwd+bwd: T={dims.T}, H={dims.H}, E={dims.E}, F={dims.F}, top-1 ids "
                         f"uniform, gate 1", "launches": sum(LayerStep.KERNELS) - 1,
             "l2": "flushed (256 MiB write) before each step"}
@@ -821,6 +841,29 @@ def main():
     elapsed = _reduce_max(elapsed, dev)
     assert int(step.b["status"].item()) == 0, "device status set during the timed steps"
 
+    # the same step captured once into a CUDA graph and replayed: how much of
+    # the step is launch overhead (context; the line's value is the eager run)
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        step.run(side)
+    stream.wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step.run(torch.cuda.current_stream(dev))
+    graph.replay()
+    torch.cuda.synchronize()
+    g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    g0.record(stream)
+    for _ in range(args.steps):
+        graph.replay()
+    g1.record(stream)
+    torch.cuda.synchronize()
+    graph_ms = g0.elapsed_time(g1) / args.steps
+    assert int(step.b["status"].item()) == 0, "device status set during the graph replays"
+    del graph
+
     per = {n: [] for n in LayerStep.NAMES}
     for evs in all_events:
         for i, n in enumerate(LayerStep.NAMES):
@@ -885,6 +928,7 @@ def main():
                          "peak_source": f"{src} bf16_tflops / bf16_tflops_sustained x {FP8_PER_BF16} (nominal "
                                         f"dense fp8/bf16 ratio)"},
             "value_excl_weight_prep": total_flops / (ms * 1e-3 - avg['quantize W13'] - avg['quantize W2']) / 1e12,
+            "ms_per_step_cuda_graph": graph_ms,
             "kernels_ms": {n: round(v * 1e3, 4) for n, v in avg.items()},
             "gemm_tflops": {n: round(gf[n] / avg[n] / 1e12, 1) for n in gf},
             "gemm_frac": {n: round(gf[n] / avg[n] / 1e12 / pk["chosen"], 3) for n in gf},

@@ -449,6 +449,69 @@ def test_layer_is_deterministic():
                            v.view(torch.uint8) if v.dtype != torch.int32 else v)
 
 
+def test_layer_replays_from_a_cuda_graph():
+    """The layer API makes no host synchronisation and keeps the group sizes
+    on the device, so weight prep, forward and backward can be captured into
+    one CUDA graph.  Replays match eager calls bit for bit, and a replay after
+    new inputs are copied into the captured buffers computes on those inputs
+    (nothing is frozen at capture time but the buffers' addresses)."""
+    import mxfp8_mixture_experts_gb300 as m
+    dev = torch.device("cuda", 0)
+    d = m.MoELayerDims(T=512, H=256, F=512, E=4, k=2)
+    dims = workloads.LayerDims(T=d.T, H=d.H, E=d.E, F=d.F, k=d.k)
+    inputs = [workloads.layer_inputs(dims, seed=s, device=dev, router="logits") for s in (13, 14)]
+    W13 = [torch.cat([i["W1"], i["W3"]], dim=2).contiguous() for i in inputs]
+
+    def eager(i):
+        wq = m.moe_layer_prep_weights(W13[i], inputs[i]["W2"])
+        ws = torch.empty(m.moe_layer_workspace_size(d), dtype=torch.uint8, device=dev)
+        out, ids, gate = m.moe_layer_fwd(inputs[i]["x"], wq, d, ws, logits=inputs[i]["logits"])
+        dX, dW13, dW2, dg = m.moe_layer_bwd(inputs[i]["x"], inputs[i]["dOut"], gate, wq, d, ws)
+        torch.cuda.synchronize()
+        return [t.clone() for t in (out, ids, gate, dX, dW13, dW2, dg)]
+
+    ref = [eager(0), eager(1)]
+    # static buffers, filled with the first inputs
+    sx, slog, sdo = inputs[0]["x"].clone(), inputs[0]["logits"].clone(), inputs[0]["dOut"].clone()
+    sW13, sW2 = W13[0].clone(), inputs[0]["W2"].clone()
+    wq = torch.empty(m.moe_layer_weights_size(d.H, d.F, d.E), dtype=torch.uint8, device=dev)
+    ws = torch.empty(m.moe_layer_workspace_size(d), dtype=torch.uint8, device=dev)
+    out = torch.empty((d.T, d.H), dtype=torch.bfloat16, device=dev)
+    ids = torch.empty((d.T, d.k), dtype=torch.int32, device=dev)
+    gate = torch.empty((d.T, d.k), dtype=torch.float32, device=dev)
+    dX = torch.empty((d.T, d.H), dtype=torch.bfloat16, device=dev)
+    dW13 = torch.empty((d.E, d.H, 2 * d.F), dtype=torch.float32, device=dev)
+    dW2 = torch.empty((d.E, d.F, d.H), dtype=torch.float32, device=dev)
+    dg = torch.empty((d.T, d.k), dtype=torch.float32, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def step():
+        m.moe_layer_prep_weights(sW13, sW2, wq)
+        m.moe_layer_fwd(sx, wq, d, ws, logits=slog, ids=ids, gate=gate, out=out, dev_status=st)
+        m.moe_layer_bwd(sx, sdo, gate, wq, d, ws, dX=dX, dW13=dW13, dW2=dW2, d_gate=dg, dev_status=st)
+
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(side):
+        step()  # warm-up on the capture stream's side (one-time set-up happens here)
+    torch.cuda.current_stream(dev).wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    for i in (0, 1, 0):
+        sx.copy_(inputs[i]["x"]); slog.copy_(inputs[i]["logits"]); sdo.copy_(inputs[i]["dOut"])
+        sW13.copy_(W13[i]); sW2.copy_(inputs[i]["W2"])
+        for t in (out, dX, dW13, dW2, dg):
+            t.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        for u, v in zip((out, ids, gate, dX, dW13, dW2, dg), ref[i]):
+            assert torch.equal(u.view(torch.uint8) if u.dtype != torch.int32 else u,
+                               v.view(torch.uint8) if v.dtype != torch.int32 else v)
+
+
 # ---------------------------------------------------------------------------
 # full-size layer (T=16384, H=5120, E=16, F=8192, top-1 softmax router): every
 # stage checked on sampled outputs that the oracle computes one at a time, on
