@@ -23,7 +23,13 @@
  *     owned by the caller; the library never allocates or frees memory and
  *     keeps no state between calls.  Outputs must not alias inputs.
  *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
- *     stream) and runs asynchronously; nothing synchronizes the host.
+ *     stream) and runs asynchronously; nothing synchronizes the host, and
+ *     group sizes stay on the device, so a sequence of calls can be captured
+ *     into a CUDA graph and replayed.  Kernels are launched with programmatic
+ *     dependent launch: each one waits for the previous work of the stream
+ *     to complete before it touches memory, so stream order is kept, while
+ *     its launch overlaps the end of that work.  Setting the environment
+ *     variable MXMOE_PDL=0 before the first call launches them plainly.
  *   - Errors found on the device (expert id out of range, bad group offsets,
  *     a pipeline wait that timed out) are written to the optional
  *     `dev_status` word (device int32, nullable) as an mx_status value; the

@@ -1,6 +1,8 @@
 // Library-level entry points: status strings, ABI version, device check.
 #include "common.cuh"
 
+#include <cstdlib>
+
 #include <mutex>
 
 namespace mxmoe {
@@ -28,10 +30,19 @@ mx_status launch_status() {
   return e == cudaSuccess ? MX_OK : MX_ERR_CUDA;
 }
 
+bool pdl_enabled() {
+  static const bool on = [] {
+    const char *v = std::getenv("MXMOE_PDL");
+    return !(v && v[0] == '0');
+  }();
+  return on;
+}
+
 // One warp waits, with the kernels' own bounded warp-wide wait, on an mbarrier
 // that nothing ever arrives on; when the limit passes it records
 // MX_ERR_TIMEOUT and exits.  Nothing is in flight when it returns.
 __global__ void k_selftest_wait_timeout(uint64_t timeout_ns, int32_t *dev_status) {
+  pdl_enter();
   __shared__ __align__(8) uint64_t bar;
   if (threadIdx.x == 0) {
     mbar_init(&bar, 1);
@@ -44,6 +55,7 @@ __global__ void k_selftest_wait_timeout(uint64_t timeout_ns, int32_t *dev_status
 // The SwiGLU kernels' sigmoid pieces (sigmoid_parts), evaluated on bf16 inputs:
 // out[3i] = s, out[3i+1] = 1 - sigma, out[3i+2] = back (sigma = s * back).
 __global__ void k_selftest_sigmoid(const uint16_t *__restrict__ a, int64_t n, float *__restrict__ out) {
+  pdl_enter();
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
     const SigParts p = sigmoid_parts(__uint_as_float((uint32_t)a[i] << 16));
     out[3 * i] = p.s;
@@ -60,7 +72,7 @@ extern "C" mx_status mx_selftest_sigmoid(const void *a, int64_t n, float *out, m
   if (st != MX_OK) return st;
   if (n == 0) return MX_OK;
   const int64_t blocks = (n + 255) / 256;
-  mxmoe::k_selftest_sigmoid<<<(unsigned)(blocks < 4096 ? blocks : 4096), 256, 0, stream>>>(
+  (void)mxmoe::launch_k(mxmoe::k_selftest_sigmoid, (unsigned)(blocks < 4096 ? blocks : 4096), 256, 0, stream, 
       static_cast<const uint16_t *>(a), n, out);
   return mxmoe::launch_status();
 }
@@ -70,7 +82,7 @@ extern "C" mx_status mx_selftest_wait_timeout(int64_t timeout_ns, int32_t *dev_s
   MX_HOST_CHECK(timeout_ns > 0 && timeout_ns <= 100000000, MX_ERR_INVALID_ARG);  // at most 100 ms
   mx_status st = mxmoe::check_device_cached();
   if (st != MX_OK) return st;
-  mxmoe::k_selftest_wait_timeout<<<1, 32, 0, stream>>>((uint64_t)timeout_ns, dev_status);
+  (void)mxmoe::launch_k(mxmoe::k_selftest_wait_timeout, 1, 32, 0, stream, (uint64_t)timeout_ns, dev_status);
   return mxmoe::launch_status();
 }
 

@@ -31,6 +31,39 @@ static inline bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>
 
 mx_status check_device_cached();  // defined in api.cu
 mx_status launch_status();        // cudaGetLastError -> mx_status
+bool pdl_enabled();               // defined in api.cu (MXMOE_PDL=0 at process start turns it off)
+
+// ---------------------------------------------------------------------------
+// Programmatic dependent launch.  Every kernel of the library is launched
+// with programmatic stream serialization and begins with pdl_enter(): the
+// wait makes the previous grid of the stream complete, with its writes
+// visible, before any thread of this grid touches global memory; the trigger
+// then lets the next grid's CTAs be scheduled, which happens once every CTA
+// of this grid has issued it (all of them resident), so the next grid's
+// launch overlaps this grid's tail instead of following its completion.  A
+// grid waiting in pdl_enter() never holds resources its predecessor still
+// needs: the predecessor's CTAs were all resident before it was scheduled.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_enter() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                            Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_enabled() ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
 
 // ---------------------------------------------------------------------------
 // device status word

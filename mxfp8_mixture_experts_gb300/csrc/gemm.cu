@@ -121,6 +121,7 @@ __device__ __forceinline__ Tile decode_tile(const Params &p, const int32_t *off,
 
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     k_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, Params p) {
+  pdl_enter();
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + SMEM_BAR);
@@ -423,7 +424,7 @@ mx_status launch_1cta(const Params &p, const uint8_t *A, int64_t a_inner, int64_
   if (st != MX_OK) return st;
   int64_t grid = max_tiles < sms ? max_tiles : sms;
   if (grid < 1) grid = 1;
-  k_grouped_gemm<<<(unsigned)grid, NUM_THREADS, SMEM_ALLOC, stream>>>(ma, mb, p);
+  (void)launch_k(k_grouped_gemm, (unsigned)grid, NUM_THREADS, SMEM_ALLOC, stream, ma, mb, p);
   return launch_status();
 }
 

@@ -242,6 +242,7 @@ __global__ void __launch_bounds__(P_THREADS, 1)
                         const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
                         const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmH,
                         const __grid_constant__ CUtensorMap tmA64, Params p) {
+  pdl_enter();
   using C = PairCfg;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -522,18 +523,22 @@ static std::mutex g_pmu;
 static int g_psmem_set[64];
 static int g_pclusters[64];
 
+// attr: room for two attributes (the CTA pair, and programmatic dependent
+// launch as for every kernel of the library, see pdl_enter)
 static void pair_config(cudaLaunchConfig_t *cfg, cudaLaunchAttribute *attr, int grid, mx_stream stream) {
   *cfg = cudaLaunchConfig_t{};
   cfg->gridDim = dim3(grid, 1, 1);
   cfg->blockDim = dim3(P_THREADS, 1, 1);
   cfg->dynamicSmemBytes = PairCfg::SMEM_ALLOC;
   cfg->stream = stream;
-  attr->id = cudaLaunchAttributeClusterDimension;
-  attr->val.clusterDim.x = 2;
-  attr->val.clusterDim.y = 1;
-  attr->val.clusterDim.z = 1;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg->attrs = attr;
-  cfg->numAttrs = 1;
+  cfg->numAttrs = pdl_enabled() ? 2 : 1;
 }
 
 mx_status launch_pair(const Params &p, const uint8_t *A, int64_t a_inner, int64_t a_outer, const uint8_t *B,
@@ -551,8 +556,9 @@ mx_status launch_pair(const Params &p, const uint8_t *A, int64_t a_inner, int64_
       int sms = 0;
       MX_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
       cudaLaunchConfig_t cfg;
-      cudaLaunchAttribute attr;
-      pair_config(&cfg, &attr, (sms / 2) * 2, nullptr);
+      cudaLaunchAttribute attr[2];
+      pair_config(&cfg, attr, (sms / 2) * 2, nullptr);
+      cfg.numAttrs = 1;  // the occupancy query needs the cluster shape only
       int n = 0;
       MX_CUDA_TRY(cudaOccupancyMaxActiveClusters(&n, k_grouped_gemm_pair, &cfg));
       if (n < 1) return MX_ERR_CUDA;
@@ -579,8 +585,8 @@ mx_status launch_pair(const Params &p, const uint8_t *A, int64_t a_inner, int64_
   }
   if (st != MX_OK) return st;
   cudaLaunchConfig_t cfg;
-  cudaLaunchAttribute attr;
-  pair_config(&cfg, &attr, 2 * clusters, stream);
+  cudaLaunchAttribute attr[2];
+  pair_config(&cfg, attr, 2 * clusters, stream);
   MX_CUDA_TRY(cudaLaunchKernelEx(&cfg, k_grouped_gemm_pair, ma, mb, msa, msb, mc, mh, ma64, p));
   return launch_status();
 }

@@ -45,6 +45,7 @@ template <bool ROW, bool COL, bool GATHER, bool E5 = false>
 // packed bf16 pairs and the packed fp32x2 scaling each save ~2.5% (the kernel
 // is close to issue-bound), measured the same way.
 __global__ void __launch_bounds__(QT_THREADS, 6) k_quantize_bf16(QuantArgs a) {
+  pdl_enter();
   __shared__ __align__(16) uint16_t tile[QT_ROWS][QT_COLS];
   // COL output staged as [64 columns][128 rows] bytes (+16 pad per row: the
   // 16-byte writes of 8 consecutive columns then fall in distinct banks)
@@ -314,6 +315,7 @@ __global__ void __launch_bounds__(SB_THREADS) k_swiglu_bwd(const float *__restri
                                                            int64_t rows, int64_t F, uint8_t *dab_rq, uint8_t *dab_rs,
                                                            uint8_t *dab_cq, uint8_t *dab_cs, uint8_t *h_cq,
                                                            uint8_t *h_cs, const int32_t *__restrict__ row_limit) {
+  pdl_enter();
   extern __shared__ __align__(16) uint8_t sb_smem[];
   float *vals = reinterpret_cast<float *>(sb_smem);                          // [3][128][33]
   uint8_t *qst = sb_smem + 3 * SB_ROWS * SB_VAL_STRIDE * 4;                    // [3][32][144]
@@ -524,6 +526,7 @@ template <bool F32, bool E5>
 __global__ void __launch_bounds__(DQ_THREADS) k_dequantize(const uint8_t *__restrict__ q, const uint8_t *__restrict__ s,
                                                            int64_t rows, int64_t cols, int64_t s_stride, int swizzled,
                                                            void *out) {
+  pdl_enter();
   const int64_t grow = blockIdx.x;  // row over all batch entries
   const int64_t b = grow / rows, r = grow - b * rows;
   const int64_t cblocks = cols / 32;
@@ -595,6 +598,7 @@ constexpr int RM_BATCH = 4;  // 16-byte loads in flight per thread
 
 __global__ void __launch_bounds__(RM_THREADS) k_quantize_rowmax(const uint16_t *__restrict__ x, int64_t cols,
                                                                 uint8_t *__restrict__ q, float *__restrict__ scale) {
+  pdl_enter();
   extern __shared__ __align__(16) uint4 rm_row[];  // cols / 8 chunks
   __shared__ uint32_t red[RM_THREADS / 32];
   const int tid = threadIdx.x;
@@ -646,13 +650,13 @@ __global__ void __launch_bounds__(RM_THREADS) k_quantize_rowmax(const uint16_t *
 template <bool GATHER>
 static void launch_quantize(const QuantArgs &a, bool row, bool col, bool e5, dim3 grid, mx_stream stream) {
   if (e5) {
-    if (row && col) k_quantize_bf16<true, true, GATHER, true><<<grid, QT_THREADS, 0, stream>>>(a);
-    else if (row) k_quantize_bf16<true, false, GATHER, true><<<grid, QT_THREADS, 0, stream>>>(a);
-    else k_quantize_bf16<false, true, GATHER, true><<<grid, QT_THREADS, 0, stream>>>(a);
+    if (row && col) (void)launch_k(k_quantize_bf16<true, true, GATHER, true>, grid, QT_THREADS, 0, stream, a);
+    else if (row) (void)launch_k(k_quantize_bf16<true, false, GATHER, true>, grid, QT_THREADS, 0, stream, a);
+    else (void)launch_k(k_quantize_bf16<false, true, GATHER, true>, grid, QT_THREADS, 0, stream, a);
   } else {
-    if (row && col) k_quantize_bf16<true, true, GATHER, false><<<grid, QT_THREADS, 0, stream>>>(a);
-    else if (row) k_quantize_bf16<true, false, GATHER, false><<<grid, QT_THREADS, 0, stream>>>(a);
-    else k_quantize_bf16<false, true, GATHER, false><<<grid, QT_THREADS, 0, stream>>>(a);
+    if (row && col) (void)launch_k(k_quantize_bf16<true, true, GATHER, false>, grid, QT_THREADS, 0, stream, a);
+    else if (row) (void)launch_k(k_quantize_bf16<true, false, GATHER, false>, grid, QT_THREADS, 0, stream, a);
+    else (void)launch_k(k_quantize_bf16<false, true, GATHER, false>, grid, QT_THREADS, 0, stream, a);
   }
 }
 
@@ -679,7 +683,7 @@ extern "C" mx_status fp8_quantize_rowmax(const void *x, int64_t rows, int64_t co
       set[dev] = 1;
     }
   }
-  k_quantize_rowmax<<<(unsigned)rows, RM_THREADS, smem, stream>>>(static_cast<const uint16_t *>(x), cols, q,
+  (void)launch_k(k_quantize_rowmax, (unsigned)rows, RM_THREADS, smem, stream, static_cast<const uint16_t *>(x), cols, q,
                                                                    row_scale);
   return launch_status();
 }
@@ -752,13 +756,13 @@ extern "C" mx_status mx_dequantize(const uint8_t *q, const uint8_t *s, int64_t b
   const int swz = scale_layout == MX_SCALE_SWIZZLED;
   const bool e5 = elem == MX_ELEM_E5M2;
   if (out_dtype == MX_OUT_F32 && e5)
-    k_dequantize<true, true><<<grid, DQ_THREADS, 0, stream>>>(q, s, rows, cols, s_stride, swz, out);
+    (void)launch_k(k_dequantize<true, true>, grid, DQ_THREADS, 0, stream, q, s, rows, cols, s_stride, swz, out);
   else if (out_dtype == MX_OUT_F32)
-    k_dequantize<true, false><<<grid, DQ_THREADS, 0, stream>>>(q, s, rows, cols, s_stride, swz, out);
+    (void)launch_k(k_dequantize<true, false>, grid, DQ_THREADS, 0, stream, q, s, rows, cols, s_stride, swz, out);
   else if (e5)
-    k_dequantize<false, true><<<grid, DQ_THREADS, 0, stream>>>(q, s, rows, cols, s_stride, swz, out);
+    (void)launch_k(k_dequantize<false, true>, grid, DQ_THREADS, 0, stream, q, s, rows, cols, s_stride, swz, out);
   else
-    k_dequantize<false, false><<<grid, DQ_THREADS, 0, stream>>>(q, s, rows, cols, s_stride, swz, out);
+    (void)launch_k(k_dequantize<false, false>, grid, DQ_THREADS, 0, stream, q, s, rows, cols, s_stride, swz, out);
   return launch_status();
 }
 
@@ -823,10 +827,10 @@ extern "C" mx_status moe_swiglu_bwd(const float *dh, const void *ab, int64_t row
   dim3 grid((unsigned)(rows / SB_ROWS), (unsigned)(F / SB_COLS));
   const uint16_t *abp = static_cast<const uint16_t *>(ab);
   if (grad_elem == MX_ELEM_E5M2)
-    k_swiglu_bwd<true><<<grid, SB_THREADS, SB_SMEM, stream>>>(dh, abp, rows, F, dab_rq, dab_rs, dab_cq, dab_cs, h_cq,
+    (void)launch_k(k_swiglu_bwd<true>, grid, SB_THREADS, SB_SMEM, stream, dh, abp, rows, F, dab_rq, dab_rs, dab_cq, dab_cs, h_cq,
                                                               h_cs, row_limit);
   else
-    k_swiglu_bwd<false><<<grid, SB_THREADS, SB_SMEM, stream>>>(dh, abp, rows, F, dab_rq, dab_rs, dab_cq, dab_cs, h_cq,
+    (void)launch_k(k_swiglu_bwd<false>, grid, SB_THREADS, SB_SMEM, stream, dh, abp, rows, F, dab_rq, dab_rs, dab_cq, dab_cs, h_cq,
                                                                h_cs, row_limit);
   return launch_status();
 }

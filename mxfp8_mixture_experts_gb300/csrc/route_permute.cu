@@ -21,6 +21,7 @@ constexpr int MAP_MAX_E = 256;
 // router: one thread per token
 // ---------------------------------------------------------------------------
 __global__ void k_route(const float *__restrict__ logits, int64_t T, int E, int k, int32_t *ids, float *gate) {
+  pdl_enter();
   const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (t >= T) return;
   const float *l = logits + t * E;
@@ -52,6 +53,7 @@ __global__ void k_route(const float *__restrict__ logits, int64_t T, int E, int 
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(MAP_CHUNK) k_map_count(const int32_t *__restrict__ ids, int64_t n, int E,
                                                          int32_t *chunk_counts, int32_t *dev_status) {
+  pdl_enter();
   __shared__ int32_t hist[MAP_MAX_E];
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
   __syncthreads();
@@ -71,6 +73,7 @@ __global__ void __launch_bounds__(MAP_CHUNK) k_map_count(const int32_t *__restri
 __global__ void __launch_bounds__(MAP_MAX_E) k_map_scan(const int32_t *__restrict__ chunk_counts, int64_t nchunks,
                                                         int E, int64_t rows_cap, int32_t *chunk_base,
                                                         int32_t *counts, int32_t *offsets, int32_t *src) {
+  pdl_enter();
   __shared__ int32_t s_pad[MAP_MAX_E + 1];
   __shared__ int32_t s_cnt[MAP_MAX_E];
   const int e = threadIdx.x;
@@ -112,6 +115,7 @@ __global__ void __launch_bounds__(MAP_MAX_E) k_map_scan(const int32_t *__restric
 __global__ void __launch_bounds__(MAP_CHUNK) k_map_assign(const int32_t *__restrict__ ids, int64_t n, int E,
                                                           const int32_t *__restrict__ chunk_base, int32_t *dst,
                                                           int32_t *src) {
+  pdl_enter();
   __shared__ int32_t warp_cnt[MAP_CHUNK / 32][MAP_MAX_E];
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   for (int i = tid; i < (MAP_CHUNK / 32) * MAP_MAX_E; i += blockDim.x) (&warp_cnt[0][0])[i] = 0;
@@ -178,6 +182,7 @@ __device__ __forceinline__ int64_t scale_off(const PermuteArgs &a, int64_t r, in
 }
 
 __global__ void __launch_bounds__(256) k_permute(PermuteArgs a) {
+  pdl_enter();
   const int lane = threadIdx.x & 31;
   const int64_t w = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int64_t nb = a.H / 32;
@@ -293,6 +298,7 @@ template <int K>
 __global__ void __launch_bounds__(256) k_unpermute(const uint16_t *__restrict__ y, const int32_t *__restrict__ dst,
                                                    const float *__restrict__ gate, int64_t T, int64_t H,
                                                    uint16_t *out) {
+  pdl_enter();
   constexpr int U = K >= 8 ? 1 : 8 / K;
   const int lane = threadIdx.x & 31;
   const int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -346,6 +352,7 @@ __global__ void __launch_bounds__(256) k_unpermute(const uint16_t *__restrict__ 
 __global__ void __launch_bounds__(256) k_gate_grad(const uint16_t *__restrict__ dOut, const uint16_t *__restrict__ y,
                                                    const int32_t *__restrict__ dst, int64_t T, int64_t H, int k,
                                                    float *d_gate) {
+  pdl_enter();
   const int lane = threadIdx.x & 31;
   const int64_t p = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   if (p >= T * k) return;
@@ -394,7 +401,7 @@ extern "C" mx_status moe_route(const float *logits, int64_t T, int32_t E, int32_
   mx_status st = check_device_cached();
   if (st != MX_OK) return st;
   if (T == 0) return MX_OK;
-  k_route<<<(unsigned)((T + 127) / 128), 128, 0, stream>>>(logits, T, E, k, ids, gate);
+  (void)launch_k(k_route, (unsigned)((T + 127) / 128), 128, 0, stream, logits, T, E, k, ids, gate);
   return launch_status();
 }
 
@@ -424,9 +431,9 @@ extern "C" mx_status moe_permute_map(const int32_t *ids, int64_t T, int32_t k, i
   const int64_t nchunks = (n + MAP_CHUNK - 1) / MAP_CHUNK;
   int32_t *chunk_counts = static_cast<int32_t *>(workspace);
   int32_t *chunk_base = chunk_counts + nchunks * E;
-  if (nchunks > 0) k_map_count<<<(unsigned)nchunks, MAP_CHUNK, 0, stream>>>(ids, n, E, chunk_counts, dev_status);
-  k_map_scan<<<1, MAP_MAX_E, 0, stream>>>(chunk_counts, nchunks, E, rows_cap, chunk_base, counts, offsets, src);
-  if (nchunks > 0) k_map_assign<<<(unsigned)nchunks, MAP_CHUNK, 0, stream>>>(ids, n, E, chunk_base, dst, src);
+  if (nchunks > 0) (void)launch_k(k_map_count, (unsigned)nchunks, MAP_CHUNK, 0, stream, ids, n, E, chunk_counts, dev_status);
+  (void)launch_k(k_map_scan, 1, MAP_MAX_E, 0, stream, chunk_counts, nchunks, E, rows_cap, chunk_base, counts, offsets, src);
+  if (nchunks > 0) (void)launch_k(k_map_assign, (unsigned)nchunks, MAP_CHUNK, 0, stream, ids, n, E, chunk_base, dst, src);
   return launch_status();
 }
 
@@ -474,9 +481,9 @@ extern "C" mx_status moe_permute_map_noalloc(const int32_t *ids, int64_t T, int3
   const int64_t nchunks = (n + MAP_CHUNK - 1) / MAP_CHUNK;
   int32_t *chunk_counts = scratch;
   int32_t *chunk_base = scratch + nchunks * E;
-  if (nchunks > 0) k_map_count<<<(unsigned)nchunks, MAP_CHUNK, 0, stream>>>(ids, n, E, chunk_counts, dev_status);
-  k_map_scan<<<1, MAP_MAX_E, 0, stream>>>(chunk_counts, nchunks, E, rows_cap, chunk_base, counts, offsets, src);
-  if (nchunks > 0) k_map_assign<<<(unsigned)nchunks, MAP_CHUNK, 0, stream>>>(ids, n, E, chunk_base, dst, src);
+  if (nchunks > 0) (void)launch_k(k_map_count, (unsigned)nchunks, MAP_CHUNK, 0, stream, ids, n, E, chunk_counts, dev_status);
+  (void)launch_k(k_map_scan, 1, MAP_MAX_E, 0, stream, chunk_counts, nchunks, E, rows_cap, chunk_base, counts, offsets, src);
+  if (nchunks > 0) (void)launch_k(k_map_assign, (unsigned)nchunks, MAP_CHUNK, 0, stream, ids, n, E, chunk_base, dst, src);
   return launch_status();
 }
 
@@ -512,7 +519,7 @@ extern "C" mx_status moe_permute(int32_t kind, const void *x, const uint8_t *x_s
   a.swizzled = scale_layout == MX_SCALE_SWIZZLED;
   const int64_t warps = T + rows_cap;
   if (warps == 0) return MX_OK;
-  k_permute<<<(unsigned)((warps + 7) / 8), 256, 0, stream>>>(a);
+  (void)launch_k(k_permute, (unsigned)((warps + 7) / 8), 256, 0, stream, a);
   return launch_status();
 }
 
@@ -529,14 +536,14 @@ extern "C" mx_status moe_unpermute(const void *y, const int32_t *dst, const floa
   const uint16_t *yy = static_cast<const uint16_t *>(y);
   uint16_t *oo = static_cast<uint16_t *>(out);
   switch (k) {
-    case 1: k_unpermute<1><<<grid, 256, 0, stream>>>(yy, dst, gate, T, H, oo); break;
-    case 2: k_unpermute<2><<<grid, 256, 0, stream>>>(yy, dst, gate, T, H, oo); break;
-    case 3: k_unpermute<3><<<grid, 256, 0, stream>>>(yy, dst, gate, T, H, oo); break;
-    case 4: k_unpermute<4><<<grid, 256, 0, stream>>>(yy, dst, gate, T, H, oo); break;
-    case 5: k_unpermute<5><<<grid, 256, 0, stream>>>(yy, dst, gate, T, H, oo); break;
-    case 6: k_unpermute<6><<<grid, 256, 0, stream>>>(yy, dst, gate, T, H, oo); break;
-    case 7: k_unpermute<7><<<grid, 256, 0, stream>>>(yy, dst, gate, T, H, oo); break;
-    default: k_unpermute<8><<<grid, 256, 0, stream>>>(yy, dst, gate, T, H, oo); break;
+    case 1: (void)launch_k(k_unpermute<1>, grid, 256, 0, stream, yy, dst, gate, T, H, oo); break;
+    case 2: (void)launch_k(k_unpermute<2>, grid, 256, 0, stream, yy, dst, gate, T, H, oo); break;
+    case 3: (void)launch_k(k_unpermute<3>, grid, 256, 0, stream, yy, dst, gate, T, H, oo); break;
+    case 4: (void)launch_k(k_unpermute<4>, grid, 256, 0, stream, yy, dst, gate, T, H, oo); break;
+    case 5: (void)launch_k(k_unpermute<5>, grid, 256, 0, stream, yy, dst, gate, T, H, oo); break;
+    case 6: (void)launch_k(k_unpermute<6>, grid, 256, 0, stream, yy, dst, gate, T, H, oo); break;
+    case 7: (void)launch_k(k_unpermute<7>, grid, 256, 0, stream, yy, dst, gate, T, H, oo); break;
+    default: (void)launch_k(k_unpermute<8>, grid, 256, 0, stream, yy, dst, gate, T, H, oo); break;
   }
   return launch_status();
 }
@@ -550,7 +557,7 @@ extern "C" mx_status moe_gate_grad(const void *dOut, const void *y, const int32_
   mx_status st = check_device_cached();
   if (st != MX_OK) return st;
   if (T == 0) return MX_OK;
-  k_gate_grad<<<(unsigned)((T * k + 7) / 8), 256, 0, stream>>>(static_cast<const uint16_t *>(dOut),
+  (void)launch_k(k_gate_grad, (unsigned)((T * k + 7) / 8), 256, 0, stream, static_cast<const uint16_t *>(dOut),
                                                                static_cast<const uint16_t *>(y), dst, T, H, k, d_gate);
   return launch_status();
 }

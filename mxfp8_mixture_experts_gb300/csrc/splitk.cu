@@ -26,6 +26,7 @@ namespace mxmoe {
 
 __global__ void k_split_offsets(const int32_t *__restrict__ off, int32_t E, int32_t splits, int64_t M_cap,
                                 int32_t *__restrict__ voff, int32_t *dev_status) {
+  pdl_enter();
   for (int g = threadIdx.x; g <= E * splits; g += blockDim.x) {
     if (g == E * splits) {
       voff[g] = off[E];
@@ -46,6 +47,7 @@ __global__ void k_split_offsets(const int32_t *__restrict__ off, int32_t E, int3
 // 4 fp32 per thread per step; total = E * N * K (a multiple of 4)
 __global__ void __launch_bounds__(256) k_split_reduce(const float4 *__restrict__ part, int64_t per_e4, int32_t E,
                                                       int32_t splits, float4 *__restrict__ out) {
+  pdl_enter();
   const int64_t total = per_e4 * E;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
     const int64_t e = i / per_e4, j = i % per_e4;
@@ -88,7 +90,7 @@ extern "C" mx_status mx_grouped_gemm_wgrad_splitk(const uint8_t *A, const uint8_
   if (st != MX_OK) return st;
   int32_t *voff = static_cast<int32_t *>(ws);
   float *part = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + round_up(((int64_t)E * splits + 1) * 4, 256));
-  k_split_offsets<<<1, 256, 0, stream>>>(offsets, E, splits, M_cap, voff, dev_status);
+  (void)launch_k(k_split_offsets, 1, 256, 0, stream, offsets, E, splits, M_cap, voff, dev_status);
   st = launch_status();
   if (st != MX_OK) return st;
   st = mx_grouped_gemm(MX_GEMM_WGRAD, A, sA, B, sB, voff, E * splits, M_cap, N, K, part, MX_OUT_F32, elem_a, elem_b,
@@ -97,7 +99,7 @@ extern "C" mx_status mx_grouped_gemm_wgrad_splitk(const uint8_t *A, const uint8_
   const int64_t per_e4 = N * K / 4;
   int64_t blocks = (per_e4 * E + 255) / 256;
   if (blocks > 152 * 16) blocks = 152 * 16;
-  k_split_reduce<<<(unsigned)blocks, 256, 0, stream>>>(reinterpret_cast<const float4 *>(part), per_e4, E, splits,
+  (void)launch_k(k_split_reduce, (unsigned)blocks, 256, 0, stream, reinterpret_cast<const float4 *>(part), per_e4, E, splits,
                                                        reinterpret_cast<float4 *>(C));
   return launch_status();
 }
