@@ -43,12 +43,12 @@ FP8_PER_BF16 = 2.0   # nominal dense fp8 / bf16 tensor rate (4.5 / 2.25 PFLOP/s)
 # (dram__bytes_read.sum + dram__bytes_write.sum per launch, summed), from an
 # ncu capture of those launches alone.  Valid only for the GEMM sources it was
 # taken on (checked by hash); reported as null otherwise.
-GEMM_TRAFFIC_BYTES_PER_STEP = 15318272512
+GEMM_TRAFFIC_BYTES_PER_STEP = 15727732480
 GEMM_TRAFFIC_HOW = ("ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum -k regex:k_grouped_gemm_pair "
                     "-s 6 -c 6 on this full-size layer step (T=16384, H=5120, E=16, F=8192, top-1): "
-                    "1.026x the algorithmic bytes")
+                    "1.053x the algorithmic bytes")
 GEMM_TRAFFIC_SOURCES = ("gemm_pair.cu", "gemm_shared.cuh", "common.cuh")
-GEMM_TRAFFIC_SHA256 = "209c16daa081ddbd940ce69fcca380ae8bcdb83f873e53bab285e56ff65e6220"
+GEMM_TRAFFIC_SHA256 = "9961f9c43be866eea696926fe680ac362a578d4e6b27b747c1435e25eb015bfb"
 
 
 def _gemm_sources_sha256():
@@ -984,10 +984,17 @@ def _e2e(m, d, dims, inp, dev, args, world):
     s = torch.cuda.current_stream(dev)
     hs, ds = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     tev = lambda: torch.cuda.Event(enable_timing=True)
-    in_ready = [tev(), tev()]      # inputs of the buffer copied in
-    done = [tev(), tev()]          # compute on the buffer finished
+    # Each copy is split at the forward/backward boundary, so the pipeline
+    # fills and drains with as little exposed copy time as the data allow:
+    # the weight prep needs no step input and runs while x and logits arrive,
+    # dOut arrives while the forward runs, and out leaves while the backward
+    # runs; only dX and d_gate follow the last backward.
+    in_fwd = [tev(), tev()]        # x, logits of the buffer copied in
+    in_bwd = [tev(), tev()]        # dOut of the buffer copied in
+    fwd_done = [tev(), tev()]      # forward on the buffer finished
+    done = [tev(), tev()]          # backward on the buffer finished
     out_read = [tev(), tev()]      # results of the buffer copied out
-    marks = []                     # (h2d start, h2d end, d2h start, d2h end) per step
+    marks = []                     # per step: h2d (start, end), d2h out (start, end), d2h rest (start, end)
 
     def h2d(i, mk):
         b = bufs[i % 2]
@@ -995,35 +1002,44 @@ def _e2e(m, d, dims, inp, dev, args, world):
             hs.wait_event(done[i % 2])         # step i-2 no longer reads this buffer
         mk[0].record(hs)
         with torch.cuda.stream(hs):
-            for n, t in h_in.items():
-                b[n].copy_(t, non_blocking=True)
-        in_ready[i % 2].record(hs)
+            b["x"].copy_(h_in["x"], non_blocking=True)
+            b["lg"].copy_(h_in["lg"], non_blocking=True)
+            in_fwd[i % 2].record(hs)
+            b["dO"].copy_(h_in["dO"], non_blocking=True)
+        in_bwd[i % 2].record(hs)
         mk[1].record(hs)
 
     def compute(i):
         b = bufs[i % 2]
-        s.wait_event(in_ready[i % 2])
         if i >= 2:
             s.wait_event(out_read[i % 2])      # step i-2's results have left this buffer
         m.moe_layer_prep_weights(W13, W2, wq)
+        s.wait_event(in_fwd[i % 2])
         m.moe_layer_fwd(b["x"], wq, d, ws, logits=b["lg"], ids=ids, gate=gate, out=b["out"])
+        fwd_done[i % 2].record(s)
+        s.wait_event(in_bwd[i % 2])
         m.moe_layer_bwd(b["x"], b["dO"], gate, wq, d, ws, dX=b["dX"], dW13=dW13, dW2=dW2, d_gate=b["dg"])
         done[i % 2].record(s)
 
     def d2h(i, mk):
-        b = bufs[i % 2]
-        ds.wait_event(done[i % 2])
+        b, h = bufs[i % 2], h_out[i % 2]
+        ds.wait_event(fwd_done[i % 2])
         mk[2].record(ds)
         with torch.cuda.stream(ds):
-            for n, t in h_out[i % 2].items():
-                t.copy_(b[n], non_blocking=True)
-        out_read[i % 2].record(ds)
+            h["out"].copy_(b["out"], non_blocking=True)
         mk[3].record(ds)
+        ds.wait_event(done[i % 2])
+        mk[4].record(ds)
+        with torch.cuda.stream(ds):
+            h["dX"].copy_(b["dX"], non_blocking=True)
+            h["dg"].copy_(b["dg"], non_blocking=True)
+        out_read[i % 2].record(ds)
+        mk[5].record(ds)
 
     def run(k, start, record):
         hs.wait_event(start)
         ds.wait_event(start)
-        mks = [[tev() for _ in range(4)] for _ in range(k)]
+        mks = [[tev() for _ in range(6)] for _ in range(k)]
         h2d(0, mks[0])
         if k > 1:
             h2d(1, mks[1])
@@ -1054,14 +1070,15 @@ def _e2e(m, d, dims, inp, dev, args, world):
     flops = sum(_gemm_flops(d, routed).values())
     h2d_b = sum(t.numel() * t.element_size() for t in h_in.values())
     d2h_b = sum(t.numel() * t.element_size() for t in h_out[0].values())
-    h2d_ms = statistics.mean(a.elapsed_time(b) for a, b, _, _ in marks)
-    d2h_ms = statistics.mean(c.elapsed_time(e) for _, _, c, e in marks)
+    h2d_ms = statistics.mean(mk[0].elapsed_time(mk[1]) for mk in marks)
+    d2h_ms = statistics.mean(mk[2].elapsed_time(mk[3]) + mk[4].elapsed_time(mk[5]) for mk in marks)
     return {"value": world * flops * args.steps / el / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d_b,
             "d2h_bytes_per_step": d2h_b, "ms_per_step": el / args.steps * 1e3,
             "h2d_ms_per_step": h2d_ms, "d2h_ms_per_step": d2h_ms,
             "h2d_GBps": h2d_b / h2d_ms / 1e6, "d2h_GBps": d2h_b / d2h_ms / 1e6,
             "copies": "pinned host <-> device, H2D and D2H on two streams of their own, double-buffered, inside "
-                      "the timed region; weight gradients stay on the device"}
+                      "the timed region, each split at the fwd/bwd boundary (dOut in while the forward runs, out "
+                      "back while the backward runs); weight gradients stay on the device"}
 
 
 if __name__ == "__main__":
