@@ -103,9 +103,11 @@ def test_layer_stagewise(dev, case):
     W13 = np.concatenate([mx.bf16_to_f64(W1b), mx.bf16_to_f64(W3b)], axis=2)
     w13c_q, w13c_s = mx.quantize_cols(W13)                       # [E, 2F, H]
     xp = _deq_swz(s["xq"], s["xs"], R, H)
-    ab_ref = moe.grouped_gemm_rows(xp, mx.dequantize_rows(w13c_q, w13c_s), off)
+    w13c = mx.dequantize_rows(w13c_q, w13c_s)
+    ab_ref = moe.grouped_gemm_rows(xp, w13c, off)
+    ab_mag = moe.grouped_gemm_rows(np.abs(xp), np.abs(w13c), off)
     ab_b = bits(s["ab"])
-    assert_bf16_within_one_ulp(ab_b[:P], ab_ref[:P], "a|b")
+    assert_bf16_within_one_ulp(ab_b[:P], ab_ref[:P], "a|b", mag=ab_mag[:P], K=H)
     abv = mx.bf16_to_f64(ab_b[:P])
     h = moe.swiglu(abv[:, :F], abv[:, F:])
     quant_mismatches_outside_margin(u8(s["hq"])[:P], mx.unswizzle_scales(u8(s["hs"]), R, F // 32)[:P], h, "hq")
@@ -113,8 +115,10 @@ def test_layer_stagewise(dev, case):
     # GEMM2
     w2c_q, w2c_s = mx.quantize_cols(mx.bf16_to_f64(W2b))          # [E, H, F]
     hp = _deq_swz(s["hq"], s["hs"], R, F)
-    y_ref = moe.grouped_gemm_rows(hp, mx.dequantize_rows(w2c_q, w2c_s), off)
-    assert_bf16_within_one_ulp(bits(s["y"])[:P], y_ref[:P], "y")
+    w2c = mx.dequantize_rows(w2c_q, w2c_s)
+    y_ref = moe.grouped_gemm_rows(hp, w2c, off)
+    y_mag = moe.grouped_gemm_rows(np.abs(hp), np.abs(w2c), off)
+    assert_bf16_within_one_ulp(bits(s["y"])[:P], y_ref[:P], "y", mag=y_mag[:P], K=F)
 
     # combine
     assert_bytes_equal(bits(s["out"]), moe.unpermute(bits(s["y"]), dst, gate_np, T, k), "out")
@@ -164,8 +168,11 @@ def test_layer_stagewise(dev, case):
 
     # dgrad1
     w13r_q, w13r_s = mx.quantize_rows(W13)                       # [E, H, 2F]
-    dxp_ref = moe.grouped_gemm_rows(_deq_swz(s["dab_rq"], s["dab_rs"], R, 2 * F), mx.dequantize_rows(w13r_q, w13r_s), off)
-    assert_bf16_within_one_ulp(bits(s["dxp"])[:P], dxp_ref[:P], "dxp")
+    dab_r = _deq_swz(s["dab_rq"], s["dab_rs"], R, 2 * F)
+    w13r = mx.dequantize_rows(w13r_q, w13r_s)
+    dxp_ref = moe.grouped_gemm_rows(dab_r, w13r, off)
+    dxp_mag = moe.grouped_gemm_rows(np.abs(dab_r), np.abs(w13r), off)
+    assert_bf16_within_one_ulp(bits(s["dxp"])[:P], dxp_ref[:P], "dxp", mag=dxp_mag[:P], K=2 * F)
 
     # x permuted, column-quantized (bit-exact)
     q, sc = mx.quantize_cols(moe.permute_rows(mx.bf16_to_f64(xb), src_full, k))
@@ -591,7 +598,8 @@ def test_layer_full_size_sampled(dev):
             (W1b if c < F else W3b)[e, :, c % F].contiguous())) for e in ex])         # [48, H]
         wq, ws_ = mx.quantize_rows(wcol)                                               # blocks along H
         terms = xhat * mx.dequantize_rows(wq, ws_)
-        assert_bf16_within_one_ulp(ab_rows[:, c], terms.sum(axis=1), f"a|b col {c}")
+        assert_bf16_within_one_ulp(ab_rows[:, c], terms.sum(axis=1), f"a|b col {c}", mag=np.abs(terms).sum(axis=1),
+                                   K=H)
 
     # fused SwiGLU -> h, quantized (teacher forced on the GPU's a, b)
     abv = mx.bf16_to_f64(ab_rows)
@@ -605,7 +613,8 @@ def test_layer_full_size_sampled(dev):
     for c in g.choice(H, 8, replace=False):
         wcol = np.stack([mx.bf16_to_f64(workloads.bf16_bits(W2b[e, :, c].contiguous())) for e in e_of[rows]])
         wq, ws_ = mx.quantize_rows(wcol)
-        assert_bf16_within_one_ulp(y_rows[:, c], (hhat * mx.dequantize_rows(wq, ws_)).sum(axis=1), f"y col {c}")
+        terms = hhat * mx.dequantize_rows(wq, ws_)
+        assert_bf16_within_one_ulp(y_rows[:, c], terms.sum(axis=1), f"y col {c}", mag=np.abs(terms).sum(axis=1), K=F)
 
     # combine (top-1): out[t] = bf16(fp32(gate * y[dst[t]])), exact
     toks = g.choice(T, 64, replace=False)
@@ -683,7 +692,9 @@ def test_layer_full_size_sampled(dev):
                                          mx.bf16_to_f64(workloads.bf16_bits(W3b[e_, c, :].contiguous()))])
                          for e_ in e_of[rows]])
         wq, ws_ = mx.quantize_rows(wrow)
-        assert_bf16_within_one_ulp(dxp_rows[:, c], (dabhat * mx.dequantize_rows(wq, ws_)).sum(axis=1), f"dxp col {c}")
+        terms = dabhat * mx.dequantize_rows(wq, ws_)
+        assert_bf16_within_one_ulp(dxp_rows[:, c], terms.sum(axis=1), f"dxp col {c}", mag=np.abs(terms).sum(axis=1),
+                                   K=2 * F)
 
     # combine of dX (unit gates, top-1): dX[t] = dxp[dst[t]] exactly
     assert_bytes_equal(bits(s["dX"][torch.as_tensor(toks, device=dev)]).view(np.uint8),
