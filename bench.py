@@ -151,9 +151,11 @@ class ClockSampler:
 # preallocated buffers, with CUDA events between launches
 # ----------------------------------------------------------------------------
 class LayerStep:
-    def __init__(self, d, inp, dev, grad_elem=0):
+    def __init__(self, d, inp, dev, grad_elem=0, wgrad_bf16=False):
         import mxfp8_mixture_experts_gb300 as m
         self.grad_elem = grad_elem  # element format of the backward's gradient operands (0 E4M3, 1 E5M2)
+        self.wgrad_cd = 0 if wgrad_bf16 else 1  # weight-gradient output: MX_OUT_BF16 or MX_OUT_F32
+        wdt = torch.bfloat16 if wgrad_bf16 else torch.float32
         self.m = m
         self.L = m.lib()
         self.d = d
@@ -196,10 +198,10 @@ class LayerStep:
         b["dab_rq"], b["dab_rs"] = u8(R * 2 * F), u8(sb(R, 2 * F))
         b["dab_cq"], b["dab_cs"] = u8(2 * F * R), u8(sb(2 * F, R))
         b["h_cq"], b["h_cs"] = u8(F * R), u8(sb(F, R))
-        b["dW2"] = torch.empty((E, F, H), dtype=torch.float32, device=dev)
+        b["dW2"] = torch.empty((E, F, H), dtype=wdt, device=dev)
         b["dxp"] = torch.empty((R, H), dtype=torch.bfloat16, device=dev)
         b["xp_cq"], b["xp_cs"] = u8(H * R), u8(sb(H, R))
-        b["dW13"] = torch.empty((E, H, 2 * F), dtype=torch.float32, device=dev)
+        b["dW13"] = torch.empty((E, H, 2 * F), dtype=wdt, device=dev)
         b["dX"] = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
         b["status"] = torch.zeros(1, dtype=torch.int32, device=dev)
         self.b = b
@@ -252,14 +254,14 @@ class LayerStep:
                               s), "dgrad2"); mark()
         chk(L.moe_swiglu_bwd(p["dh"], p["ab"], R, F, ge, p["dab_rq"], p["dab_rs"], p["dab_cq"], p["dab_cs"], p["h_cq"],
                              p["h_cs"], lim, s), "swiglu bwd"); mark()
-        chk(L.mx_grouped_gemm(2, p["h_cq"], p["h_cs"], p["dy_cq"], p["dy_cs"], p["off"], E, R, F, H, p["dW2"], 1, 0, ge, st,
+        chk(L.mx_grouped_gemm(2, p["h_cq"], p["h_cs"], p["dy_cq"], p["dy_cs"], p["off"], E, R, F, H, p["dW2"], self.wgrad_cd, 0, ge, st,
                               s), "wgrad2"); mark()
         chk(L.mx_grouped_gemm(1, p["dab_rq"], p["dab_rs"], p["w13_rq"], p["w13_rs"], p["off"], E, R, H, 2 * F,
                               p["dxp"], 0, ge, 0, st, s), "dgrad1"); mark()
         chk(L.moe_gather_quant(x, None, p["src"], T, H, k, R, 2, 0, None, None, p["xp_cq"], p["xp_cs"], lim, s),
             "x col quant"); mark()
         chk(L.mx_grouped_gemm(2, p["xp_cq"], p["xp_cs"], p["dab_cq"], p["dab_cs"], p["off"], E, R, H, 2 * F,
-                              p["dW13"], 1, 0, ge, st, s), "wgrad1"); mark()
+                              p["dW13"], self.wgrad_cd, 0, ge, st, s), "wgrad1"); mark()
         chk(L.moe_unpermute(p["dxp"], p["dst"], None, T, H, k, p["dX"], s), "combine dX"); mark()
 
     NAMES = ["quantize W13", "quantize W2", "route", "map", "permute+quant", "gemm1+swiglu", "gemm2", "combine",
@@ -745,6 +747,8 @@ def main():
     ap.add_argument("--k", type=int, default=None, help="override top-k (a variant; the bench line is top-1)")
     ap.add_argument("--grad-format", default="e4m3", choices=["e4m3", "e5m2"],
                     help="element format of the backward's gradient operands (a variant; the bench line is e4m3)")
+    ap.add_argument("--wgrad-dtype", default="f32", choices=["f32", "bf16"],
+                    help="weight gradients in fp32 or bf16 (a variant; the bench line is fp32)")
     ap.add_argument("--workload", default="layer",
                     choices=["layer", "gemm", "quantize", "dequantize", "permute", "rowmax"],
                     help="layer: the full training step (the bench line); gemm / quantize / dequantize / "
@@ -777,6 +781,8 @@ def main():
               "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"}
     if args.grad_format != "e4m3":
         config["grad_format"] = args.grad_format
+    if args.wgrad_dtype != "f32":
+        config["wgrad_dtype"] = args.wgrad_dtype
 
     if args.impl == "reference":
         if rank != 0:
@@ -806,7 +812,7 @@ def main():
     torch.cuda.set_device(dev)
     d = m.MoELayerDims(T=dims.T, H=dims.H, F=dims.F, E=dims.E, k=dims.k)
     inp = workloads.layer_inputs(dims, seed=rank, device=dev, router="logits")
-    step = LayerStep(d, inp, dev, grad_elem=1 if args.grad_format == "e5m2" else 0)
+    step = LayerStep(d, inp, dev, grad_elem=1 if args.grad_format == "e5m2" else 0, wgrad_bf16=args.wgrad_dtype == "bf16")
     stream = torch.cuda.current_stream(dev)
 
     def barrier():
@@ -905,7 +911,8 @@ def main():
         bf16["mxfp8_speedup"] = bf16["ms_per_step"] / ms
 
     # the capture is of the default workload only: full sizes, top-1, E4M3 gradients
-    default_work = args.T is None and args.E is None and args.k in (None, 1) and args.grad_format == "e4m3"
+    default_work = (args.T is None and args.E is None and args.k in (None, 1) and args.grad_format == "e4m3"
+                    and args.wgrad_dtype == "f32")
     traffic = (GEMM_TRAFFIC_BYTES_PER_STEP if default_work and GEMM_TRAFFIC_SHA256 == _gemm_sources_sha256()
                else None)
     line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
@@ -968,8 +975,10 @@ def _e2e(m, d, dims, inp, dev, args, world):
     ws = torch.empty(m.moe_layer_workspace_size(d), dtype=torch.uint8, device=dev)
     h_in = {"x": inp["x"].cpu().pin_memory(), "lg": inp["logits"].cpu().pin_memory(),
             "dO": inp["dOut"].cpu().pin_memory()}
-    dW13 = torch.empty((d.E, d.H, 2 * d.F), dtype=torch.float32, device=dev)
-    dW2 = torch.empty((d.E, d.F, d.H), dtype=torch.float32, device=dev)
+    wdt = torch.bfloat16 if args.wgrad_dtype == "bf16" else torch.float32
+    wcd = m.MX_OUT_BF16 if args.wgrad_dtype == "bf16" else m.MX_OUT_F32
+    dW13 = torch.empty((d.E, d.H, 2 * d.F), dtype=wdt, device=dev)
+    dW2 = torch.empty((d.E, d.F, d.H), dtype=wdt, device=dev)
     ids = torch.empty((d.T, d.k), dtype=torch.int32, device=dev)
     gate = torch.empty((d.T, d.k), dtype=torch.float32, device=dev)
     bufs = []
@@ -1018,7 +1027,8 @@ def _e2e(m, d, dims, inp, dev, args, world):
         m.moe_layer_fwd(b["x"], wq, d, ws, logits=b["lg"], ids=ids, gate=gate, out=b["out"])
         fwd_done[i % 2].record(s)
         s.wait_event(in_bwd[i % 2])
-        m.moe_layer_bwd(b["x"], b["dO"], gate, wq, d, ws, dX=b["dX"], dW13=dW13, dW2=dW2, d_gate=b["dg"])
+        m.moe_layer_bwd(b["x"], b["dO"], gate, wq, d, ws, dX=b["dX"], dW13=dW13, dW2=dW2, d_gate=b["dg"],
+                        grad_elem=1 if args.grad_format == "e5m2" else 0, wgrad_dtype=wcd)
         done[i % 2].record(s)
 
     def d2h(i, mk):

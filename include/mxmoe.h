@@ -472,12 +472,15 @@ mx_status moe_gate_grad(const void *dOut, const void *y, const int32_t *dst,
  * (gate NULL = all ones) are inputs.  out bf16 [T, H].  Saves what the
  * backward needs in `ws` (moe_layer_workspace_size bytes).
  *
- * moe_layer_bwd: dOut bf16 [T, H] -> dX bf16 [T, H], dW13 fp32 [E, H, 2F],
- * dW2 fp32 [E, F, H], d_gate fp32 [T, k] (NULL: not computed).  Uses the `ws`
- * and `wq` of the matching forward.  grad_elem: element format of the two
- * gradient operands the backward quantizes, dY = gate * dOut and [da|db]
- * (MX_ELEM_E4M3; MX_ELEM_E5M2 is the gradient option); weights, h and the
- * permuted input stay E4M3.
+ * moe_layer_bwd: dOut bf16 [T, H] -> dX bf16 [T, H], dW13 [E, H, 2F] and dW2
+ * [E, F, H] in `wgrad_dtype`, d_gate fp32 [T, k] (NULL: not computed).  Uses
+ * the `ws` and `wq` of the matching forward.  grad_elem: element format of
+ * the two gradient operands the backward quantizes, dY = gate * dOut and
+ * [da|db] (MX_ELEM_E4M3; MX_ELEM_E5M2 is the gradient option); weights, h and
+ * the permuted input stay E4M3.  wgrad_dtype: MX_OUT_F32 (fp32 weight
+ * gradients, the reading for gradients that feed an optimizer) or
+ * MX_OUT_BF16 (each element the fp32 accumulation rounded once to bf16: the
+ * weight-gradient GEMMs then write half the bytes).
  */
 int64_t moe_layer_weights_size(int64_t H, int64_t F, int32_t E);
 int64_t moe_layer_workspace_size(int64_t T, int64_t H, int64_t F, int32_t E,
@@ -492,9 +495,9 @@ mx_status moe_layer_fwd(const void *x, const float *logits, int32_t *ids,
                         mx_stream stream);
 mx_status moe_layer_bwd(const void *x, const void *dOut, const float *gate,
                         const void *wq, int64_t T, int64_t H, int64_t F,
-                        int32_t E, int32_t k, int32_t grad_elem, void *ws, int64_t ws_bytes,
-                        void *dX, float *dW13, float *dW2, float *d_gate,
-                        int32_t *dev_status, mx_stream stream);
+                        int32_t E, int32_t k, int32_t grad_elem, int32_t wgrad_dtype,
+                        void *ws, int64_t ws_bytes, void *dX, void *dW13, void *dW2,
+                        float *d_gate, int32_t *dev_status, mx_stream stream);
 
 #ifdef __cplusplus
 }

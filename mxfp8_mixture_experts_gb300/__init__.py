@@ -317,15 +317,21 @@ def moe_layer_fwd(x: torch.Tensor, wq: torch.Tensor, d: MoELayerDims, ws: torch.
 
 def moe_layer_bwd(x: torch.Tensor, dOut: torch.Tensor, gate, wq: torch.Tensor, d: MoELayerDims,
                   ws: torch.Tensor, *, dX=None, dW13=None, dW2=None, d_gate=None, want_d_gate: bool = True,
-                  dev_status: torch.Tensor | None = None, grad_elem: int = MX_ELEM_E4M3):
-    """Backward -> (dX bf16 [T,H], dW13 fp32 [E,H,2F], dW2 fp32 [E,F,H], d_gate fp32 [T,k] or None)."""
+                  dev_status: torch.Tensor | None = None, grad_elem: int = MX_ELEM_E4M3,
+                  wgrad_dtype: int = MX_OUT_F32):
+    """Backward -> (dX bf16 [T,H], dW13 [E,H,2F], dW2 [E,F,H], d_gate fp32 [T,k] or None); the
+    weight gradients are fp32 (wgrad_dtype MX_OUT_F32) or bf16 (MX_OUT_BF16)."""
     dev = x.device
+    wdt = torch.float32 if wgrad_dtype == MX_OUT_F32 else torch.bfloat16
     dX = torch.empty((d.T, d.H), dtype=torch.bfloat16, device=dev) if dX is None else dX
-    dW13 = torch.empty((d.E, d.H, 2 * d.F), dtype=torch.float32, device=dev) if dW13 is None else dW13
-    dW2 = torch.empty((d.E, d.F, d.H), dtype=torch.float32, device=dev) if dW2 is None else dW2
+    dW13 = torch.empty((d.E, d.H, 2 * d.F), dtype=wdt, device=dev) if dW13 is None else dW13
+    dW2 = torch.empty((d.E, d.F, d.H), dtype=wdt, device=dev) if dW2 is None else dW2
+    _req(dW13, wdt, "dW13")
+    _req(dW2, wdt, "dW2")
     if want_d_gate and d_gate is None:
         d_gate = torch.empty((d.T, d.k), dtype=torch.float32, device=dev)
-    _lib.check(lib().moe_layer_bwd(_ptr(x), _ptr(dOut), _ptr(gate), _ptr(wq), d.T, d.H, d.F, d.E, d.k, grad_elem, _ptr(ws),
+    _lib.check(lib().moe_layer_bwd(_ptr(x), _ptr(dOut), _ptr(gate), _ptr(wq), d.T, d.H, d.F, d.E, d.k, grad_elem,
+                                   wgrad_dtype, _ptr(ws),
                                    ws.numel(), _ptr(dX), _ptr(dW13), _ptr(dW2), _ptr(d_gate), _ptr(dev_status),
                                    _stream(dev)), "moe_layer_bwd")
     return dX, dW13, dW2, d_gate

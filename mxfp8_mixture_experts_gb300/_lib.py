@@ -63,7 +63,7 @@ SIGNATURES = {
     "moe_layer_workspace_size": (_i64, [_i64, _i64, _i64, _i32, _i32]),
     "moe_layer_prep_weights": (_i32, [_p, _p, _i64, _i64, _i32, _p, _i64, _p]),
     "moe_layer_fwd": (_i32, [_p, _p, _p, _p, _p, _i64, _i64, _i64, _i32, _i32, _p, _i64, _p, _p, _p]),
-    "moe_layer_bwd": (_i32, [_p, _p, _p, _p, _i64, _i64, _i64, _i32, _i32, _i32, _p, _i64, _p, _p, _p, _p, _p, _p]),
+    "moe_layer_bwd": (_i32, [_p, _p, _p, _p, _i64, _i64, _i64, _i32, _i32, _i32, _i32, _p, _i64, _p, _p, _p, _p, _p, _p]),
 }
 
 _lib = None

@@ -104,6 +104,6 @@ extern "C" const char *mx_status_string(mx_status s) {
   }
 }
 
-extern "C" int32_t mx_abi_version(void) { return 3; }
+extern "C" int32_t mx_abi_version(void) { return 4; }
 
 extern "C" mx_status mx_check_device(void) { return mxmoe::check_device_cached(); }

@@ -176,11 +176,12 @@ extern "C" mx_status moe_layer_fwd(const void *x, const float *logits, int32_t *
 }
 
 extern "C" mx_status moe_layer_bwd(const void *x, const void *dOut, const float *gate, const void *wq, int64_t T,
-                                   int64_t H, int64_t F, int32_t E, int32_t k, int32_t grad_elem, void *ws,
-                                   int64_t ws_bytes, void *dX, float *dW13, float *dW2, float *d_gate,
-                                   int32_t *dev_status, mx_stream stream) {
+                                   int64_t H, int64_t F, int32_t E, int32_t k, int32_t grad_elem,
+                                   int32_t wgrad_dtype, void *ws, int64_t ws_bytes, void *dX, void *dW13, void *dW2,
+                                   float *d_gate, int32_t *dev_status, mx_stream stream) {
   MX_HOST_CHECK(wq && ws && dW13 && dW2 && (T == 0 || (x && dOut && dX)), MX_ERR_INVALID_ARG);
   MX_HOST_CHECK(grad_elem == MX_ELEM_E4M3 || grad_elem == MX_ELEM_E5M2, MX_ERR_INVALID_ARG);
+  MX_HOST_CHECK(wgrad_dtype == MX_OUT_F32 || wgrad_dtype == MX_OUT_BF16, MX_ERR_INVALID_ARG);
   const int32_t ge = grad_elem, e4 = MX_ELEM_E4M3;
   MX_TRY(check_dims(T, H, F, E, k));
   MX_HOST_CHECK(ws_bytes >= moe_layer_workspace_size(T, H, F, E, k), MX_ERR_WORKSPACE);
@@ -201,7 +202,7 @@ extern "C" mx_status moe_layer_bwd(const void *x, const void *dOut, const float 
   MX_TRY(moe_swiglu_bwd(w.dh, w.ab, R, F, ge, w.dab_rq, w.dab_rs, w.dab_cq, w.dab_cs, w.h_cq, w.h_cs, row_limit,
                         stream));
   // dW2[e] = h^T dY over the expert's tokens -> [F, H]
-  MX_TRY(mx_grouped_gemm(MX_GEMM_WGRAD, w.h_cq, w.h_cs, w.dy_cq, w.dy_cs, w.offsets, E, R, F, H, dW2, MX_OUT_F32,
+  MX_TRY(mx_grouped_gemm(MX_GEMM_WGRAD, w.h_cq, w.h_cs, w.dy_cq, w.dy_cs, w.offsets, E, R, F, H, dW2, wgrad_dtype,
                          e4, ge, dev_status, stream));
   // dxp = dab W13^T : B = W13[e] [H, 2F] quantized along 2F
   MX_TRY(mx_grouped_gemm(MX_GEMM_DGRAD, w.dab_rq, w.dab_rs, v.w13_rq, v.w13_rs, w.offsets, E, R, H, 2 * F, w.dxp,
@@ -211,7 +212,7 @@ extern "C" mx_status moe_layer_bwd(const void *x, const void *dOut, const float 
                           row_limit, stream));
   // dW13[e] = xp^T dab over the expert's tokens -> [H, 2F]
   MX_TRY(mx_grouped_gemm(MX_GEMM_WGRAD, w.xp_cq, w.xp_cs, w.dab_cq, w.dab_cs, w.offsets, E, R, H, 2 * F, dW13,
-                         MX_OUT_F32, e4, ge, dev_status, stream));
+                         wgrad_dtype, e4, ge, dev_status, stream));
   MX_TRY(moe_unpermute(w.dxp, w.dst, nullptr, T, H, k, dX, stream));
   return MX_OK;
 }

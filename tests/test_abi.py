@@ -43,7 +43,7 @@ def test_status_strings(lib):
     for code in range(0, 10):
         s = lib.mx_status_string(code).decode()
         assert s.startswith("MX_")
-    assert lib.mx_abi_version() == 3
+    assert lib.mx_abi_version() == 4
 
 
 def test_size_queries(lib):

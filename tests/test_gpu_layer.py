@@ -456,6 +456,33 @@ def test_layer_is_deterministic():
                            v.view(torch.uint8) if v.dtype != torch.int32 else v)
 
 
+def test_layer_bf16_weight_gradients():
+    """wgrad_dtype = MX_OUT_BF16: the weight gradients are the fp32 ones of
+    the default run rounded once to bf16 (round to nearest even), bit for
+    bit, since both runs accumulate the same products in the same order and
+    only the epilogue rounds; dX and d_gate are unchanged."""
+    import mxfp8_mixture_experts_gb300 as m
+    dev = torch.device("cuda", 0)
+    d = m.MoELayerDims(T=512, H=256, F=512, E=4, k=2)
+    inp = workloads.layer_inputs(workloads.LayerDims(T=d.T, H=d.H, E=d.E, F=d.F, k=d.k), seed=17, device=dev,
+                                 router="logits")
+    W13 = torch.cat([inp["W1"], inp["W3"]], dim=2).contiguous()
+    wq = m.moe_layer_prep_weights(W13, inp["W2"])
+    ws = torch.empty(m.moe_layer_workspace_size(d), dtype=torch.uint8, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    _, _, gate = m.moe_layer_fwd(inp["x"], wq, d, ws, logits=inp["logits"], dev_status=st)
+    f32 = m.moe_layer_bwd(inp["x"], inp["dOut"], gate, wq, d, ws, dev_status=st)
+    f32 = [t.clone() for t in f32]
+    b16 = m.moe_layer_bwd(inp["x"], inp["dOut"], gate, wq, d, ws, dev_status=st, wgrad_dtype=m.MX_OUT_BF16)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert b16[1].dtype == torch.bfloat16 and b16[2].dtype == torch.bfloat16
+    for got, ref, what in ((b16[1], f32[1], "dW13"), (b16[2], f32[2], "dW2")):
+        assert torch.equal(got.view(torch.int16), ref.to(torch.bfloat16).view(torch.int16)), what
+    assert torch.equal(b16[0].view(torch.int16), f32[0].view(torch.int16))
+    assert torch.equal(b16[3], f32[3])
+
+
 def test_layer_replays_from_a_cuda_graph():
     """The layer API makes no host synchronisation and keeps the group sizes
     on the device, so weight prep, forward and backward can be captured into
